@@ -1,0 +1,20 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built libpagedattn")
+
+
+@pytest.fixture(scope="session")
+def ora():
+    import oracle
+    from oracle import build as obuild
+    obuild.build()
+    return oracle.Oracle()
