@@ -1,0 +1,223 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn, the paged KV-cache attention hot path
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow three web pages on vLLM / PagedAttention:
+ *  [ATT]  "Configuring vLLM and PagedAttention for High Throughput Enterprise
+ *         LLM Serving", section "Architectural Foundations: PagedAttention &
+ *         Virtual Memory": KV cache split into blocks of B tokens drawn from a
+ *         global physical page pool; a block table maps logical blocks to
+ *         physical pages; attention weights
+ *         A_ij = exp(q_i.k_j/sqrt(d)) / sum_m exp(q_i.k_m/sqrt(d)); the kernel
+ *         fetches k_j from page BlockTable[j / B].
+ *  [PHASE] same page, "Memory Bottlenecks in Autoregressive LLM Inference":
+ *         prefill writes K/V for every position; decode reads the whole cache
+ *         from HBM for each new token (bandwidth bound).
+ *  [CHUNK] same page, "High-Throughput Batching: Continuous Batching & Chunked
+ *         Prefill": prompts split into 512/1024-token chunks that ride along
+ *         with decode iterations; pages returned to the free pool on <eos>.
+ *  [SHARE] same page, "Zero-Copy Prefix Caching & Shared Sampling", and
+ *         "vLLM Guide: High-Throughput Multi-GPU LLM Serving with
+ *         PagedAttention", section "What Is PagedAttention?": blocks allocated
+ *         on demand; shared prefixes point at the same physical pages, with
+ *         copy-on-write.
+ *  [TABLE] "vLLM High-Performance Inference Engine: PagedAttention Principles
+ *         and Deployment Guide", section "PagedAttention Architecture Deep
+ *         Dive": block table with per-page ref_count.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Pools: k_pool and v_pool are bf16 [num_blocks][num_kv_heads][block_size]
+ *    [head_dim], row-major, one tensor per layer.  One (block, kv head) is a
+ *    contiguous block_size*head_dim*2-byte run.
+ *  - Block tables: int32 [num_seqs][max_blocks_per_seq]; entry i of row s is the
+ *    physical block holding tokens i*B .. i*B+B-1 of sequence s.  Token j of a
+ *    sequence sits in block table[s][j / B] at offset j % B.
+ *  - Slots: int64, slot = block * block_size + offset; slot < 0 = no write.
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - Every device pointer is owned by the caller; the library allocates no
+ *    device memory.  Pointers marked "device" must be device memory of the
+ *    current device; bf16 tensors must be 16-byte aligned.
+ *  - Every GPU call is asynchronous and ordered on `stream` (a cudaStream_t
+ *    passed as void*, NULL = legacy default stream).  The return value reports
+ *    host-side validation and launch errors only.
+ *  - Errors found on the device (bad context length, page or slot id) are
+ *    or-ed into *err_flag (device int32, may be NULL) as PA_DEVERR_* bits; the
+ *    offending work is skipped (attention rows are written as zeros), nothing
+ *    traps.  The flag is never cleared by the library.
+ *  - Thread safety: calls are re-entrant; the only global state is a
+ *    per-device cache of SM count and of the driver's tensor-map encoder.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,     /* bad argument (null pointer, size, alignment) */
+  PA_ERR_UNSUPPORTED = -2, /* valid but not built (head_dim, block_size, GQA group) */
+  PA_ERR_CUDA = -3,        /* CUDA runtime / launch error */
+  PA_ERR_OOM = -4,         /* block manager: no free block */
+  PA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
+  PA_ERR_STATE = -6        /* block manager: unknown / duplicate sequence id,
+                              reference count underflow */
+} pa_status;
+
+/* Device error bits or-ed into *err_flag. */
+#define PA_DEVERR_CTX 1      /* context_len <= 0, > max_blocks_per_seq*B or > max_context_len */
+#define PA_DEVERR_PAGE 2     /* block-table entry outside [0, num_blocks) */
+#define PA_DEVERR_SLOT 4     /* slot >= num_blocks * block_size */
+#define PA_DEVERR_PAIR 8     /* copy pair with a block id outside [0, num_blocks) */
+#define PA_DEVERR_TIMEOUT 16 /* an on-chip wait gave up (bounded waits only) */
+
+/* Shape of one paged-attention call.  head_dim in {64, 128}; block_size in
+ * {16, 32}; num_q_heads a multiple of num_kv_heads with a group of at most 16.
+ * max_context_len bounds every context_lens[s] of the call (it sizes the
+ * grid); scale multiplies q.k (1/sqrt(head_dim) per [ATT]). */
+typedef struct pa_decode_desc {
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int num_blocks;
+  int max_blocks_per_seq;
+  int max_context_len;
+  float scale;
+} pa_decode_desc;
+
+/* Library version string. */
+const char *pa_version(void);
+
+/* Human-readable name of a pa_status value. */
+const char *pa_status_string(int status);
+
+/* Bytes of device workspace pa_paged_attention_decode needs for `desc` on the
+ * current device (0 when no context is split).  The workspace holds split-K
+ * partial results and one int32 arrival counter per (sequence, kv head): it
+ * must be zero-filled once before its first use; every completed call leaves
+ * the counters zero again.  Returns 0 for an invalid desc. */
+size_t pa_decode_workspace_bytes(const pa_decode_desc *desc);
+
+/* Paged decode attention [ATT][PHASE]: for every sequence s and query head h,
+ *   out[s][h] = sum_j softmax_j(scale * q[s][h] . k_j) v_j,  j = 0..ctx_s-1,
+ * with k_j, v_j read from block block_tables[s][j / B], offset j % B of kv head
+ * h / G.  ctx_s = context_lens[s] includes the token generated this step, whose
+ * K/V must already be in the cache (pa_reshape_and_cache).  Softmax in fp32
+ * with a running max; bf16 output.
+ *   q            device bf16 [num_seqs][num_q_heads][head_dim]
+ *   k_pool,v_pool device bf16 pools (layout above)
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens device int32 [num_seqs]
+ *   out          device bf16 [num_seqs][num_q_heads][head_dim]
+ *   workspace    device, >= pa_decode_workspace_bytes(desc) (may be NULL when
+ *                that is 0), zero-filled before first use, not shared by calls
+ *                that may overlap on the GPU
+ *   err_flag     device int32 or NULL
+ * Returns PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or
+ * PA_ERR_CUDA.  num_seqs == 0 launches nothing. */
+int pa_paged_attention_decode(const pa_decode_desc *desc, const void *q, const void *k_pool,
+                              const void *v_pool, const int32_t *block_tables,
+                              const int32_t *context_lens, void *out, void *workspace,
+                              size_t workspace_bytes, int32_t *err_flag, void *stream);
+
+/* Causal chunked-prefill attention [PHASE][CHUNK] on the tensor cores.
+ * Chunk r (r < desc->num_seqs) has C_r = cu_q[r+1] - cu_q[r] query tokens and
+ * context ctx_r = context_lens[r] that INCLUDES the chunk (its K/V must already
+ * be cached).  Query row i of chunk r sits at position ctx_r - C_r + i and
+ * attends keys 0..ctx_r - C_r + i of the chunk's block-table row.
+ *   q       device bf16 [cu_q[R]][num_q_heads][head_dim]
+ *   cu_q    device int32 [R + 1], cu_q[0] = 0, non-decreasing
+ *   max_q_len  bound on every C_r (sizes the grid)
+ *   out     device bf16 [cu_q[R]][num_q_heads][head_dim]
+ * head_dim must be 128.  Other arguments as in pa_paged_attention_decode. */
+int pa_paged_attention_prefill_chunk(const pa_decode_desc *desc, const void *q,
+                                     const int32_t *cu_q, int max_q_len, const void *k_pool,
+                                     const void *v_pool, const int32_t *block_tables,
+                                     const int32_t *context_lens, void *out, int32_t *err_flag,
+                                     void *stream);
+
+/* Writes the K/V of num_tokens new tokens into their cache slots [PHASE][SHARE]:
+ *   k_pool[slot / B][h][slot % B][:] = k[t][h][:]  (same for v), for t in order.
+ * Bit-exact copy.  slot < 0: token skipped.  slot >= num_blocks*B: skipped and
+ * PA_DEVERR_SLOT set.  Two tokens with the same slot: unspecified which wins.
+ *   k, v          device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping  device int64 [num_tokens] */
+int pa_reshape_and_cache(const void *k, const void *v, void *k_pool, void *v_pool,
+                         const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, int32_t *err_flag,
+                         void *stream);
+
+/* Copy-on-write page copies [SHARE][TABLE]: for every layer l and pair i,
+ *   block pairs[i][1] of k_pools[l] and v_pools[l] := block pairs[i][0].
+ * A block is block_bytes = num_kv_heads*block_size*head_dim*2 contiguous bytes
+ * (a multiple of 16).  Bit-exact.  Destinations must be distinct and must not
+ * also be sources within one call (the copies run concurrently).
+ *   k_pools, v_pools  HOST arrays of num_layers device pointers (1..256 layers)
+ *   block_pairs       device int64 [num_pairs][2] (src, dst)
+ * A pair with an id outside [0, num_blocks) is skipped with PA_DEVERR_PAIR. */
+int pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_layers,
+                   const int64_t *block_pairs, int num_pairs, int num_blocks, size_t block_bytes,
+                   int32_t *err_flag, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Host block manager [TABLE][SHARE][CHUNK] (plain C++, no GPU): a free list
+ * of num_blocks physical blocks of block_size tokens, per-sequence block
+ * tables, per-block reference counts.  Blocks are allocated on demand (a
+ * sequence of n tokens holds ceil(n / B) blocks), shared by fork, copied on
+ * write when a sharer appends into a block with ref_count > 1, and returned to
+ * the free list when the last reference is dropped.  The free list is LIFO;
+ * initially blocks are handed out in increasing id order.  Not thread safe.
+ * ------------------------------------------------------------------------ */
+typedef struct pa_bm pa_bm;
+
+/* NULL on bad arguments (num_blocks <= 0 or block_size <= 0) or no memory. */
+pa_bm *pa_bm_create(int num_blocks, int block_size);
+void pa_bm_destroy(pa_bm *bm);
+
+/* New sequence seq_id (>= 0, unused) holding num_tokens (>= 0) tokens:
+ * allocates ceil(num_tokens / B) blocks.  PA_ERR_OOM leaves no trace. */
+int pa_bm_add_seq(pa_bm *bm, int seq_id, int num_tokens);
+
+/* child shares every block of parent (ref_count + 1 each), same length. */
+int pa_bm_fork(pa_bm *bm, int parent_id, int child_id);
+
+/* Appends one token to seq_id.  *slot_out gets its slot.  If the token starts
+ * a new block, a free block is taken.  If it lands in a block with ref_count >
+ * 1, a fresh block is taken, cow_pair_out = {old, new} is returned for
+ * pa_copy_blocks, and the old block's ref_count drops by one; otherwise
+ * cow_pair_out = {-1, -1}.  PA_ERR_OOM leaves the sequence unchanged. */
+int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]);
+
+/* Drops seq_id: every block's ref_count - 1, blocks reaching 0 go back to the
+ * free list (the <eos> path of [CHUNK]). */
+int pa_bm_free_seq(pa_bm *bm, int seq_id);
+
+/* Copies seq_id's block table into out[0..cap-1]; *n = its length.  Returns
+ * PA_ERR_INVALID if cap < *n (nothing copied beyond cap). */
+int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n);
+
+/* Tokens held by seq_id, or -1 if unknown. */
+int pa_bm_seq_len(const pa_bm *bm, int seq_id);
+
+/* Reference count of a block (0 = free), -1 if out of range. */
+int pa_bm_ref_count(const pa_bm *bm, int block);
+
+/* Number of free blocks. */
+int pa_bm_num_free(const pa_bm *bm);
+
+/* Unused token slots in allocated blocks over all live sequences (each shared
+ * block counted once), i.e. internal fragmentation in tokens. */
+int64_t pa_bm_wasted_slots(const pa_bm *bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,313 @@
+"""ctypes binding of libpagedattn (``include/pagedattn.h``).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  torch supplies device memory and streams.  If the shared
+library is missing the calls raise immediately -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+from . import build as _build
+
+_c = ctypes
+_P = _c.c_void_p
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OOM, PA_ERR_WORKSPACE, PA_ERR_STATE = (
+    0, -1, -2, -3, -4, -5, -6)
+DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+# Every symbol include/pagedattn.h declares.
+EXPORTS = (
+    "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
+    "pa_paged_attention_prefill_chunk", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
+    "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
+)
+
+
+class DecodeDesc(_c.Structure):
+    _fields_ = [("num_seqs", _c.c_int), ("num_q_heads", _c.c_int), ("num_kv_heads", _c.c_int),
+                ("head_dim", _c.c_int), ("block_size", _c.c_int), ("num_blocks", _c.c_int),
+                ("max_blocks_per_seq", _c.c_int), ("max_context_len", _c.c_int), ("scale", _c.c_float)]
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_LIB = None
+_LOCK = threading.Lock()
+
+
+def load(path: Optional[str] = None):
+    """Loads the shared library (raises if it has not been built)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is not None and path is None:
+            return _LIB
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"libpagedattn is not built ({p} missing); run "
+                               "`python -m paged_kv_cache_262_gb300.build`")
+        lib = _c.CDLL(p)
+        i, sz, i64 = _c.c_int, _c.c_size_t, _c.c_int64
+        lib.pa_version.restype = _c.c_char_p
+        lib.pa_version.argtypes = []
+        lib.pa_status_string.restype = _c.c_char_p
+        lib.pa_status_string.argtypes = [i]
+        lib.pa_decode_workspace_bytes.restype = sz
+        lib.pa_decode_workspace_bytes.argtypes = [_c.POINTER(DecodeDesc)]
+        lib.pa_paged_attention_decode.restype = i
+        lib.pa_paged_attention_decode.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, sz,
+                                                  _P, _P]
+        lib.pa_paged_attention_prefill_chunk.restype = i
+        lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, _P, _P, _P, _P,
+                                                         _P, _P, _P]
+        lib.pa_reshape_and_cache.restype = i
+        lib.pa_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, i, i, i, i, i, _P, _P]
+        lib.pa_copy_blocks.restype = i
+        lib.pa_copy_blocks.argtypes = [_c.POINTER(_P), _c.POINTER(_P), i, _P, i, i, sz, _P, _P]
+        lib.pa_bm_create.restype = _P
+        lib.pa_bm_create.argtypes = [i, i]
+        lib.pa_bm_destroy.restype = None
+        lib.pa_bm_destroy.argtypes = [_P]
+        lib.pa_bm_add_seq.restype = i
+        lib.pa_bm_add_seq.argtypes = [_P, i, i]
+        lib.pa_bm_fork.restype = i
+        lib.pa_bm_fork.argtypes = [_P, i, i]
+        lib.pa_bm_append.restype = i
+        lib.pa_bm_append.argtypes = [_P, i, _c.POINTER(i64), _c.POINTER(i64)]
+        lib.pa_bm_free_seq.restype = i
+        lib.pa_bm_free_seq.argtypes = [_P, i]
+        lib.pa_bm_block_table.restype = i
+        lib.pa_bm_block_table.argtypes = [_P, i, _c.POINTER(_c.c_int32), i, _c.POINTER(i)]
+        lib.pa_bm_seq_len.restype = i
+        lib.pa_bm_seq_len.argtypes = [_P, i]
+        lib.pa_bm_ref_count.restype = i
+        lib.pa_bm_ref_count.argtypes = [_P, i]
+        lib.pa_bm_num_free.restype = i
+        lib.pa_bm_num_free.argtypes = [_P]
+        lib.pa_bm_wasted_slots.restype = i64
+        lib.pa_bm_wasted_slots.argtypes = [_P]
+        if path is None:
+            _LIB = lib
+        return lib
+
+
+def status_string(st: int) -> str:
+    try:
+        return load().pa_status_string(int(st)).decode()
+    except Exception:
+        return "unknown"
+
+
+def version() -> str:
+    return load().pa_version().decode()
+
+
+def _check(st: int, what: str):
+    if st != PA_OK:
+        raise PaError(st, what)
+
+
+# --------------------------------------------------------------- tensor helpers
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _need(t, dtype, name, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def make_desc(q, k_pool, block_tables, *, num_seqs=None, scale=None, max_context_len=None) -> DecodeDesc:
+    import math
+    nblk, hkv, bs, d = k_pool.shape
+    return DecodeDesc(int(q.shape[0] if num_seqs is None else num_seqs), int(q.shape[1]), int(hkv), int(d),
+                      int(bs), int(nblk), int(block_tables.shape[1]),
+                      int(max_context_len if max_context_len is not None else block_tables.shape[1] * bs),
+                      float(scale if scale is not None else 1.0 / math.sqrt(d)))
+
+
+def decode_workspace_bytes(desc: DecodeDesc) -> int:
+    return int(load().pa_decode_workspace_bytes(_c.byref(desc)))
+
+
+_WS = {}
+
+
+def decode_workspace(desc: DecodeDesc, device):
+    """A zero-filled workspace of the size the call needs, cached per device
+    and reused (every call leaves its counters zero again)."""
+    import torch
+    need = decode_workspace_bytes(desc)
+    if need == 0:
+        return None
+    key = torch.device(device).index
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+# --------------------------------------------------------------- the four calls
+def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=None, *, scale=None,
+                           max_context_len=None, workspace=None, err_flag=None, stream=None):
+    """out[s][h] = softmax(scale q k^T) v over the paged context (see pagedattn.h)."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
+    if workspace is None:
+        workspace = decode_workspace(desc, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_paged_attention_decode(_c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                          _ptr(block_tables), _ptr(context_lens), _ptr(out),
+                                          _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_paged_attention_decode")
+    return out
+
+
+def paged_attention_prefill_chunk(q, cu_q, k_pool, v_pool, block_tables, context_lens, out=None, *,
+                                  max_q_len, scale=None, max_context_len=None, err_flag=None, stream=None):
+    """Causal chunked-prefill attention (see pagedattn.h)."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    desc = make_desc(q, k_pool, block_tables, num_seqs=context_lens.shape[0], scale=scale,
+                     max_context_len=max_context_len)
+    st = load().pa_paged_attention_prefill_chunk(_c.byref(desc), _ptr(q), _ptr(cu_q), int(max_q_len),
+                                                 _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                                 _ptr(context_lens), _ptr(out), _ptr(err_flag),
+                                                 _stream_ptr(stream))
+    _check(st, "pa_paged_attention_prefill_chunk")
+    return out
+
+
+def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, *, err_flag=None, stream=None):
+    """k_pool[slot // B][h][slot % B] = k[t][h] (and v) for every token t."""
+    import torch
+    _need(k, torch.bfloat16, "k", 3)
+    _need(v, torch.bfloat16, "v", 3)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    nblk, hkv, bs, d = k_pool.shape
+    st = load().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping),
+                                     int(slot_mapping.shape[0]), int(hkv), int(d), int(bs), int(nblk),
+                                     _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def copy_blocks(k_pools: Sequence, v_pools: Sequence, block_pairs, *, err_flag=None, stream=None):
+    """Block pairs[i][1] := block pairs[i][0] in every layer's K and V pool."""
+    import torch
+    L = len(k_pools)
+    if L != len(v_pools) or L == 0:
+        raise ValueError("k_pools and v_pools must be non-empty and of equal length")
+    for t in list(k_pools) + list(v_pools):
+        _need(t, torch.bfloat16, "pool", 4)
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    nblk = k_pools[0].shape[0]
+    blk_bytes = k_pools[0][0].numel() * 2
+    kp = (_P * L)(*[t.data_ptr() for t in k_pools])
+    vp = (_P * L)(*[t.data_ptr() for t in v_pools])
+    st = load().pa_copy_blocks(kp, vp, L, _ptr(block_pairs), int(block_pairs.shape[0]), int(nblk),
+                               int(blk_bytes), _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_copy_blocks")
+
+
+# --------------------------------------------------------------- block manager
+class BlockManager:
+    """Host block manager (free list, block tables, ref counts, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        self._h = self._lib.pa_bm_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise PaError(PA_ERR_INVALID, "pa_bm_create")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq_id: int, num_tokens: int):
+        _check(self._lib.pa_bm_add_seq(self._h, int(seq_id), int(num_tokens)), "pa_bm_add_seq")
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")
+
+    def append(self, seq_id: int):
+        """Returns (slot, cow_pair or None)."""
+        slot = _c.c_int64()
+        pair = (_c.c_int64 * 2)()
+        _check(self._lib.pa_bm_append(self._h, int(seq_id), _c.byref(slot), pair), "pa_bm_append")
+        return slot.value, (None if pair[0] < 0 else (pair[0], pair[1]))
+
+    def free_seq(self, seq_id: int):
+        _check(self._lib.pa_bm_free_seq(self._h, int(seq_id)), "pa_bm_free_seq")
+
+    def block_table(self, seq_id: int):
+        n = _c.c_int()
+        st = self._lib.pa_bm_block_table(self._h, int(seq_id), None, 0, _c.byref(n))
+        if st not in (PA_OK, PA_ERR_INVALID):
+            raise PaError(st, "pa_bm_block_table")
+        buf = (_c.c_int32 * max(n.value, 1))()
+        _check(self._lib.pa_bm_block_table(self._h, int(seq_id), buf, n.value, _c.byref(n)),
+               "pa_bm_block_table")
+        return list(buf[: n.value])
+
+    def seq_len(self, seq_id: int) -> int:
+        return self._lib.pa_bm_seq_len(self._h, int(seq_id))
+
+    def ref_count(self, block: int) -> int:
+        return self._lib.pa_bm_ref_count(self._h, int(block))
+
+    def num_free(self) -> int:
+        return self._lib.pa_bm_num_free(self._h)
+
+    def wasted_slots(self) -> int:
+        return self._lib.pa_bm_wasted_slots(self._h)

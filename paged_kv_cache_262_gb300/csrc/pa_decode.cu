@@ -1,0 +1,452 @@
+// Paged decode attention for sm_103a.
+//
+// Computes, for every sequence s and query head h, the attention of
+// "Configuring vLLM and PagedAttention for High Throughput Enterprise LLM
+// Serving" ("Architectural Foundations: PagedAttention & Virtual Memory"):
+//   out = sum_j softmax_j(scale * q.k_j) v_j,  k_j, v_j in block BlockTable[j / B]
+// over the whole cached context -- the bandwidth-bound decode phase of
+// "Memory Bottlenecks in Autoregressive LLM Inference" on the same page.
+//
+// Design (one CTA per (context part, kv head, sequence), 4 warps):
+//  * The part's block-table entries are staged once in shared memory.
+//  * Each warp owns every 4th page of the part and a private ring of NST
+//    shared-memory slots.  Lane 0 gathers a page's K and V runs (B rows x D
+//    bf16 each, one (block, kv head) run is contiguous in the pool) with 2-D TMA
+//    loads (128-byte swizzle, L2 evict-first) that complete on the slot's
+//    mbarrier.  No warp ever waits for another warp while streaming.
+//  * QK^T and PV are warp MMAs (m16n8k16, bf16 in, fp32 accumulate): tokens are
+//    the M side of S^T = K Q^T (the G query heads of the kv head are the N side,
+//    so one K page read serves the whole GQA group), and d is the M side of
+//    O^T = V^T P^T.  The probabilities move from the S^T accumulator to the PV
+//    operand with movmatrix (no shared-memory round trip).
+//  * Online softmax in fp32 (running max and sum, base-2 exponent).  The
+//    probabilities are rounded to bf16 once and the same rounded values feed
+//    both the PV product and the running sum.
+//  * Warps are merged in shared memory at the end; a context cut into several
+//    parts writes (o/l, m, l) per part to the workspace, and the last CTA of a
+//    (sequence, kv head) to arrive (atomic counter, no waiting) merges the
+//    parts in part order -- deterministic, one launch.
+//  * Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+#include "pagedattn.h"
+
+namespace pa {
+namespace {
+
+struct DecodeArgs {
+  const __nv_bfloat16 *q;
+  const int32_t *bt;
+  const int32_t *ctx;
+  __nv_bfloat16 *out;
+  float *ws_o;
+  float *ws_ml;
+  int32_t *ws_cnt;
+  int32_t *err;
+  int S, Hq, Hkv, G, num_blocks, max_blocks, max_ctx, part_pages, max_parts;
+  float scale_log2;
+};
+
+template <int D, int B, int NW, int NST>
+struct DecodeSmem {
+  static constexpr int kHalves = D / 64;           // 64-column TMA boxes per row
+  static constexpr int kBoxBytes = B * 128;        // B rows x 128 bytes
+  static constexpr int kPageBytes = kHalves * kBoxBytes;
+  static constexpr int kSlotBytes = 2 * kPageBytes;  // K then V
+  static constexpr int kRingBytes = NW * NST * kSlotBytes;
+  // After streaming, the ring is reused for the merge buffers (floats):
+  // red_o [NW][16][D], red_m [NW][16], red_l [NW][16], wts [kMaxParts][16].
+  static constexpr int kRedBytes = (NW * 16 * D + 2 * NW * 16 + kMaxParts * 16) * 4;
+  static constexpr int kRegion0 = kRingBytes > kRedBytes ? kRingBytes : kRedBytes;
+  static constexpr int kBarOff = (kRegion0 + 1023) & ~1023;
+  static constexpr int kTblOff = kBarOff + NW * NST * 8;
+  static constexpr int kMiscOff = kTblOff + kMaxPartPages * 4;
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // base re-aligned to 1024 in the kernel
+};
+
+template <int D, int B, int NT, int NW, int NST>
+__global__ void __launch_bounds__(NW * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeArgs a) {
+  using L = DecodeSmem<D, B, NW, NST>;
+  constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
+  constexpr int MT = B / 16;  // 16-token tiles per page
+  constexpr int DT = D / 16;  // 16-row d tiles of O^T = V^T P^T
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
+  int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kTblOff);
+  int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
+
+  const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.G;
+  const int ctx = __ldg(a.ctx + s);
+  const bool bad = ctx <= 0 || ctx > a.max_blocks * B || ctx > a.max_ctx;
+  const int npages = bad ? 0 : (ctx + B - 1) / B;
+  const int nparts = bad ? 1 : (npages + a.part_pages - 1) / a.part_pages;
+  if (part >= nparts) return;
+  __nv_bfloat16 *out_base = a.out + ((size_t)s * a.Hq + (size_t)kvh * G) * D;
+  if (bad) {
+    for (int i = tid; i < G * D; i += NW * 32) out_base[i] = __float2bfloat16(0.f);
+    if (tid == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
+    return;
+  }
+
+  // ---- stage this part's block-table entries; init this warp's barriers
+  const int p0 = part * a.part_pages;
+  const int np = min(npages - p0, a.part_pages);
+  const int32_t *bt_row = a.bt + (size_t)s * a.max_blocks + p0;
+  for (int i = tid; i < np; i += NW * 32) {
+    int pg = __ldg(bt_row + i);
+    if (pg < 0 || pg >= a.num_blocks) {
+      if (a.err) atomicOr(a.err, PA_DEVERR_PAGE);
+      pg = -1;
+    }
+    tbl[i] = pg;
+  }
+  uint64_t *my_bars = bars + warp * NST;
+  if (lane == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(&my_bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  uint8_t *ring = smem + warp * NST * L::kSlotBytes;
+  const int nmine = np > warp ? (np - warp + NW - 1) / NW : 0;
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int i) {  // lane 0: gather local page i of this warp into its slot
+    const int pg = tbl[warp + i * NW];
+    uint64_t *bar = &my_bars[i % NST];
+    uint8_t *slot = ring + (i % NST) * L::kSlotBytes;
+    if (pg < 0) {
+      mbar_arrive(bar);  // nothing to load; keep the phase sequence intact
+      return;
+    }
+    mbar_arrive_expect_tx(bar, L::kSlotBytes);
+    const int row = (pg * a.Hkv + kvh) * B;
+#pragma unroll
+    for (int h = 0; h < L::kHalves; ++h)
+      tma_load_2d_hint(slot + h * L::kBoxBytes, &tmK, h * 64, row, bar, pol);
+#pragma unroll
+    for (int h = 0; h < L::kHalves; ++h)
+      tma_load_2d_hint(slot + L::kPageBytes + h * L::kBoxBytes, &tmV, h * 64, row, bar, pol);
+  };
+  if (lane == 0)
+    for (int i = 0; i < NST && i < nmine; ++i) issue(i);
+
+  // ---- Q^T fragments (MMA B operand): head 8nt + lane/4, d pairs
+  uint32_t qf[NT][KS][2];
+  const __nv_bfloat16 *qb = a.q + ((size_t)s * a.Hq + (size_t)kvh * G) * D;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = nt * 8 + (lane >> 2);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int d0 = kk * 16 + 2 * (lane & 3);
+      if (g < G) {
+        qf[nt][kk][0] = __ldg(reinterpret_cast<const uint32_t *>(qb + (size_t)g * D + d0));
+        qf[nt][kk][1] = __ldg(reinterpret_cast<const uint32_t *>(qb + (size_t)g * D + d0 + 8));
+      } else {
+        qf[nt][kk][0] = qf[nt][kk][1] = 0u;
+      }
+    }
+  }
+
+  // Running state.  Lane holds heads 8nt + 2(lane%4) + e (e = 0, 1) and, in o,
+  // the O^T rows d = 16dt + lane/4 (+8).
+  float m_run[NT][2], l_run[NT][2], o[NT][DT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) o[nt][dt][0] = o[nt][dt][1] = o[nt][dt][2] = o[nt][dt][3] = 0.f;
+  }
+
+  bool timed_out = false;
+  int i = 0;
+  for (; i < nmine; ++i) {
+    const int stg = i % NST;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&my_bars[stg], (uint32_t)((i / NST) & 1)));
+    if (!ok) {
+      timed_out = true;
+      break;
+    }
+    const int lp = warp + i * NW;
+    if (tbl[lp] >= 0) {
+      const uint32_t kb = smem_u32(ring + stg * L::kSlotBytes);
+      const uint32_t vb = kb + L::kPageBytes;
+      const int tok0 = (p0 + lp) * B;
+
+      // S^T[token][head] = K Q^T
+      float sc[MT][NT][4];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int c = 2 * kk + (lane >> 4);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          uint32_t af[4];
+          ldsm_x4(kb + (c >> 3) * L::kBoxBytes + sw128(r, c & 7), af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(sc[mt][nt], af, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+      }
+
+      // online softmax: mask tokens past the context, page max, rescale
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float t0 = -INFINITY, t1 = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          const int j = tok0 + mt * 16 + (lane >> 2);
+          const bool v0 = j < ctx, v1 = j + 8 < ctx;
+          sc[mt][nt][0] = v0 ? sc[mt][nt][0] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][1] = v0 ? sc[mt][nt][1] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][2] = v1 ? sc[mt][nt][2] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][3] = v1 ? sc[mt][nt][3] * a.scale_log2 : -INFINITY;
+          t0 = fmaxf(t0, fmaxf(sc[mt][nt][0], sc[mt][nt][2]));
+          t1 = fmaxf(t1, fmaxf(sc[mt][nt][1], sc[mt][nt][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+        }
+        const float mn0 = fmaxf(m_run[nt][0], t0), mn1 = fmaxf(m_run[nt][1], t1);
+        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          o[nt][dt][0] *= al0;
+          o[nt][dt][1] *= al1;
+          o[nt][dt][2] *= al0;
+          o[nt][dt][3] *= al1;
+        }
+      }
+
+      // O^T[d][head] += V^T P^T, one 16-token k-tile at a time
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint32_t lo = pack_bf16(exp2f(sc[mt][nt][0] - m_run[nt][0]),
+                                        exp2f(sc[mt][nt][1] - m_run[nt][1]));
+          const uint32_t hi = pack_bf16(exp2f(sc[mt][nt][2] - m_run[nt][0]),
+                                        exp2f(sc[mt][nt][3] - m_run[nt][1]));
+          l_run[nt][0] += bf16_lo(lo) + bf16_lo(hi);
+          l_run[nt][1] += bf16_hi(lo) + bf16_hi(hi);
+          pb[nt][0] = movmatrix_t(lo);
+          pb[nt][1] = movmatrix_t(hi);
+        }
+#pragma unroll
+        for (int dt = 0; dt < DT; ++dt) {
+          const int r = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+          const int c = 2 * dt + ((lane >> 3) & 1);
+          uint32_t af[4];
+          ldsm_x4_t(vb + (c >> 3) * L::kBoxBytes + sw128(r, c & 7), af);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_16816(o[nt][dt], af, pb[nt][0], pb[nt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && i + NST < nmine) {
+      fence_proxy_async_smem();
+      issue(i + NST);
+    }
+  }
+  if (timed_out) {
+    if (lane == 0 && a.err) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+    for (int k = i; k < nmine && k < i + NST; ++k) mbar_wait(&my_bars[k % NST], (uint32_t)((k / NST) & 1));
+  }
+
+  // ---- per-warp sums across the lanes that share a head
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) l_run[nt][e] += __shfl_xor_sync(0xffffffffu, l_run[nt][e], off);
+
+  // ---- merge the warps (ring memory is reused)
+  __syncthreads();
+  float *red_o = reinterpret_cast<float *>(smem);
+  float *red_m = red_o + NW * 16 * D;
+  float *red_l = red_m + NW * 16;
+  float *wts = red_l + NW * 16;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int g = nt * 8 + 2 * (lane & 3);
+#pragma unroll
+    for (int dt = 0; dt < DT; ++dt) {
+      const int d = dt * 16 + (lane >> 2);
+      red_o[(warp * 16 + g) * D + d] = o[nt][dt][0];
+      red_o[(warp * 16 + g + 1) * D + d] = o[nt][dt][1];
+      red_o[(warp * 16 + g) * D + d + 8] = o[nt][dt][2];
+      red_o[(warp * 16 + g + 1) * D + d + 8] = o[nt][dt][3];
+    }
+    if (lane < 4) {
+      red_m[warp * 16 + g] = m_run[nt][0];
+      red_m[warp * 16 + g + 1] = m_run[nt][1];
+      red_l[warp * 16 + g] = l_run[nt][0];
+      red_l[warp * 16 + g + 1] = l_run[nt][1];
+    }
+  }
+  __syncthreads();
+
+  const bool split = nparts > 1;
+  const size_t unit = (size_t)s * a.Hkv + kvh;
+  for (int idx = tid; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, red_m[w * 16 + g]);
+    float l = 0.f, acc = 0.f;
+    if (mx != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float f = exp2f(red_m[w * 16 + g] - mx);
+        l += red_l[w * 16 + g] * f;
+        acc += red_o[(w * 16 + g) * D + d] * f;
+      }
+    }
+    const float val = l > 0.f ? acc / l : 0.f;
+    if (!split) {
+      out_base[idx] = __float2bfloat16(val);
+    } else {
+      const size_t u = (unit * a.max_parts + part) * G + g;
+      a.ws_o[u * D + d] = val;
+      if (d == 0) {
+        a.ws_ml[2 * u] = mx;
+        a.ws_ml[2 * u + 1] = l;
+      }
+    }
+  }
+  if (!split) return;
+
+  // ---- split-K: the last part of this (sequence, kv head) merges all parts
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) misc[0] = (atomicAdd(a.ws_cnt + unit, 1) == nparts - 1);
+  __syncthreads();
+  if (!misc[0]) return;
+  __threadfence();
+  const size_t ubase = unit * a.max_parts;
+  if (tid < G) {
+    const int g = tid;
+    float M = -INFINITY;
+    for (int p = 0; p < nparts; ++p) {
+      const float l = __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g) + 1);
+      if (l > 0.f) M = fmaxf(M, __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g)));
+    }
+    float den = 0.f;
+    for (int p = 0; p < nparts; ++p) {
+      const float m = __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g));
+      const float l = __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g) + 1);
+      const float w = l > 0.f ? l * exp2f(m - M) : 0.f;
+      wts[p * 16 + g] = w;
+      den += w;
+    }
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    for (int p = 0; p < nparts; ++p) wts[p * 16 + g] *= inv;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < G * D; idx += NW * 32) {
+    const int g = idx / D, d = idx - g * D;
+    float acc = 0.f;
+    for (int p = 0; p < nparts; ++p) acc += wts[p * 16 + g] * __ldcg(a.ws_o + ((ubase + p) * G + g) * D + d);
+    out_base[idx] = __float2bfloat16(acc);
+  }
+  if (tid == 0) a.ws_cnt[unit] = 0;
+}
+
+template <int D, int B, int NT>
+int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
+                  cudaStream_t st) {
+  constexpr int NW = 4;
+  constexpr int NST = (B == 16) ? 3 : 2;
+  using L = DecodeSmem<D, B, NW, NST>;
+  static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
+  auto kern = decode_kernel<D, B, NT, NW, NST>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  kern<<<grid, NW * 32, L::kAlloc, st>>>(tk, tv, a);
+  return launch_status(cudaGetLastError());
+}
+
+template <int D, int B>
+int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
+                cudaStream_t st) {
+  return G <= 8 ? launch_decode<D, B, 1>(tk, tv, a, grid, st) : launch_decode<D, B, 2>(tk, tv, a, grid, st);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q, const void *k_pool,
+                                         const void *v_pool, const int32_t *block_tables,
+                                         const int32_t *context_lens, void *out, void *workspace,
+                                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  using namespace pa;
+  int st = validate_decode_desc(d);
+  if (st != PA_OK) return st;
+  if (d->num_seqs == 0) return PA_OK;
+  if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+    return PA_ERR_INVALID;
+  if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  const int sms = current_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  const DecodePlan plan = make_decode_plan(d, sms);
+  if (plan.total() > 0 && (!workspace || workspace_bytes < plan.total() || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
+  CUtensorMap tk, tv;
+  if (!encode_2d_bf16(&tk, k_pool, rows, d->head_dim, d->block_size, 64, true) ||
+      !encode_2d_bf16(&tv, v_pool, rows, d->head_dim, d->block_size, 64, true))
+    return PA_ERR_CUDA;
+  DecodeArgs a;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.bt = block_tables;
+  a.ctx = context_lens;
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  a.ws_o = plan.total() ? reinterpret_cast<float *>(ws) : nullptr;
+  a.ws_ml = plan.total() ? reinterpret_cast<float *>(ws + plan.ws_o_bytes) : nullptr;
+  a.ws_cnt = plan.total() ? reinterpret_cast<int32_t *>(ws + plan.ws_o_bytes + plan.ws_ml_bytes) : nullptr;
+  a.err = err_flag;
+  a.S = d->num_seqs;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.G = d->num_q_heads / d->num_kv_heads;
+  a.num_blocks = d->num_blocks;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.max_ctx = d->max_context_len;
+  a.part_pages = plan.part_pages;
+  a.max_parts = plan.max_parts;
+  a.scale_log2 = d->scale * 1.4426950408889634f;
+  const dim3 grid(plan.max_parts, d->num_kv_heads, d->num_seqs);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d->head_dim == 128)
+    return d->block_size == 16 ? dispatch_nt<128, 16>(a.G, tk, tv, a, grid, s)
+                               : dispatch_nt<128, 32>(a.G, tk, tv, a, grid, s);
+  return d->block_size == 16 ? dispatch_nt<64, 16>(a.G, tk, tv, a, grid, s)
+                             : dispatch_nt<64, 32>(a.G, tk, tv, a, grid, s);
+}

@@ -1,0 +1,51 @@
+// Host-side helpers shared by the launchers of libpagedattn (not part of the
+// public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedattn.h"
+
+namespace pa {
+
+// SM count of the current device (cached per device); <= 0 on error.
+int current_sm_count();
+
+// Encodes a 2-D bf16 tensor map over `rows` x `cols` elements (row pitch
+// cols*2 bytes) with a box of box_rows x box_cols and 128-byte swizzling.
+// Returns false when the driver encoder is unavailable or rejects the map.
+bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+
+// Encodes a 3-D bf16 tensor map (dims innermost first) with 128-byte swizzle.
+bool encode_3d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[3],
+                    const uint64_t strides_bytes[2], const uint32_t box[3]);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int launch_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Longest context part one decode CTA streams, and most parts per sequence.
+constexpr int kMaxPartPages = 512;
+constexpr int kMaxParts = 256;
+
+// Split-K plan of a decode call: every sequence's pages are cut into parts of
+// part_pages pages; max_parts parts at most per sequence.
+struct DecodePlan {
+  int part_pages = 0;
+  int max_parts = 0;
+  size_t ws_o_bytes = 0;    // fp32 [S][Hkv][max_parts][G][D]
+  size_t ws_ml_bytes = 0;   // fp32 [S][Hkv][max_parts][G][2]
+  size_t ws_cnt_bytes = 0;  // int32 [S][Hkv]
+  size_t total() const { return ws_o_bytes + ws_ml_bytes + ws_cnt_bytes; }
+};
+
+// Validates `d` for the decode kernel; PA_OK or an error status.
+int validate_decode_desc(const pa_decode_desc *d);
+
+// The plan used by both pa_decode_workspace_bytes and the launcher.
+DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count);
+
+}  // namespace pa

@@ -1,0 +1,93 @@
+"""The C-ABI library loads and exports every call include/pagedattn.h
+declares; host-side validation rejects bad arguments before any GPU work.
+(No compute call runs here: this file needs no GPU.)"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_262_gb300 as pa
+from paged_kv_cache_262_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    return pa.load()
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(pa_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(pa.EXPORTS), declared ^ set(pa.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", pbuild.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pa_\w+)", out))
+    assert declared <= exported, declared - exported
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in pa.version()
+    assert pa.status_string(pa.PA_ERR_WORKSPACE) == "workspace missing or too small"
+    assert pa.status_string(12345) == "unknown status"
+
+
+def _desc(**kw):
+    d = dict(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16, num_blocks=10,
+             max_blocks_per_seq=4, max_context_len=64, scale=0.1)
+    d.update(kw)
+    return pa.DecodeDesc(**d)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(head_dim=96), pa.PA_ERR_UNSUPPORTED),
+    (dict(block_size=8), pa.PA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=6, num_kv_heads=4), pa.PA_ERR_INVALID),
+    (dict(num_q_heads=34, num_kv_heads=2), pa.PA_ERR_UNSUPPORTED),
+    (dict(num_seqs=-1), pa.PA_ERR_INVALID),
+    (dict(num_blocks=0), pa.PA_ERR_INVALID),
+])
+def test_decode_desc_validation(lib, kw, expect):
+    d = _desc(**kw)
+    st = lib.pa_paged_attention_decode(ctypes.byref(d), 16, 16, 16, 16, 16, 16, None, 0, None, None)
+    assert st == expect
+    assert lib.pa_decode_workspace_bytes(ctypes.byref(d)) == 0
+
+
+def test_decode_null_and_misaligned_pointers(lib):
+    d = _desc()
+    assert lib.pa_paged_attention_decode(None, 16, 16, 16, 16, 16, 16, None, 0, None, None) == pa.PA_ERR_INVALID
+    assert lib.pa_paged_attention_decode(ctypes.byref(d), None, 16, 16, 16, 16, 16, None, 0, None, None) == pa.PA_ERR_INVALID
+    assert lib.pa_paged_attention_decode(ctypes.byref(d), 18, 16, 16, 16, 16, 16, None, 0, None, None) == pa.PA_ERR_INVALID
+    # zero sequences: nothing to launch, OK without touching the GPU
+    d0 = _desc(num_seqs=0)
+    assert lib.pa_paged_attention_decode(ctypes.byref(d0), None, None, None, None, None, None, None, 0, None, None) == pa.PA_OK
+
+
+def test_cache_call_validation(lib):
+    f = lib.pa_reshape_and_cache
+    assert f(16, 16, 16, 16, 16, 0, 8, 128, 16, 10, None, None) == pa.PA_OK  # nothing to write
+    assert f(16, 16, 16, 16, 16, 4, 8, 100, 16, 10, None, None) == pa.PA_ERR_UNSUPPORTED
+    assert f(None, 16, 16, 16, 16, 4, 8, 128, 16, 10, None, None) == pa.PA_ERR_INVALID
+    assert f(24, 16, 16, 16, 16, 4, 8, 128, 16, 10, None, None) == pa.PA_ERR_INVALID
+    P = ctypes.c_void_p * 1
+    g = lib.pa_copy_blocks
+    assert g(P(16), P(16), 1, 16, 0, 10, 4096, None, None) == pa.PA_OK  # no pairs
+    assert g(P(16), P(16), 0, 16, 1, 10, 4096, None, None) == pa.PA_ERR_INVALID
+    assert g(P(16), P(16), 1, 16, 1, 10, 4095, None, None) == pa.PA_ERR_INVALID
+    assert g(P(None), P(16), 1, 16, 1, 10, 4096, None, None) == pa.PA_ERR_INVALID

@@ -1,0 +1,189 @@
+"""Host block manager (plain C++, no GPU): on-demand allocation, sharing,
+copy-on-write, free on <eos>, fragmentation bound, error states."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import paged_kv_cache_262_gb300 as pa
+import workloads as wl
+from paged_kv_cache_262_gb300 import build as pbuild
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pbuild.build()
+
+
+def test_block_table_example_1024_tokens():
+    """'PagedAttention Architecture Deep Dive' example: 1024 tokens at 16 per
+    page occupy 64 pages; a shared page has ref_count 2."""
+    fx = json.load(open(os.path.join(GOLDEN, "block_table_example.json")))
+    bm = pa.BlockManager(200, fx["block_size"])
+    bm.add_seq(0, fx["tokens"])
+    t = bm.block_table(0)
+    assert len(t) == fx["pages"]
+    assert bm.num_free() == 200 - fx["pages"]
+    bm.fork(0, 1)
+    assert bm.ref_count(t[2]) == 2
+    assert bm.wasted_slots() == 0
+
+
+def test_on_demand_allocation_and_waste_bound():
+    """ceil(n/B) blocks per sequence; at most B-1 unused slots per sequence,
+    so waste stays under 4 % once sequences are long compared with B."""
+    B = 16
+    st = wl.Stream(3, 3)
+    lens = st.integers(128, 2048, 64)
+    bm = pa.BlockManager(int(sum((l + B - 1) // B for l in lens)), B)
+    for i, n in enumerate(lens):
+        bm.add_seq(i, int(n))
+        assert len(bm.block_table(i)) == (n + B - 1) // B
+    assert bm.num_free() == 0
+    w = bm.wasted_slots()
+    assert w == sum((-int(n)) % B for n in lens)
+    assert w <= (B - 1) * len(lens)
+    assert w / (w + lens.sum()) < 0.04
+    tables = [bm.block_table(i) for i in range(len(lens))]
+    flat = [b for t in tables for b in t]
+    assert len(flat) == len(set(flat))  # no block given twice
+
+
+def test_free_returns_all_blocks_and_reuses_them():
+    bm = pa.BlockManager(10, 16)
+    bm.add_seq(1, 40)
+    bm.add_seq(2, 33)
+    assert bm.num_free() == 10 - 3 - 3
+    t1 = bm.block_table(1)
+    bm.free_seq(1)
+    assert bm.num_free() == 7
+    assert all(bm.ref_count(b) == 0 for b in t1)
+    bm.add_seq(3, 16)
+    assert bm.block_table(3)[0] in t1  # freed pages are reused next
+    bm.free_seq(2)
+    bm.free_seq(3)
+    assert bm.num_free() == 10
+
+
+def test_fork_append_copy_on_write():
+    B = 16
+    bm = pa.BlockManager(32, B)
+    bm.add_seq(0, 20)  # 2 blocks, last one holds 4 tokens
+    for c in (1, 2, 3):
+        bm.fork(0, c)
+    t0 = bm.block_table(0)
+    assert [bm.ref_count(b) for b in t0] == [4, 4]
+    pairs = []
+    for s in (0, 1, 2, 3):
+        slot, pair = bm.append(s)
+        t = bm.block_table(s)
+        assert slot == t[1] * B + 4
+        pairs.append(pair)
+    # three sharers copy the partial block, the last one writes in place
+    assert all(p is not None and p[0] == t0[1] for p in pairs[:3])
+    assert pairs[3] is None
+    assert len({p[1] for p in pairs[:3]}) == 3
+    assert bm.ref_count(t0[1]) == 1 and bm.ref_count(t0[0]) == 4
+    assert bm.seq_len(2) == 21
+    # a full shared block needs no copy: the token opens a new block
+    bm.add_seq(10, 32)
+    bm.fork(10, 11)
+    slot, pair = bm.append(11)
+    assert pair is None and slot % B == 0 and bm.block_table(11)[:2] == bm.block_table(10)
+
+
+def test_prefix_sharing_structure():
+    """64 prompts x 4 samples over a 2048-token prefix: the prefix blocks end up
+    with ref_count 256 and each partial last block is copied 3 times."""
+    plan = wl.prefix_sharing_plan()
+    B = plan.B
+    bm = pa.BlockManager(plan.num_blocks, B)
+    bm.add_seq(100000, plan.prefix_len)
+    prefix = bm.block_table(100000)
+    for p in range(plan.num_prompts):
+        bm.fork(100000, p * 4)
+        for _ in range(int(plan.suffix_lens[p])):
+            slot, pair = bm.append(p * 4)
+            assert pair is None
+    bm.free_seq(100000)
+    for p in range(plan.num_prompts):
+        for i in (1, 2, 3):
+            bm.fork(p * 4, p * 4 + i)
+    assert all(bm.ref_count(b) == 256 for b in prefix)
+    ncow = 0
+    for s in range(plan.num_prompts * 4):
+        _, pair = bm.append(s)
+        ncow += pair is not None
+    partial = sum(1 for x in plan.suffix_lens if (plan.prefix_len + int(x)) % B)
+    assert ncow == 3 * partial
+
+
+def test_errors_and_oom_leave_no_trace():
+    bm = pa.BlockManager(4, 16)
+    with pytest.raises(pa.PaError) as e:
+        bm.add_seq(0, 80)
+    assert e.value.status == pa.PA_ERR_OOM and bm.num_free() == 4
+    bm.add_seq(0, 64)
+    with pytest.raises(pa.PaError) as e:
+        bm.append(0)
+    assert e.value.status == pa.PA_ERR_OOM and bm.seq_len(0) == 64
+    with pytest.raises(pa.PaError) as e:
+        bm.add_seq(0, 1)
+    assert e.value.status == pa.PA_ERR_STATE
+    with pytest.raises(pa.PaError):
+        bm.free_seq(7)
+    with pytest.raises(pa.PaError):
+        bm.fork(7, 8)
+    bm.free_seq(0)
+    with pytest.raises(pa.PaError):
+        bm.free_seq(0)
+    assert bm.ref_count(-1) == -1 and bm.ref_count(4) == -1
+    with pytest.raises(pa.PaError):
+        pa.BlockManager(0, 16)
+
+
+def test_random_operations_keep_invariants():
+    """Random add/fork/append/free: reference counts equal the number of tables
+    that hold each block, free + referenced = pool, lengths match tables."""
+    st = wl.Stream(21, 21)
+    B, N = 16, 300
+    bm = pa.BlockManager(N, B)
+    live = {}
+    nxt = 0
+    u = st.uniform(4000)
+    for k in range(4000):
+        op = u[k]
+        try:
+            if op < 0.25 or not live:
+                bm.add_seq(nxt, int(u[k] * 1e6) % 100)
+                live[nxt] = True
+                nxt += 1
+            elif op < 0.4:
+                p = list(live)[int(u[k] * 1e7) % len(live)]
+                bm.fork(p, nxt)
+                live[nxt] = True
+                nxt += 1
+            elif op < 0.85:
+                s = list(live)[int(u[k] * 1e7) % len(live)]
+                bm.append(s)
+            else:
+                s = list(live)[int(u[k] * 1e7) % len(live)]
+                bm.free_seq(s)
+                del live[s]
+        except pa.PaError as e:
+            assert e.status == pa.PA_ERR_OOM
+        if k % 97 == 0:
+            refs = np.zeros(N, int)
+            for s in live:
+                t = bm.block_table(s)
+                assert len(t) == (bm.seq_len(s) + B - 1) // B
+                for b in t:
+                    refs[b] += 1
+            assert all(bm.ref_count(b) == refs[b] for b in range(N))
+            assert bm.num_free() == int((refs == 0).sum())
+    for s in list(live):
+        bm.free_seq(s)
+    assert bm.num_free() == N
