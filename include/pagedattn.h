@@ -100,9 +100,9 @@ const char *pa_status_string(int status);
 
 /* Bytes of device workspace pa_paged_attention_decode needs for `desc` on the
  * current device (0 when no context is split).  The workspace holds split-K
- * partial results and one int32 arrival counter per (sequence, kv head): it
- * must be zero-filled once before its first use; every completed call leaves
- * the counters zero again.  Returns 0 for an invalid desc. */
+ * partial results and one 64-bit arrival counter per (sequence, kv head)
+ * tagged with a per-call epoch, so it needs no initialisation and may be
+ * reused across calls of any shape.  Returns 0 for an invalid desc. */
 size_t pa_decode_workspace_bytes(const pa_decode_desc *desc);
 
 /* Paged decode attention [ATT][PHASE]: for every sequence s and query head h,
@@ -117,8 +117,8 @@ size_t pa_decode_workspace_bytes(const pa_decode_desc *desc);
  *   context_lens device int32 [num_seqs]
  *   out          device bf16 [num_seqs][num_q_heads][head_dim]
  *   workspace    device, >= pa_decode_workspace_bytes(desc) (may be NULL when
- *                that is 0), zero-filled before first use, not shared by calls
- *                that may overlap on the GPU
+ *                that is 0), 16-byte aligned, any contents; calls that may
+ *                overlap on the GPU must not share one
  *   err_flag     device int32 or NULL
  * Returns PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE or
  * PA_ERR_CUDA.  num_seqs == 0 launches nothing. */

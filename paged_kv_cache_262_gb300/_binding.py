@@ -157,8 +157,8 @@ _WS = {}
 
 
 def decode_workspace(desc: DecodeDesc, device):
-    """A zero-filled workspace of the size the call needs, cached per device
-    and reused (every call leaves its counters zero again)."""
+    """A workspace of the size the call needs, cached per device and reused
+    (its contents need no clearing between calls)."""
     import torch
     need = decode_workspace_bytes(desc)
     if need == 0:
@@ -166,7 +166,7 @@ def decode_workspace(desc: DecodeDesc, device):
     key = torch.device(device).index
     ws = _WS.get(key)
     if ws is None or ws.numel() < need:
-        ws = torch.zeros(need, dtype=torch.uint8, device=device)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
         _WS[key] = ws
     return ws
 

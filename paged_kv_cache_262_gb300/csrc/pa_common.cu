@@ -136,7 +136,7 @@ DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
     auto up = [](size_t b) { return (b + 255) & ~(size_t)255; };
     p.ws_o_bytes = up(n * d->head_dim * sizeof(float));
     p.ws_ml_bytes = up(n * 2 * sizeof(float));
-    p.ws_cnt_bytes = up((size_t)d->num_seqs * d->num_kv_heads * sizeof(int32_t));
+    p.ws_cnt_bytes = up((size_t)d->num_seqs * d->num_kv_heads * sizeof(unsigned long long));
   }
   return p;
 }

@@ -25,12 +25,15 @@
 //  * Warps are merged in shared memory at the end; a context cut into several
 //    parts writes (o/l, m, l) per part to the workspace, and the last CTA of a
 //    (sequence, kv head) to arrive (atomic counter, no waiting) merges the
-//    parts in part order -- deterministic, one launch.
+//    parts in part order -- deterministic, one launch.  The counter carries a
+//    per-call epoch tag, so stale workspace contents never need clearing.
 //  * Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <atomic>
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -46,11 +49,26 @@ struct DecodeArgs {
   __nv_bfloat16 *out;
   float *ws_o;
   float *ws_ml;
-  int32_t *ws_cnt;
+  unsigned long long *ws_cnt;  // per (sequence, kv head): epoch << 32 | arrivals
   int32_t *err;
   int S, Hq, Hkv, G, num_blocks, max_blocks, max_ctx, part_pages, max_parts;
   float scale_log2;
+  unsigned int epoch;  // unique per call, never 0
 };
+
+// Counts one arrival of this call at *c and returns the arrivals so far.  A
+// counter whose epoch tag is not this call's (left by another call or holding
+// stale data) restarts at 1, so the workspace needs no zero-fill.
+__device__ __forceinline__ unsigned int arrive_count(unsigned long long *c, unsigned int epoch) {
+  const unsigned long long tag = (unsigned long long)epoch << 32;
+  unsigned long long old = atomicAdd(c, 0ull), prev;
+  for (;;) {
+    const unsigned long long nv = ((old >> 32) == epoch) ? old + 1 : (tag | 1ull);
+    prev = atomicCAS(c, old, nv);
+    if (prev == old) return (unsigned int)(nv & 0xffffffffull);
+    old = prev;
+  }
+}
 
 template <int D, int B, int NW, int NST>
 struct DecodeSmem {
@@ -344,7 +362,7 @@ __global__ void __launch_bounds__(NW * 32)
   // ---- split-K: the last part of this (sequence, kv head) merges all parts
   __threadfence();
   __syncthreads();
-  if (tid == 0) misc[0] = (atomicAdd(a.ws_cnt + unit, 1) == nparts - 1);
+  if (tid == 0) misc[0] = (arrive_count(a.ws_cnt + unit, a.epoch) == (unsigned int)nparts);
   __syncthreads();
   if (!misc[0]) return;
   __threadfence();
@@ -374,7 +392,17 @@ __global__ void __launch_bounds__(NW * 32)
     for (int p = 0; p < nparts; ++p) acc += wts[p * 16 + g] * __ldcg(a.ws_o + ((ubase + p) * G + g) * D + d);
     out_base[idx] = __float2bfloat16(acc);
   }
-  if (tid == 0) a.ws_cnt[unit] = 0;
+  if (tid == 0) a.ws_cnt[unit] = 0ull;
+}
+
+std::atomic<unsigned int> g_epoch{0};
+
+unsigned int next_epoch() {
+  unsigned int e;
+  do {
+    e = g_epoch.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);
+  return e;
 }
 
 template <int D, int B, int NT>
@@ -430,7 +458,10 @@ extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q,
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   a.ws_o = plan.total() ? reinterpret_cast<float *>(ws) : nullptr;
   a.ws_ml = plan.total() ? reinterpret_cast<float *>(ws + plan.ws_o_bytes) : nullptr;
-  a.ws_cnt = plan.total() ? reinterpret_cast<int32_t *>(ws + plan.ws_o_bytes + plan.ws_ml_bytes) : nullptr;
+  a.ws_cnt = plan.total()
+                 ? reinterpret_cast<unsigned long long *>(ws + plan.ws_o_bytes + plan.ws_ml_bytes)
+                 : nullptr;
+  a.epoch = next_epoch();
   a.err = err_flag;
   a.S = d->num_seqs;
   a.Hq = d->num_q_heads;

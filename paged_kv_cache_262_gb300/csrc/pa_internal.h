@@ -38,7 +38,7 @@ struct DecodePlan {
   int max_parts = 0;
   size_t ws_o_bytes = 0;    // fp32 [S][Hkv][max_parts][G][D]
   size_t ws_ml_bytes = 0;   // fp32 [S][Hkv][max_parts][G][2]
-  size_t ws_cnt_bytes = 0;  // int32 [S][Hkv]
+  size_t ws_cnt_bytes = 0;  // uint64 [S][Hkv] epoch-tagged arrival counters
   size_t total() const { return ws_o_bytes + ws_ml_bytes + ws_cnt_bytes; }
 };
 

@@ -197,3 +197,24 @@ def test_repeated_calls_reuse_workspace(torch, ora, parts):
         assert np.array_equal(bf16_host(run_step(torch, case, d)), first)
     ref, _ = ora.decode_case(case)
     assert_close(first, ref, "repeat")
+
+
+def test_workspace_needs_no_clearing(torch, ora, parts):
+    """Garbage in the workspace and calls of different split layouts sharing
+    one workspace do not change results (epoch-tagged arrival counters)."""
+    parts(3)
+    a = wl.make_decode_case("wa", [900, 40, 1300], 16, 2, 128, 16, seed=9, with_new_tokens=False)
+    b = wl.make_decode_case("wb", [2000, 2000, 17, 600, 5], 8, 4, 64, 32, seed=10, with_new_tokens=False)
+    da, db = upload_case(a, torch), upload_case(b, torch)
+    need = max(pa.decode_workspace_bytes(pa.make_desc(d["q"], d["k_pool"], d["bt"], max_context_len=c.max_context_len))
+               for d, c in ((da, a), (db, b)))
+    ws = torch.randint(0, 256, (need,), dtype=torch.uint8, device="cuda")
+    ref_a, _ = ora.decode_case(a)
+    ref_b, _ = ora.decode_case(b)
+    for _ in range(3):
+        for d, c, ref in ((da, a, ref_a), (db, b, ref_b)):
+            out = pa.paged_attention_decode(d["q"], d["k_pool"], d["v_pool"], d["bt"], d["ctx"], scale=c.scale,
+                                            max_context_len=c.max_context_len, workspace=ws)
+            torch.cuda.synchronize()
+            assert_close(bf16_host(out), ref, c.name)
+        ws[: need // 2].random_(0, 256)  # scribble over partial results and counters
