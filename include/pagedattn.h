@@ -127,6 +127,33 @@ int pa_paged_attention_decode(const pa_decode_desc *desc, const void *q, const v
                               const int32_t *context_lens, void *out, void *workspace,
                               size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/* Size of the fixed device scratch array of pa_paged_attention_decode_noalloc
+ * (8 MiB, held on every GPU that loads the library until the process exits). */
+#define PA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Paged decode attention that allocates nothing and takes no workspace.  No
+ * page describes this call; it exists for callers that cannot allocate device
+ * memory (a plugin whose host framework owns all device memory, a path where
+ * cudaMalloc's implicit synchronisation is not allowed, memory fixed at
+ * start-up).  Same arguments, results and errors as pa_paged_attention_decode
+ * without the workspace pair: the split-K scratch is a file-scope device array
+ * of PA_NOALLOC_SCRATCH_BYTES.  Calls no cudaMalloc/cudaFree and no allocating
+ * library routine.
+ *  - Returns PA_ERR_WORKSPACE, before any launch, when the shape needs more
+ *    scratch than PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes(desc)
+ *    tells how much it needs).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress) and caches it; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents; nothing in it has to start at zero (its arrival counters are
+ *    tagged per call).  Calls that may overlap on the GPU race on the array:
+ *    order them on one stream or serialise them. */
+int pa_paged_attention_decode_noalloc(const pa_decode_desc *desc, const void *q,
+                                      const void *k_pool, const void *v_pool,
+                                      const int32_t *block_tables, const int32_t *context_lens,
+                                      void *out, int32_t *err_flag, void *stream);
+
 /* Causal chunked-prefill attention [PHASE][CHUNK] on the tensor cores.
  * Chunk r (r < desc->num_seqs) has C_r = cu_q[r+1] - cu_q[r] query tokens and
  * context ctx_r = context_lens[r] that INCLUDES the chunk (its K/V must already

@@ -23,7 +23,7 @@ DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 
 # Every symbol include/pagedattn.h declares.
 EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
-    "pa_paged_attention_prefill_chunk", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
 )
@@ -66,6 +66,8 @@ def load(path: Optional[str] = None):
         lib.pa_paged_attention_decode.restype = i
         lib.pa_paged_attention_decode.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, sz,
                                                   _P, _P]
+        lib.pa_paged_attention_decode_noalloc.restype = i
+        lib.pa_paged_attention_decode_noalloc.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P]
         lib.pa_paged_attention_prefill_chunk.restype = i
         lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, _P, _P, _P, _P,
                                                          _P, _P, _P]
@@ -192,6 +194,30 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=No
                                           _ptr(block_tables), _ptr(context_lens), _ptr(out),
                                           _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode")
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def paged_attention_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, out=None, *, scale=None,
+                                   max_context_len=None, err_flag=None, stream=None):
+    """Decode attention without a workspace (fixed device scratch array; for
+    callers that cannot allocate device memory -- see pagedattn.h)."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
+    st = load().pa_paged_attention_decode_noalloc(_c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                                  _ptr(block_tables), _ptr(context_lens), _ptr(out),
+                                                  _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_paged_attention_decode_noalloc")
     return out
 
 
