@@ -103,14 +103,15 @@ int validate_decode_desc(const pa_decode_desc *d) {
 }
 
 // Split policy.  Each CTA streams one part (part_pages pages of one
-// (sequence, kv head)).  Parts are sized so that the longest sequence's parts
-// over all (sequence, kv head) units give about kWaves waves of resident CTAs;
-// a part is never shorter than kMinPartPages pages unless the whole context is.
-// PA_PARTITION_PAGES in the environment overrides the part length (tuning).
+// (sequence, kv head)); two CTAs are resident per SM.  Long parts amortise the
+// per-CTA set-up and the split-K merge, so parts are sized for about 1.5 CTAs
+// per resident slot over the longest-context bound (never below
+// kMinPartPages pages unless the context is shorter); CTAs start longest
+// context first, which keeps the ragged tail short.  PA_PARTITION_PAGES in the
+// environment overrides the part length (tuning).
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
   constexpr int kCtasPerSm = 2;
-  constexpr int kWaves = 4;
-  constexpr int kMinPartPages = 16;
+  constexpr int kMinPartPages = 32;
   DecodePlan p;
   const int B = d->block_size;
   const int64_t max_pages = std::max<int64_t>(1, ((int64_t)d->max_context_len + B - 1) / B);
@@ -120,8 +121,8 @@ DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
   if (env && atoi(env) > 0) {
     pp = atoi(env);
   } else {
-    const int64_t slots = (int64_t)std::max(sm_count, 1) * kCtasPerSm * kWaves;
-    pp = (units * max_pages + slots - 1) / slots;
+    const int64_t slots = (int64_t)std::max(sm_count, 1) * kCtasPerSm;
+    pp = (units * max_pages * 2 + slots * 3 - 1) / (slots * 3);
     pp = std::max<int64_t>(pp, kMinPartPages);
   }
   pp = std::max<int64_t>(pp, (max_pages + kMaxParts - 1) / kMaxParts);

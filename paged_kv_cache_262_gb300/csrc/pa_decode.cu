@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <atomic>
 
@@ -54,6 +55,7 @@ struct DecodeArgs {
   int S, Hq, Hkv, G, num_blocks, max_blocks, max_ctx, part_pages, max_parts;
   float scale_log2;
   unsigned int epoch;  // unique per call, never 0
+  int lpt;             // order CTAs longest context first
 };
 
 // Counts one arrival of this call at *c and returns the arrivals so far.  A
@@ -84,15 +86,86 @@ struct DecodeSmem {
   static constexpr int kBarOff = (kRegion0 + 1023) & ~1023;
   static constexpr int kTblOff = kBarOff + NW * NST * 8;
   static constexpr int kMiscOff = kTblOff + kMaxPartPages * 4;
-  static constexpr int kBytes = kMiscOff + 16;
+  // misc: [0..3] broadcast words, [4..7] warp totals, [8..135] length histogram
+  static constexpr int kBytes = kMiscOff + 4 * 136;
   static constexpr int kAlloc = kBytes + 1024;  // base re-aligned to 1024 in the kernel
 };
+
+// Length class of a sequence for longest-first ordering: quarter-octave
+// buckets of its page count (1 .. 68), 0 for an invalid context.
+__device__ __forceinline__ int length_bucket(int ctx, int B, int max_blocks, int max_ctx) {
+  if (ctx <= 0 || ctx > max_blocks * B || ctx > max_ctx) return 0;
+  const int p = (ctx + B - 1) / B;
+  const int msb = 31 - __clz(p);
+  const int frac = msb >= 2 ? (p >> (msb - 2)) & 3 : (p << (2 - msb)) & 3;
+  return 4 * msb + frac + 1;
+}
+
+// Index of the sequence of rank r when sequences are ordered by decreasing
+// length bucket, ties in index order.  Whole CTA; misc holds 136 ints.
+template <int NT_>
+__device__ int seq_of_rank(int r, const int32_t *ctx, int S, int B, int max_blocks, int max_ctx, int *misc) {
+  constexpr int kThreads = NT_;
+  int *hist = misc + 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < 128; i += kThreads) hist[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < S; i += kThreads) atomicAdd(&hist[length_bucket(__ldg(ctx + i), B, max_blocks, max_ctx)], 1);
+  __syncthreads();
+  if (warp == 0) {  // bucket holding rank r, scanning buckets from the longest down
+    int c[4], t = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[j] = hist[127 - 4 * lane - j];
+      t += c[j];
+    }
+    int incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - t;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (r >= run && r < run + c[j]) {
+        misc[0] = 127 - 4 * lane - j;
+        misc[1] = r - run;
+      }
+      run += c[j];
+    }
+  }
+  __syncthreads();
+  const int bstar = misc[0], k = misc[1];
+  const int chunk = (S + kThreads - 1) / kThreads;
+  const int beg = min(S, tid * chunk), end = min(S, beg + chunk);
+  int cnt = 0;
+  for (int i = beg; i < end; ++i) cnt += length_bucket(__ldg(ctx + i), B, max_blocks, max_ctx) == bstar;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) misc[4 + warp] = incl;
+  __syncthreads();
+  int excl = incl - cnt;
+  for (int w = 0; w < warp; ++w) excl += misc[4 + w];
+  if (k >= excl && k < excl + cnt) {
+    int left = k - excl;
+    for (int i = beg; i < end; ++i)
+      if (length_bucket(__ldg(ctx + i), B, max_blocks, max_ctx) == bstar && left-- == 0) misc[2] = i;
+  }
+  __syncthreads();
+  return misc[2];
+}
 
 template <int D, int B, int NT, int NW, int NST>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
   using L = DecodeSmem<D, B, NW, NST>;
+  static_assert(NW <= 4, "misc holds four warp totals");
   constexpr int KS = D / 16;  // k-steps of S^T = K Q^T
   constexpr int MT = B / 16;  // 16-token tiles per page
   constexpr int DT = D / 16;  // 16-row d tiles of O^T = V^T P^T
@@ -103,7 +176,15 @@ __global__ void __launch_bounds__(NW * 32)
   int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kTblOff);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
 
-  const int part = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  // CTAs are dispatched in linear order; map that order to (sequence rank,
+  // part, kv head) so that the longest contexts start first.
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int per_seq = a.max_parts * a.Hkv;
+  const int rank = lin / per_seq;
+  const int part = (lin - rank * per_seq) / a.Hkv;
+  const int kvh = lin - rank * per_seq - part * a.Hkv;
+  const int s = (a.lpt && a.S > 1) ? seq_of_rank<NW * 32>(rank, a.ctx, a.S, B, a.max_blocks, a.max_ctx, misc)
+                                   : rank;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
   const int ctx = __ldg(a.ctx + s);
@@ -462,6 +543,10 @@ extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q,
                  ? reinterpret_cast<unsigned long long *>(ws + plan.ws_o_bytes + plan.ws_ml_bytes)
                  : nullptr;
   a.epoch = next_epoch();
+  {
+    const char *env = getenv("PA_DECODE_LPT");
+    a.lpt = (env && env[0] == '0') ? 0 : 1;
+  }
   a.err = err_flag;
   a.S = d->num_seqs;
   a.Hq = d->num_q_heads;

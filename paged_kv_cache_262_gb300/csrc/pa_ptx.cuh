@@ -134,4 +134,94 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return static_cast<uint32_t>(r * 128 + (((c ^ r) & 7) << 4));
 }
 
+// ------------------------------------------------------- tcgen05 (TMEM, UMMA)
+// TMEM addresses are (lane << 16) | column.  A warp may touch only the 32 lanes
+// of its own quarter: lanes 32*(warp%4) .. 32*(warp%4)+31.
+
+// Allocates ncols TMEM columns (power of two >= 32); whole warp.  The base
+// address is written to *smem_dst.
+__device__ __forceinline__ void tmem_alloc(uint32_t *smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand (rows of
+// 128 bytes, 8-row atoms of 1024 bytes, atom base 1024-aligned).
+//   K-major: lbo unused, sbo = byte stride between 8-row groups.
+//   MN-major: lbo = byte stride between 64-element blocks along M/N,
+//             sbo = byte stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of sm_100-class tensor cores
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives on *bar once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+#define PA_R32(i) "=r"(r[i])
+// 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : PA_R32(0), PA_R32(1), PA_R32(2), PA_R32(3), PA_R32(4), PA_R32(5), PA_R32(6), PA_R32(7),
+        PA_R32(8), PA_R32(9), PA_R32(10), PA_R32(11), PA_R32(12), PA_R32(13), PA_R32(14), PA_R32(15),
+        PA_R32(16), PA_R32(17), PA_R32(18), PA_R32(19), PA_R32(20), PA_R32(21), PA_R32(22), PA_R32(23),
+        PA_R32(24), PA_R32(25), PA_R32(26), PA_R32(27), PA_R32(28), PA_R32(29), PA_R32(30), PA_R32(31)
+      : "r"(taddr)
+      : "memory");
+}
+#undef PA_R32
+#define PA_W32(i) "r"(r[i])
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      PA_W32(0), PA_W32(1), PA_W32(2), PA_W32(3), PA_W32(4), PA_W32(5), PA_W32(6), PA_W32(7),
+      PA_W32(8), PA_W32(9), PA_W32(10), PA_W32(11), PA_W32(12), PA_W32(13), PA_W32(14), PA_W32(15),
+      PA_W32(16), PA_W32(17), PA_W32(18), PA_W32(19), PA_W32(20), PA_W32(21), PA_W32(22), PA_W32(23),
+      PA_W32(24), PA_W32(25), PA_W32(26), PA_W32(27), PA_W32(28), PA_W32(29), PA_W32(30), PA_W32(31)
+      : "memory");
+}
+#undef PA_W32
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 }  // namespace pa
