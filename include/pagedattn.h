@@ -157,18 +157,26 @@ int pa_paged_attention_decode_noalloc(const pa_decode_desc *desc, const void *q,
 /* Causal chunked-prefill attention [PHASE][CHUNK] on the tensor cores.
  * Chunk r (r < desc->num_seqs) has C_r = cu_q[r+1] - cu_q[r] query tokens and
  * context ctx_r = context_lens[r] that INCLUDES the chunk (its K/V must already
- * be cached).  Query row i of chunk r sits at position ctx_r - C_r + i and
- * attends keys 0..ctx_r - C_r + i of the chunk's block-table row.
- *   q       device bf16 [cu_q[R]][num_q_heads][head_dim]
- *   cu_q    device int32 [R + 1], cu_q[0] = 0, non-decreasing
- *   max_q_len  bound on every C_r (sizes the grid)
- *   out     device bf16 [cu_q[R]][num_q_heads][head_dim]
- * head_dim must be 128.  Other arguments as in pa_paged_attention_decode. */
+ * be cached, e.g. by pa_reshape_and_cache).  Query row i of chunk r sits at
+ * position ctx_r - C_r + i and attends keys 0 .. ctx_r - C_r + i of the
+ * chunk's block-table row:
+ *   out[cu_q[r]+i][h] = sum_j softmax_j(scale * q[cu_q[r]+i][h] . k_j) v_j.
+ * QK^T and PV run as tcgen05 MMAs (bf16 in, fp32 accumulate in TMEM); softmax
+ * in fp32; bf16 output.
+ *   q          device bf16 [total_q][num_q_heads][128]
+ *   cu_q       device int32 [R + 1], non-decreasing, cu_q[R] <= total_q
+ *   max_q_len  bound on every C_r (sizes the grid); total_q = rows of q / out
+ *   out        device bf16 [total_q][num_q_heads][128]; rows outside every
+ *              chunk are not written
+ * head_dim must be 128 and the GQA group size 1, 2, 4, 8 or 16.  A chunk
+ * with C_r > ctx_r, ctx_r > max_context_len or a row range outside
+ * [0, total_q) sets PA_DEVERR_CTX (its rows are zeroed when in range).  Other
+ * arguments and errors as in pa_paged_attention_decode (no workspace). */
 int pa_paged_attention_prefill_chunk(const pa_decode_desc *desc, const void *q,
-                                     const int32_t *cu_q, int max_q_len, const void *k_pool,
-                                     const void *v_pool, const int32_t *block_tables,
-                                     const int32_t *context_lens, void *out, int32_t *err_flag,
-                                     void *stream);
+                                     const int32_t *cu_q, int max_q_len, int total_q,
+                                     const void *k_pool, const void *v_pool,
+                                     const int32_t *block_tables, const int32_t *context_lens,
+                                     void *out, int32_t *err_flag, void *stream);
 
 /* Writes the K/V of num_tokens new tokens into their cache slots [PHASE][SHARE]:
  *   k_pool[slot / B][h][slot % B][:] = k[t][h][:]  (same for v), for t in order.

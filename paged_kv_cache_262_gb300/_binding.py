@@ -69,8 +69,8 @@ def load(path: Optional[str] = None):
         lib.pa_paged_attention_decode_noalloc.restype = i
         lib.pa_paged_attention_decode_noalloc.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P]
         lib.pa_paged_attention_prefill_chunk.restype = i
-        lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, _P, _P, _P, _P,
-                                                         _P, _P, _P]
+        lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, i, _P, _P, _P,
+                                                         _P, _P, _P, _P]
         lib.pa_reshape_and_cache.restype = i
         lib.pa_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, i, i, i, i, i, _P, _P]
         lib.pa_copy_blocks.restype = i
@@ -237,7 +237,7 @@ def paged_attention_prefill_chunk(q, cu_q, k_pool, v_pool, block_tables, context
     desc = make_desc(q, k_pool, block_tables, num_seqs=context_lens.shape[0], scale=scale,
                      max_context_len=max_context_len)
     st = load().pa_paged_attention_prefill_chunk(_c.byref(desc), _ptr(q), _ptr(cu_q), int(max_q_len),
-                                                 _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                                 int(q.shape[0]), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                                                  _ptr(context_lens), _ptr(out), _ptr(err_flag),
                                                  _stream_ptr(stream))
     _check(st, "pa_paged_attention_prefill_chunk")

@@ -1,9 +1,424 @@
-// Causal chunked-prefill attention (tcgen05) -- not yet built: the entry point
-// validates nothing and reports PA_ERR_UNSUPPORTED.
+// Causal chunked-prefill attention over the paged KV cache, on the tcgen05
+// tensor cores of sm_103a.
+//
+// Follows "Configuring vLLM and PagedAttention for High Throughput Enterprise
+// LLM Serving": the prefill phase attends every prompt position at once and is
+// compute bound ("Memory Bottlenecks in Autoregressive LLM Inference"); long
+// prompts are processed in chunks (512 or 1024 tokens) that ride along with
+// decode iterations ("High-Throughput Batching: Continuous Batching & Chunked
+// Prefill"); keys and values are read through the block table,
+// P_physical = BlockTable[j / B] ("Architectural Foundations").  A chunk of C
+// query tokens over a context of ctx tokens (the chunk included) places query
+// row i at position ctx - C + i; it attends keys 0 .. ctx - C + i.
+//
+// One CTA per (query tile, kv head, chunk).  A query tile is 128 MMA rows:
+// 128/G consecutive positions x the G query heads that share the kv head, so
+// each K/V tile serves the whole GQA group.  Roles (6 warps):
+//   warps 0-3  load the Q tile, run the softmax of one row each (TMEM lane =
+//              row), write P (bf16) into shared memory, rescale O, and store
+//              the output;
+//   warp 4     gathers 128-key K and V tiles page by page with 2-D TMA
+//              (128-byte swizzle) into a two-stage ring;
+//   warp 5     owns the TMEM allocation and issues the MMAs:
+//              S_j = Q K_j^T (fp32, TMEM, double buffered) and
+//              O += P_j V_j (fp32, TMEM; V read MN-major).
+// The softmax keeps a running max per row in base 2 and rescales O only when
+// the max grows by more than 8 (2^8); until then probabilities are taken
+// against the stale max, which the final normalisation by the same running
+// sum makes exact.  Value rows of keys past the context are zeroed in shared
+// memory before they meet a zero probability (unused cache slots may hold
+// NaNs).  Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
 #include "pagedattn.h"
 
-extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *, const void *, const int32_t *,
-                                                int, const void *, const void *, const int32_t *,
-                                                const int32_t *, void *, int32_t *, void *) {
-  return PA_ERR_UNSUPPORTED;
+namespace pa {
+namespace {
+
+struct PrefillArgs {
+  const __nv_bfloat16 *q;
+  const int32_t *cu_q;
+  const int32_t *bt;
+  const int32_t *ctx;
+  __nv_bfloat16 *out;
+  int32_t *err;
+  int R, Hq, Hkv, num_blocks, max_blocks, max_ctx, total_q;
+  float scale_log2;
+};
+
+constexpr int kD = 128;         // head_dim
+constexpr int kBM = 128;        // MMA rows per tile
+constexpr int kBN = 128;        // keys per tile
+constexpr int kHalf = 16384;    // one 64-column half of a 128 x 128 bf16 tile
+constexpr int kTile = 32768;    // 128 x 128 bf16
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;      // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
+constexpr int kOffP = kOffV + 2 * kTile;
+constexpr int kOffBar = kOffP + kTile;
+constexpr int kSmem = kOffBar + 256 + 1024;
+constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
+constexpr int kThreads = 192;
+
+enum { BAR_Q = 0, BAR_KV_FULL = 1, BAR_KV_EMPTY = 3, BAR_S_FULL = 5, BAR_P_FULL = 7, BAR_PV_DONE = 8, NBARS = 9 };
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) { return pack_bf16(a, b); }
+
+template <int B, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const PrefillArgs a) {
+  constexpr int TP = kBM / G;        // positions per tile
+  constexpr int PAGES = kBN / B;     // pages per key tile
+  constexpr uint32_t kIdS = umma_idesc_bf16(128, 128, false, false);
+  constexpr uint32_t kIdPV = umma_idesc_bf16(128, 128, false, true);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffBar + NBARS * 8);
+  volatile int *dead = reinterpret_cast<volatile int *>(smem + kOffBar + NBARS * 8 + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qt = gridDim.x - 1 - blockIdx.x;  // later tiles see more keys: start them first
+  const int g = blockIdx.y, r = blockIdx.z;
+  const int c0 = __ldg(a.cu_q + r), c1 = __ldg(a.cu_q + r + 1);
+  const int C = c1 - c0;
+  const int ctx = __ldg(a.ctx + r);
+  const int q0 = qt * TP;
+  if (C <= 0 || q0 >= C) return;
+  const bool bad = ctx <= 0 || C > ctx || ctx > a.max_blocks * B || ctx > a.max_ctx || c0 < 0 ||
+                   c1 > a.total_q;
+  if (bad) {  // zero this tile's rows, report
+    if (c0 >= 0 && c1 <= a.total_q) {
+      for (int m = threadIdx.x; m < kBM; m += kThreads) {
+        const int t = q0 + m / G;
+        if (t >= C) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + t) * a.Hq + g * G + m % G) * kD);
+        for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (threadIdx.x == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
+    return;
+  }
+  const int npages = (ctx + B - 1) / B;
+  const int pos_lo = ctx - C + q0;                     // first position of the tile
+  const int pos_hi = ctx - C + min(C, q0 + TP) - 1;    // last valid position
+  const int T = pos_hi / kBN + 1;                      // key tiles
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[BAR_Q], 128);
+    mbar_init(&bars[BAR_KV_FULL], 1);
+    mbar_init(&bars[BAR_KV_FULL + 1], 1);
+    mbar_init(&bars[BAR_KV_EMPTY], 1);
+    mbar_init(&bars[BAR_KV_EMPTY + 1], 1);
+    mbar_init(&bars[BAR_S_FULL], 1);
+    mbar_init(&bars[BAR_S_FULL + 1], 1);
+    mbar_init(&bars[BAR_P_FULL], 128);
+    mbar_init(&bars[BAR_PV_DONE], 1);
+    *dead = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  auto wait = [&](int b, uint32_t parity) {
+    if (*dead) return false;
+    if (mbar_wait(&bars[b], parity)) return true;
+    *dead = 1;
+    if (a.err) atomicOr(a.err, PA_DEVERR_TIMEOUT);
+    return false;
+  };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      const int32_t *bt_row = a.bt + (size_t)r * a.max_blocks;
+      for (int j = 0; j < T; ++j) {
+        const int st = j & 1;
+        if (j >= 2 && !wait(BAR_KV_EMPTY + st, (uint32_t)(((j >> 1) - 1) & 1))) break;
+        int pages[PAGES];
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < PAGES; ++i) {
+          const int pi = j * PAGES + i;
+          int pg = -1;
+          if (pi < npages) {
+            pg = __ldg(bt_row + pi);
+            if (pg < 0 || pg >= a.num_blocks) {
+              if (a.err) atomicOr(a.err, PA_DEVERR_PAGE);
+              pg = -1;
+            }
+          }
+          pages[i] = pg;
+          n += pg >= 0;
+        }
+        uint64_t *bar = &bars[BAR_KV_FULL + st];
+        if (n == 0) {
+          mbar_arrive(bar);
+          continue;
+        }
+        mbar_arrive_expect_tx(bar, (uint32_t)n * B * 128 * 4);
+        uint8_t *kd = smem + kOffK + st * kTile;
+        uint8_t *vd = smem + kOffV + st * kTile;
+#pragma unroll
+        for (int i = 0; i < PAGES; ++i) {
+          if (pages[i] < 0) continue;
+          const int row = (pages[i] * a.Hkv + g) * B;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d_hint(kd + h * kHalf + i * B * 128, &tmK, h * 64, row, bar, pol);
+            tma_load_2d_hint(vd + h * kHalf + i * B * 128, &tmV, h * 64, row, bar, pol);
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t sq = smem_u32(smem + kOffQ), sk = smem_u32(smem + kOffK);
+      const uint32_t sv = smem_u32(smem + kOffV), sp = smem_u32(smem + kOffP);
+      auto issue_s = [&](int j) {
+        const int st = j & 1;
+        const uint32_t kb = sk + st * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + st * 128, umma_desc_sw128(sq + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
+                    kIdS, kk > 0);
+        }
+        umma_commit(&bars[BAR_S_FULL + st]);
+      };
+      bool ok = wait(BAR_Q, 0) && wait(BAR_KV_FULL, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) {
+          if (!wait(BAR_KV_FULL + ((j + 1) & 1), (uint32_t)(((j + 1) >> 1) & 1))) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!wait(BAR_P_FULL, (uint32_t)(j & 1))) break;
+        tc_fence_after();
+        const uint32_t vb = sv + (j & 1) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + 256, umma_desc_sw128(sp + aoff, 16, 1024),
+                    umma_desc_sw128(vb + kk * 2048, kHalf, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars[BAR_PV_DONE]);
+        umma_commit(&bars[BAR_KV_EMPTY + (j & 1)]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------- softmax (row = m)
+    const int m = warp * 32 + lane;
+    const int tloc = q0 + m / G;                 // position index within the chunk
+    const bool row_valid = tloc < C;
+    const int pos = row_valid ? ctx - C + tloc : ctx - 1;
+    const int head = g * G + m % G;
+    // Q row -> shared memory (128-byte swizzle, two 64-column halves)
+    {
+      uint8_t *qd = smem + kOffQ;
+      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(qd + (c >> 3) * kHalf + sw128(m, c & 7)) = v;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[BAR_Q]);
+    }
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m_run = -INFINITY, l_run = 0.f;
+    uint8_t *pd = smem + kOffP;
+    for (int j = 0; j < T; ++j) {
+      const int st = j & 1;
+      if (!wait(BAR_S_FULL + st, (uint32_t)((j >> 1) & 1))) break;
+      tc_fence_after();
+      float s[kBN];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + st * 128 + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      const int key0 = j * kBN;
+      float mx = -INFINITY;
+      if (key0 + kBN - 1 <= pos_lo) {  // every key visible to every row of the tile
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          s[i] *= a.scale_log2;
+          mx = fmaxf(mx, s[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          s[i] = (key0 + i <= pos) ? s[i] * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[i]);
+        }
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const bool rescale = m_new > m_run + 8.f;
+      const float m_use = rescale ? m_new : m_run;
+      const float alpha = rescale ? exp2f(m_run - m_new) : 1.f;
+      // value rows of keys past the context must not carry NaNs into 0 * v
+      if (key0 + kBN > ctx) {
+        if (!wait(BAR_KV_FULL + st, (uint32_t)((j >> 1) & 1))) break;
+        if (key0 + m >= ctx) {
+          uint8_t *vd = smem + kOffV + st * kTile;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4 *>(vd + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(vd + kHalf + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      if (j >= 1) {
+        if (!wait(BAR_PV_DONE, (uint32_t)((j - 1) & 1))) break;  // O stable, P buffer free
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(lane_base + 256 + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(lane_base + 256 + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          w[e] = pack2(exp2f(s[c * 8 + 2 * e] - m_use), exp2f(s[c * 8 + 2 * e + 1] - m_use));
+          lsum += bf16_lo(w[e]) + bf16_hi(w[e]);
+        }
+        *reinterpret_cast<uint4 *>(pd + (c >> 3) * kHalf + sw128(m, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run = l_run * alpha + lsum;
+      m_run = m_use;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[BAR_P_FULL]);
+    }
+    if (wait(BAR_PV_DONE, (uint32_t)((T - 1) & 1))) {
+      tc_fence_after();
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + 256 + c * 32, v);
+        tmem_wait_ld();
+        if (row_valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 o;
+            o.x = pack2(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
+            o.y = pack2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
+            o.z = pack2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
+            o.w = pack2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
+            dst[c * 4 + i] = o;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int B, int G>
+int launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a, dim3 grid,
+                   cudaStream_t st) {
+  auto kern = prefill_kernel<B, G>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
+    return PA_ERR_CUDA;
+  kern<<<grid, kThreads, kSmem, st>>>(tk, tv, a);
+  return launch_status(cudaGetLastError());
+}
+
+template <int B>
+int dispatch_g(int G, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a, dim3 grid,
+               cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_prefill<B, 1>(tk, tv, a, grid, st);
+    case 2: return launch_prefill<B, 2>(tk, tv, a, grid, st);
+    case 4: return launch_prefill<B, 4>(tk, tv, a, grid, st);
+    case 8: return launch_prefill<B, 8>(tk, tv, a, grid, st);
+    case 16: return launch_prefill<B, 16>(tk, tv, a, grid, st);
+    default: return PA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const void *q, const int32_t *cu_q,
+                                                int max_q_len, int total_q, const void *k_pool,
+                                                const void *v_pool, const int32_t *block_tables,
+                                                const int32_t *context_lens, void *out, int32_t *err_flag,
+                                                void *stream) {
+  using namespace pa;
+  int st = validate_decode_desc(d);
+  if (st != PA_OK) return st;
+  if (d->head_dim != 128) return PA_ERR_UNSUPPORTED;
+  const int G = d->num_q_heads / d->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
+  if (max_q_len < 0 || total_q < 0) return PA_ERR_INVALID;
+  if (d->num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
+  if (!q || !cu_q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PA_ERR_INVALID;
+  if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  const long long tiles = ((long long)max_q_len * G + kBM - 1) / kBM;
+  if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+  const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
+  CUtensorMap tk, tv;
+  if (!encode_2d_bf16(&tk, k_pool, rows, 128, d->block_size, 64, true) ||
+      !encode_2d_bf16(&tv, v_pool, rows, 128, d->block_size, 64, true))
+    return PA_ERR_CUDA;
+  PrefillArgs a;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.cu_q = cu_q;
+  a.bt = block_tables;
+  a.ctx = context_lens;
+  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.err = err_flag;
+  a.R = d->num_seqs;
+  a.Hq = d->num_q_heads;
+  a.Hkv = d->num_kv_heads;
+  a.num_blocks = d->num_blocks;
+  a.max_blocks = d->max_blocks_per_seq;
+  a.max_ctx = d->max_context_len;
+  a.total_q = total_q;
+  a.scale_log2 = d->scale * 1.4426950408889634f;
+  const dim3 grid((unsigned)tiles, d->num_kv_heads, d->num_seqs);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return d->block_size == 16 ? dispatch_g<16>(G, tk, tv, a, grid, s) : dispatch_g<32>(G, tk, tv, a, grid, s);
 }
