@@ -1,18 +1,27 @@
 """Benchmark of the paged-attention hot path on one GB300 (or N replicas).
 
-One step = one pass of the hot path over one batch of synthetic input:
-reshape_and_cache of the step's new tokens, then paged decode attention over
-every sequence (one layer).  The workload (default: the Llama-3-8B-shaped
-decode layer -- 64 seqs, ctx ~U[128,2048], 32q/8kv heads, D=128, B=16) is
-generated by the seeded generator in ``workloads``.  To keep reads coming from
-HBM, each step uses the next of NL layer pools (each a separate copy of the
-cache, together several times the 129 MB L2).
+One step = one pass of the hot path over one batch of synthetic input from the
+seeded generator in ``workloads``:
 
-Prints ONE JSON line.  ``value`` is algorithmic KV bytes per second (the K and
-V of every cached token read once, q read, out written, the new tokens'
-K/V read and written) over the device-timed step; ``e2e`` is the same metric
-through the C-ABI call with the step's inputs copied from pinned host memory
-and the output copied back inside the timed region.
+* decode workloads (default ``llama8b_decode``: 64 seqs, ctx ~U[128,2048],
+  32q/8kv heads, D=128, B=16; also ``long_context_decode``, ``tiny_decode``):
+  reshape_and_cache of the step's new tokens, then paged decode attention;
+* ``prefix_sharing``: 64 prompts x 4 samples over a 2048-token prefix built by
+  the host block manager; copy_blocks of the copy-on-write pairs,
+  reshape_and_cache of the appended tokens, decode over the shared tables;
+* ``mixed_step``: one reshape_and_cache of every new token, chunked prefill of
+  16 x 512 query tokens (tensor cores), decode of 240 sequences (B=32).
+
+To keep reads coming from HBM, each step uses the next of NL layer pools
+(separate copies of the cache, together several times the 129 MB L2).
+
+Prints ONE JSON line.  ``value`` is algorithmic HBM bytes per second over the
+device-timed step: every cached K/V byte a step must read once (shared
+prefix pages once), q read, out written, new tokens and copied pages read and
+written.  ``e2e`` is the same metric through the C-ABI calls with the step's
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region.  ``roofline`` covers the step's dominant kernel, timed with CUDA
+events on its launch stream.
 
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
 workload (the pages publish no runnable implementation to compare with).
@@ -22,6 +31,7 @@ data path; max time over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -31,6 +41,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Callable, Dict, List, Optional
 
 import numpy as np
 
@@ -39,8 +50,11 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-DECODE_KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_262_gb300", "csrc", "pa_decode.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
+CSRC = os.path.join(ROOT, "paged_kv_cache_262_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s"
+L2_BYTES = 129e6
+WORKLOADS = ["llama8b_decode", "long_context_decode", "tiny_decode", "prefix_sharing", "mixed_step"]
 
 
 def parse():
@@ -49,8 +63,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama8b_decode",
-                    choices=["llama8b_decode", "long_context_decode", "tiny_decode"])
+    ap.add_argument("--workload", default="llama8b_decode", choices=WORKLOADS)
+    ap.add_argument("--chunks", type=int, default=16, help="mixed_step: prefill chunks")
+    ap.add_argument("--decodes", type=int, default=240, help="mixed_step: decode sequences")
     ap.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0 = auto, > 4x L2)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -58,46 +73,31 @@ def parse():
     return ap.parse_args()
 
 
-# ------------------------------------------------------------------ helpers
-def make_case(name):
-    return {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
-            "tiny_decode": wl.tiny_decode}[name]()
-
-
-def algorithmic_bytes(case):
-    """Bytes the step must move at least once (see module docstring)."""
-    S, Hq, Hkv, D, B = case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size
-    ctx = case.context_lens.astype(np.int64)
-    kv = int(ctx.sum()) * Hkv * D * 2 * 2
-    qo = 2 * S * Hq * D * 2
-    tables = int(((ctx + B - 1) // B).sum()) * 4 + S * 4
-    decode = kv + qo + tables
-    T = 0 if case.slot_mapping is None else len(case.slot_mapping)
-    cache = T * Hkv * D * 2 * 2 * 2 + T * 8
-    return decode, cache
-
-
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         try:
             j = json.load(open(p))
-            return float(j["hbm_gbs"]), float(j.get("bf16_tflops", 1900.0)), "measured"
+            return {"hbm": float(j["hbm_gbs"]), "bf16": float(j["bf16_tflops"]),
+                    "bf16_sustained": float(j.get("bf16_tflops_sustained", j["bf16_tflops"])),
+                    "source": "measured"}
         except Exception:
             pass
-    return 6800.0, 1900.0, "fallback"
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-def decode_traffic_per_launch():
-    """dram read+write bytes per decode launch from the committed ncu capture,
-    or None when the kernel source changed since the capture."""
+def kernel_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch of `kernel` on `workload` from the
+    committed ncu capture, or None when the kernel's source changed since."""
     if not os.path.exists(TRAFFIC_FILE):
-        return None, None
-    j = json.load(open(TRAFFIC_FILE))
-    h = hashlib.sha256(open(DECODE_KERNEL_SRC, "rb").read()).hexdigest()
-    if j.get("kernel_sha256") != h:
-        return None, None
-    return j.get("bytes_per_launch"), j
+        return None
+    j = json.load(open(TRAFFIC_FILE)).get(f"{kernel}@{workload}")
+    if not j:
+        return None
+    src = os.path.join(CSRC, j["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != j["sha256"]:
+        return None
+    return j.get("bytes_per_launch")
 
 
 class ClockSampler:
@@ -119,8 +119,7 @@ class ClockSampler:
         except Exception:
             self.proc = None
             return
-        self.t = threading.Thread(target=self._read, daemon=True)
-        self.t.start()
+        threading.Thread(target=self._read, daemon=True).start()
 
     def _read(self):
         for line in self.proc.stdout:
@@ -135,12 +134,8 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        rows = []
-        for t, line in self.samples:
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            rows.append((t, f))
+        rows = [(t, [x.strip() for x in line.split(",")]) for t, line in self.samples]
+        rows = [(t, f) for t, f in rows if len(f) >= 9]
         win = [f for t, f in rows if t0 - 0.05 <= t <= t1 + 0.05]
         label = "timed"
         if not win:
@@ -156,14 +151,221 @@ class ClockSampler:
                 return None
         sm = [num(f[1]) for f in win if num(f[1]) is not None]
         reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for f in win:
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"], f[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": num(win[0][2]), "reasons": sorted(reasons), "samples": len(win),
-                "window": label}
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][2]),
+                "reasons": sorted(reasons), "samples": len(win), "window": label}
+
+
+# ------------------------------------------------------------------ workloads
+@dataclasses.dataclass
+class Bench:
+    """One workload's step: what it reads per step, what it launches, what it counts."""
+    name: str
+    describe: str
+    host_inputs: Dict[str, np.ndarray]        # per-step inputs (copied H2D in e2e)
+    step: Callable                            # step(i, inputs: dict of device tensors, ev) -> outputs list
+    step_bytes: int                           # algorithmic HBM bytes per step
+    launches: int                             # our kernels per step
+    kernel: str                               # dominant kernel
+    bound: str                                # "hbm" or "tensor"
+    kernel_work: float                        # bytes (hbm) or flops (tensor) per dominant launch
+    seqs: int
+    extra: Dict = dataclasses.field(default_factory=dict)
+    layers: int = 1
+    pool_mb: float = 0.0
+
+
+def decode_bytes(ctx, Hq, Hkv, D, B):
+    ctx = np.asarray(ctx, dtype=np.int64)
+    return int(ctx.sum()) * Hkv * D * 2 * 2 + 2 * len(ctx) * Hq * D * 2 + int(((ctx + B - 1) // B).sum()) * 4 \
+        + len(ctx) * 4
+
+
+def cache_bytes(T, Hkv, D):
+    return T * Hkv * D * 2 * 2 * 2 + T * 8
+
+
+def n_layers(args, pool_bytes):
+    n = args.layers or max(2, int(math.ceil(5 * L2_BYTES / max(pool_bytes, 1))))
+    return min(n, 64)
+
+
+def build_decode(args, torch, pa, dev, case):
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    NL = n_layers(args, case.k_pool.nbytes * 2)
+    kp0, vp0 = up(case.k_pool), up(case.v_pool)
+    kps = [kp0] + [kp0.clone() for _ in range(NL - 1)]
+    vps = [vp0] + [vp0.clone() for _ in range(NL - 1)]
+    desc = pa.make_desc(up(case.q), kp0, torch.from_numpy(case.block_tables), scale=case.scale,
+                        max_context_len=case.max_context_len)
+    ws = pa.decode_workspace(desc, dev)
+    stream = torch.cuda.current_stream()
+    outs = {"out": torch.empty((case.num_seqs, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device=dev)}
+
+    def step(i, x, ev):
+        l = i % NL
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
+        ev and ev[0].record(stream)
+        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], outs["out"], scale=case.scale,
+                                  max_context_len=case.max_context_len, workspace=ws, stream=stream)
+        ev and ev[1].record(stream)
+        return [outs["out"]]
+
+    dec = decode_bytes(case.context_lens, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size)
+    T = len(case.slot_mapping)
+    return Bench(case.name, f"{case.name}: {case.num_seqs} seqs, ctx {int(case.context_lens.min())}.."
+                 f"{int(case.context_lens.max())} (mean {case.context_lens.mean():.0f}), {case.num_q_heads}q/"
+                 f"{case.num_kv_heads}kv heads, D={case.head_dim}, B={case.block_size}, reshape_and_cache of {T} tokens",
+                 {"q": case.q, "new_k": case.new_k, "new_v": case.new_v, "slots": case.slot_mapping,
+                  "bt": case.block_tables, "ctx": case.context_lens},
+                 step, dec + cache_bytes(T, case.num_kv_heads, case.head_dim), 2, "decode_kernel", "hbm", dec,
+                 case.num_seqs, layers=NL, pool_mb=case.k_pool.nbytes * 2 / 1e6)
+
+
+def prefix_sharing_setup(pa):
+    """Tables, copy-on-write pairs and slots of the prefix-sharing workload,
+    produced by the host block manager (fork per prompt and per sample, then
+    one appended token per sample)."""
+    plan = wl.prefix_sharing_plan()
+    B, R = plan.B, plan.samples_per_prompt
+    bm = pa.BlockManager(plan.num_blocks, B)
+    root = 10 ** 6
+    bm.add_seq(root, plan.prefix_len)
+    for p in range(plan.num_prompts):
+        bm.fork(root, p * R)
+        for _ in range(int(plan.suffix_lens[p])):
+            bm.append(p * R)
+        for i in range(1, R):
+            bm.fork(p * R, p * R + i)
+    bm.free_seq(root)
+    S = plan.num_prompts * R
+    slots, pairs = [], []
+    for s in range(S):
+        slot, pair = bm.append(s)
+        slots.append(slot)
+        if pair is not None:
+            pairs.append(pair)
+    ctx = np.array([bm.seq_len(s) for s in range(S)], np.int32)
+    tables = [bm.block_table(s) for s in range(S)]
+    bt = np.full((S, max(len(t) for t in tables)), -1, np.int32)
+    for s, t in enumerate(tables):
+        bt[s, : len(t)] = t
+    return plan, bt, ctx, np.array(slots, np.int64), np.array(pairs, np.int64).reshape(-1, 2)
+
+
+def build_prefix(args, torch, pa, dev):
+    plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa)
+    kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    NL = n_layers(args, kp.nbytes * 2)
+    kp0, vp0 = up(kp), up(vp)
+    kps = [kp0] + [kp0.clone() for _ in range(NL - 1)]
+    vps = [vp0] + [vp0.clone() for _ in range(NL - 1)]
+    S, Hq, Hkv, D, B = len(ctx), plan.Hq, plan.Hkv, plan.D, plan.B
+    desc = pa.make_desc(up(q), kp0, torch.from_numpy(bt), max_context_len=int(ctx.max()))
+    ws = pa.decode_workspace(desc, dev)
+    stream = torch.cuda.current_stream()
+    outs = {"out": torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)}
+
+    def step(i, x, ev):
+        l = i % NL
+        pa.copy_blocks([kps[l]], [vps[l]], x["pairs"], stream=stream)
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
+        ev and ev[0].record(stream)
+        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], outs["out"],
+                                  max_context_len=int(ctx.max()), workspace=ws, stream=stream)
+        ev and ev[1].record(stream)
+        return [outs["out"]]
+
+    unique_pages = np.unique(bt[bt >= 0])
+    # unique KV bytes: every distinct page's tokens in use, once (pages are full except last ones)
+    uniq_tokens = 0
+    seen = set()
+    for s in range(S):
+        n = int(ctx[s])
+        for k, pg in enumerate(bt[s]):
+            if pg < 0 or pg in seen:
+                continue
+            seen.add(int(pg))
+            uniq_tokens += min(B, n - k * B)
+    kv_unique = uniq_tokens * Hkv * D * 2 * 2
+    dec_unique = kv_unique + 2 * S * Hq * D * 2 + int(((ctx.astype(np.int64) + B - 1) // B).sum()) * 4 + S * 4
+    dec_logical = decode_bytes(ctx, Hq, Hkv, D, B)
+    copy = len(pairs) * Hkv * B * D * 2 * 2 * 2
+    return Bench("prefix_sharing", f"prefix_sharing: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
+                 f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512], {Hq}q/{Hkv}kv, D={D}, B={B}; "
+                 f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + decode",
+                 {"q": q, "new_k": nk, "new_v": nv, "slots": slots, "pairs": pairs, "bt": bt, "ctx": ctx},
+                 step, dec_unique + copy + cache_bytes(S, Hkv, D), 3, "decode_kernel", "hbm", dec_unique, S,
+                 extra={"unique_pages": int(len(unique_pages)), "logical_decode_bytes": dec_logical,
+                        "unique_decode_bytes": dec_unique, "cow_pairs": int(len(pairs))},
+                 layers=NL, pool_mb=kp.nbytes * 2 / 1e6)
+
+
+def build_mixed(args, torch, pa, dev):
+    st = wl.Stream(0, 6)
+    cctx = st.integers(512, 8192, 16)[: args.chunks]
+    dctx = st.integers(64, 4096, 240)[: args.decodes]
+    m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, 32, seed=0, stream=105)
+    dec = m.decode
+    up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
+    NL = n_layers(args, dec.k_pool.nbytes * 2)
+    kp0, vp0 = up(dec.k_pool), up(dec.v_pool)
+    kps = [kp0] + [kp0.clone() for _ in range(NL - 1)]
+    vps = [vp0] + [vp0.clone() for _ in range(NL - 1)]
+    desc = pa.make_desc(up(dec.q), kp0, torch.from_numpy(dec.block_tables), max_context_len=dec.max_context_len)
+    ws = pa.decode_workspace(desc, dev)
+    stream = torch.cuda.current_stream()
+    T = int(m.cu_q[-1])
+    outs = {"pout": torch.empty((T, 32, 128), dtype=torch.bfloat16, device=dev),
+            "dout": torch.empty((dec.num_seqs, 32, 128), dtype=torch.bfloat16, device=dev)}
+    max_cctx = int(m.chunk_ctx.max())
+
+    def step(i, x, ev):
+        l = i % NL
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
+        ev and ev[0].record(stream)
+        pa.paged_attention_prefill_chunk(x["q_chunk"], x["cu_q"], kps[l], vps[l], x["chunk_bt"], x["chunk_ctx"],
+                                         outs["pout"], max_q_len=512, max_context_len=max_cctx, stream=stream)
+        ev and ev[1].record(stream)
+        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], outs["dout"],
+                                  max_context_len=dec.max_context_len, workspace=ws, stream=stream)
+        ev and ev[2].record(stream)
+        return [outs["pout"], outs["dout"]]
+
+    flops = 0
+    for r in range(len(cctx)):
+        c = int(cctx[r])
+        pos = np.arange(c - 512, c, dtype=np.int64)
+        flops += 4 * 128 * 32 * int((pos + 1).sum())
+    pre_bytes = int(np.asarray(cctx, np.int64).sum()) * 8 * 128 * 4 + 2 * T * 32 * 128 * 2
+    dbytes = decode_bytes(dec.context_lens, 32, 8, 128, 32)
+    Tn = T + dec.num_seqs
+    new_k = np.concatenate([m.chunk_new_k, dec.new_k])
+    new_v = np.concatenate([m.chunk_new_v, dec.new_v])
+    slots = np.concatenate([m.chunk_slots, dec.slot_mapping])
+    return Bench("mixed_step", f"mixed_step: {len(cctx)} prefill chunks x 512 tokens (ctx {int(cctx.min())}..{int(cctx.max())})"
+                 f" + {dec.num_seqs} decodes (ctx {int(dctx.min())}..{int(dctx.max())}), 32q/8kv, D=128, B=32; "
+                 f"reshape_and_cache of {Tn} tokens + prefill + decode",
+                 {"q_chunk": m.q_chunk, "cu_q": m.cu_q, "chunk_bt": m.chunk_tables, "chunk_ctx": m.chunk_ctx,
+                  "q": dec.q, "bt": dec.block_tables, "ctx": dec.context_lens, "new_k": new_k, "new_v": new_v,
+                  "slots": slots},
+                 step, pre_bytes + dbytes + cache_bytes(Tn, 8, 128), 3, "prefill_kernel", "tensor", flops,
+                 dec.num_seqs, extra={"prefill_flops": flops, "decode_bytes": dbytes, "prefill_kv_bytes": pre_bytes},
+                 layers=NL, pool_mb=dec.k_pool.nbytes * 2 / 1e6)
+
+
+def build(args, torch, pa, dev):
+    if args.workload == "prefix_sharing":
+        return build_prefix(args, torch, pa, dev)
+    if args.workload == "mixed_step":
+        return build_mixed(args, torch, pa, dev)
+    case = {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
+            "tiny_decode": wl.tiny_decode}[args.workload]()
+    return build_decode(args, torch, pa, dev, case)
 
 
 # ------------------------------------------------------------------ our arm
@@ -176,87 +378,67 @@ def run_ours(args, rank, world, local_rank):
     pa.load()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    case = make_case(args.workload)
-    dec_bytes, cache_bytes = algorithmic_bytes(case)
-    step_bytes = dec_bytes + cache_bytes
+    b = build(args, torch, pa, dev)
 
-    def up(a):
-        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint16).view(np.int16)).to(dev).view(
-            torch.bfloat16)
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if a.dtype == np.uint16:
+            t = t.view(torch.int16)
+        t = t.to(dev)
+        return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
 
-    pool_bytes = case.k_pool.nbytes * 2
-    l2 = 129e6
-    NL = args.layers or max(2, int(math.ceil(5 * l2 / max(pool_bytes, 1))))
-    NL = min(NL, 64)
-    kp0, vp0 = up(case.k_pool), up(case.v_pool)
-    kps = [kp0] + [kp0.clone() for _ in range(NL - 1)]
-    vps = [vp0] + [vp0.clone() for _ in range(NL - 1)]
-    q = up(case.q)
-    nk, nv = up(case.new_k), up(case.new_v)
-    slots = torch.from_numpy(case.slot_mapping).to(dev)
-    bt = torch.from_numpy(case.block_tables).to(dev)
-    ctx = torch.from_numpy(case.context_lens).to(dev)
-    out = torch.empty_like(q)
-    desc = pa.make_desc(q, kp0, bt, scale=case.scale, max_context_len=case.max_context_len)
-    ws = pa.decode_workspace(desc, dev)
+    x = {k: to_dev(v) for k, v in b.host_inputs.items()}
     stream = torch.cuda.current_stream()
-
-    def step(i, dq=q, dnk=nk, dnv=nv, dsl=slots, dbt=bt, dctx=ctx, dout=out, ev=None):
-        l = i % NL
-        pa.reshape_and_cache(dnk, dnv, kps[l], vps[l], dsl, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        pa.paged_attention_decode(dq, kps[l], vps[l], dbt, dctx, dout, scale=case.scale,
-                                  max_context_len=case.max_context_len, workspace=ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+    nev = 3 if b.kernel == "prefill_kernel" else 2
 
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.start()
         time.sleep(0.3)
     for i in range(args.warmup):
-        step(i)
+        b.step(i, x, None)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    # ---- timed region (device): K steps
-    t_wall0 = time.time()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
     torch.cuda.synchronize()
+    t_wall0 = time.time()
     e0.record(stream)
     for i in range(args.steps):
-        step(i, ev=dev_ev[i])
+        b.step(i, x, evs[i])
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     ms = e0.elapsed_time(e1)
-    dec_ms = statistics.mean(a.elapsed_time(b) for a, b in dev_ev)
-    dec_ms_median = statistics.median(a.elapsed_time(b) for a, b in dev_ev)
+    k_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    k_mean, k_median = statistics.mean(k_ms), statistics.median(k_ms)
+    side = {}
+    if nev == 3:
+        d_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
+        side["decode_launch_ms_mean"] = statistics.mean(d_ms)
+        side["decode_gbs"] = round(b.extra["decode_bytes"] / (side["decode_launch_ms_mean"] / 1e3) / 1e9, 1)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
-    # ---- e2e: same steps through the C-ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-        h_q, h_nk, h_nv = pin(q), pin(nk), pin(nv)
-        h_sl, h_bt, h_ctx = pin(slots), pin(bt), pin(ctx)
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q, d_nk, d_nv = torch.empty_like(q), torch.empty_like(nk), torch.empty_like(nv)
-        d_sl, d_bt, d_ctx = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(ctx)
-        d_out = torch.empty_like(out)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nk, h_nv, h_sl, h_bt, h_ctx))
-        d2h = h_out.numel() * h_out.element_size()
+        h_in = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16
+                                    else np.ascontiguousarray(v)).pin_memory() for k, v in b.host_inputs.items()}
+        d_in = {k: torch.empty_like(v, device=dev) for k, v in h_in.items()}
+        x2 = {k: (d_in[k].view(torch.bfloat16) if b.host_inputs[k].dtype == np.uint16 else d_in[k]) for k in d_in}
+        outs = b.step(0, x, None)
+        h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out)
 
         def e2e_step(i):
-            for d, h in ((d_q, h_q), (d_nk, h_nk), (d_nv, h_nv), (d_sl, h_sl), (d_bt, h_bt), (d_ctx, h_ctx)):
-                d.copy_(h, non_blocking=True)
-            step(i, d_q, d_nk, d_nv, d_sl, d_bt, d_ctx, d_out)
-            h_out.copy_(d_out, non_blocking=True)
+            for k in h_in:
+                d_in[k].copy_(h_in[k], non_blocking=True)
+            o = b.step(i, x2, None)
+            for hd, dd in zip(h_out, o):
+                hd.copy_(dd, non_blocking=True)
 
         for i in range(args.warmup):
             e2e_step(i)
@@ -274,119 +456,142 @@ def run_ours(args, rank, world, local_rank):
             t = torch.tensor([e2e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        e2e = {"value": step_bytes * args.steps * world / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / args.steps}
+        e2e = {"value": round(b.step_bytes * args.steps * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps}
     if sampler:
         sampler.stop()
-
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms = float(t.item())
     if rank != 0:
         return None
-    hbm_peak, _, peak_src = load_peaks()
-    dec_gbs = dec_bytes / (dec_ms / 1e3) / 1e9
-    traffic, _ = decode_traffic_per_launch()
-    value = step_bytes * args.steps * world / (ms / 1e3) / 1e9
+    peaks = load_peaks()
+    if b.bound == "hbm":
+        achieved = b.kernel_work / (k_mean / 1e3) / 1e9
+        peak, unit = peaks["hbm"], "GB/s"
+        peak_note = f"{peaks['source']} hbm_gbs (copy, read+write bytes)"
+    else:
+        achieved = b.kernel_work / (k_mean / 1e3) / 1e12
+        peak, unit = peaks["bf16_sustained"], "TFLOP/s"
+        peak_note = f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step); burst {peaks['bf16']}"
+    value = b.step_bytes * args.steps * world / (ms / 1e3) / 1e9
     res = {
-        "metric": "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s",
-        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{case.name}: {case.num_seqs} seqs, ctx {int(case.context_lens.min())}.."
-                               f"{int(case.context_lens.max())} (mean {case.context_lens.mean():.0f}), "
-                               f"{case.num_q_heads}q/{case.num_kv_heads}kv heads, D={case.head_dim}, "
-                               f"B={case.block_size}, reshape_and_cache of {len(case.slot_mapping)} tokens",
-                   "seqs": case.num_seqs, "layer_pools": NL,
-                   "l2": f"inputs larger than L2: {NL} layer pools of {pool_bytes / 1e6:.0f} MB rotated",
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": b.describe, "seqs": b.seqs, "layer_pools": b.layers,
+                   "l2": f"inputs larger than L2: {b.layers} layer pools of {b.pool_mb:.0f} MB rotated",
                    "parallelism": f"replicas{world}"},
-        "decode_tokens_per_s": round(case.num_seqs * args.steps * world / (ms / 1e3), 1),
-        "gpu_launches": 2 * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(dec_gbs, 1),
-                     "peak": hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs)"
-                     if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "unit": "GB/s", "frac": round(dec_gbs / hbm_peak, 4),
-                     "traffic": traffic, "algorithmic_bytes_per_launch": dec_bytes,
-                     "launch_ms_mean": dec_ms, "launch_ms_median": dec_ms_median},
+        "decode_tokens_per_s": round(b.seqs * args.steps * world / (ms / 1e3), 1),
+        "gpu_launches": b.launches * args.steps,
+        "roofline": {"bound": b.bound, "kernel": b.kernel, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_source": peak_note, "unit": unit, "frac": round(achieved / peak, 4),
+                     "traffic": kernel_traffic(b.kernel, b.name), "algorithmic_per_launch": b.kernel_work,
+                     "launch_ms_mean": k_mean, "launch_ms_median": k_median},
         "clocks": clocks,
     }
+    res.update(side)
+    if b.extra:
+        res["workload_extra"] = b.extra
     if e2e:
         res["e2e"] = e2e
     if not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(args, args.cpu_seconds)
     return res
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
-def oracle_units(case):
-    return [(s, g) for s in range(case.num_seqs) for g in range(case.num_kv_heads)]
-
-
-def time_oracle_units(ora, case, units):
-    """Runs the oracle on the given (seq, kv head) units (all G query heads of
-    each, plus the unit's share of the cache write); returns (seconds, bytes)."""
-    G = case.num_q_heads // case.num_kv_heads
-    D = case.head_dim
-    t0 = time.perf_counter()
-    nbytes = 0
-    for s, g in units:
-        for h in range(g * G, (g + 1) * G):
-            ora.decode_head(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens,
-                            case.scale, s, h)
-        nbytes += int(case.context_lens[s]) * D * 2 * 2 + 2 * G * D * 2
-    return time.perf_counter() - t0, nbytes
-
-
-def cpu_baseline(case, budget_s):
+def oracle_units(args):
+    """The workload as a list of oracle work units; each returns the algorithmic
+    bytes it covered.  Units are whole (sequence, kv head) decode units or whole
+    prefill rows (all heads of one query position)."""
     import oracle
     ora = oracle.default()
-    units = oracle_units(case)
-    # bounded sample: whole (seq, kv head) units in order until the budget is used
-    done, secs, nbytes = 0, 0.0, 0
+    units: List[Callable[[], int]] = []
+    if args.workload == "mixed_step":
+        st = wl.Stream(0, 6)
+        cctx = st.integers(512, 8192, 16)[: args.chunks]
+        dctx = st.integers(64, 4096, 240)[: args.decodes]
+        m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, 32, seed=0, stream=105)
+        kp, vp = m.decode.k_pool.copy(), m.decode.v_pool.copy()
+        ora.reshape_and_cache(m.chunk_new_k, m.chunk_new_v, kp, vp, m.chunk_slots)
+        for r in range(len(cctx)):
+            for i in range(512):
+                def u(r=r, i=i):
+                    for h in range(32):
+                        ora.prefill_row(m.q_chunk, m.cu_q, kp, vp, m.chunk_tables, m.chunk_ctx, m.decode.scale, r, i, h)
+                    return (int(cctx[r]) - 512 + i + 1) * 8 * 128 * 4
+                units.append(u)
+        return units, "prefill rows (all 32 heads of one query position)"
+    if args.workload == "prefix_sharing":
+        import paged_kv_cache_262_gb300 as pa
+        plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa)
+        kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
+        if len(pairs):
+            ora.copy_blocks([kp], [vp], pairs)
+        ora.reshape_and_cache(nk, nv, kp, vp, slots)
+        case = wl.DecodeCase("prefix_sharing", len(ctx), plan.Hq, plan.Hkv, plan.D, plan.B, plan.num_blocks,
+                             bt.shape[1], 1 / math.sqrt(plan.D), ctx, bt, q, kp, vp)
+    else:
+        case = {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
+                "tiny_decode": wl.tiny_decode}[args.workload]()
+        if case.new_k is not None:
+            ora.reshape_and_cache(case.new_k, case.new_v, case.k_pool, case.v_pool, case.slot_mapping)
+    G = case.num_q_heads // case.num_kv_heads
+    for s in range(case.num_seqs):
+        for g in range(case.num_kv_heads):
+            def u(s=s, g=g):
+                for h in range(g * G, (g + 1) * G):
+                    ora.decode_head(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens,
+                                    case.scale, s, h)
+                return int(case.context_lens[s]) * case.head_dim * 2 * 2 + 2 * G * case.head_dim * 2
+            units.append(u)
+    return units, "(sequence, kv head) decode units (all query heads of the group)"
+
+
+def cpu_baseline(args, budget_s):
+    units, kind = oracle_units(args)
+    secs, nbytes, done = 0.0, 0, 0
     while done < len(units) and secs < budget_s:
-        t, b = time_oracle_units(ora, case, units[done: done + 8])
-        secs += t
-        nbytes += b
-        done += 8
+        t0 = time.perf_counter()
+        nbytes += units[done]()
+        secs += time.perf_counter() - t0
+        done += 1
     return {"value": round(nbytes / secs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"fp64 C oracle, single thread, {min(done, len(units))} of {len(units)} "
-                      f"(seq, kv head) units of the same workload, {secs:.1f} s"}
+            "sample": f"fp64 C oracle, single thread: first {done} of {len(units)} {kind} of {args.workload}, "
+                      f"{secs:.1f} s"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    import oracle
     from oracle import build as obuild
     obuild.build()
-    ora = oracle.default()
-    case = make_case(args.workload)
-    units = oracle_units(case)
-    # size each step's sample so warmup + steps end within ~2 minutes
-    t_unit, _ = time_oracle_units(ora, case, units[:2])
-    t_unit /= 2
-    per_step = max(1, int((120.0 / max(args.steps + args.warmup, 1)) / max(t_unit, 1e-6)))
-    per_step = min(per_step, len(units))
-    k = 0
+    units, kind = oracle_units(args)
+    t0 = time.perf_counter()
+    units[0]()
+    t_unit = max(time.perf_counter() - t0, 1e-6)
+    per_step = max(1, min(len(units), int((120.0 / max(args.steps + args.warmup, 1)) / t_unit)))
+    k = 1
     for _ in range(args.warmup):
-        time_oracle_units(ora, case, [units[(k + j) % len(units)] for j in range(per_step)])
-        k += per_step
+        for _ in range(per_step):
+            units[k % len(units)]()
+            k += 1
     secs, nbytes = 0.0, 0
     for _ in range(args.steps):
-        t, b = time_oracle_units(ora, case, [units[(k + j) % len(units)] for j in range(per_step)])
-        k += per_step
-        secs += t
-        nbytes += b
+        t0 = time.perf_counter()
+        for _ in range(per_step):
+            nbytes += units[k % len(units)]()
+            k += 1
+        secs += time.perf_counter() - t0
     value = nbytes / secs / 1e9
-    return {"impl": "reference", "metric": "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s",
-            "value": round(value, 6), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": case.name, "parallelism": "single host thread"},
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "parallelism": "single host thread"},
             "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{per_step} (seq, kv head) unit(s) of {case.name} per step"},
+                             "sample": f"{per_step} {kind} of {args.workload} per step"},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
