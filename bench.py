@@ -159,6 +159,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(win), "window": label}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (ranks run independent replicas; the job
+    takes as long as its slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
 # ------------------------------------------------------------------ workloads
 @dataclasses.dataclass
 class Bench:
@@ -451,19 +467,12 @@ def run_ours(args, rank, world, local_rank):
             e2e_step(i)
         f1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = f0.elapsed_time(f1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(b.step_bytes * args.steps * world / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
+        e2e = {"value": round(job_throughput(b.step_bytes, args.steps, world, e2e_ms), 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps}
     if sampler:
         sampler.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     if rank != 0:
         return None
     peaks = load_peaks()
@@ -475,7 +484,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = b.kernel_work / (k_mean / 1e3) / 1e12
         peak, unit = peaks["bf16_sustained"], "TFLOP/s"
         peak_note = f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step); burst {peaks['bf16']}"
-    value = b.step_bytes * args.steps * world / (ms / 1e3) / 1e9
+    value = job_throughput(b.step_bytes, args.steps, world, ms)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
