@@ -15,10 +15,11 @@
 // 128/G consecutive positions x the G query heads that share the kv head, so
 // each K/V tile serves the whole GQA group.  Roles (6 warps):
 //   warps 0-3  load the Q tile, run the softmax of one row each (TMEM lane =
-//              row), write P (bf16) into shared memory, rescale O, and store
-//              the output;
+//              row), write P (bf16) into one of two shared-memory buffers,
+//              rescale O, and store the output;
 //   warp 4     gathers 128-key K and V tiles page by page with 2-D TMA
-//              (128-byte swizzle) into a two-stage ring;
+//              (128-byte swizzle) into two-stage rings; a K stage is refilled
+//              as soon as its S MMA is done, a V stage once its PV MMA is;
 //   warp 5     owns the TMEM allocation and issues the MMAs:
 //              S_j = Q K_j^T (fp32, TMEM, double buffered) and
 //              O += P_j V_j (fp32, TMEM; V read MN-major).
@@ -59,13 +60,19 @@ constexpr int kTile = 32768;    // 128 x 128 bf16
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr int kOffP = kOffV + 2 * kTile;
-constexpr int kOffBar = kOffP + kTile;
+constexpr int kOffP = kOffV + 2 * kTile;     // 2 buffers
+constexpr int kOffBar = kOffP + 2 * kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
 constexpr int kThreads = 192;
 
-enum { BAR_Q = 0, BAR_KV_FULL = 1, BAR_KV_EMPTY = 3, BAR_S_FULL = 5, BAR_P_FULL = 7, BAR_PV_DONE = 8, NBARS = 9 };
+// Barriers (pairs are indexed by tile parity): Q loaded; K stage full / free
+// (free once S_j is done); V stage full / free (free once PV_j is done); S
+// buffer full; P buffer written; PV MMA of the tile done.
+enum {
+  BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = 3, BAR_V_FULL = 5, BAR_V_EMPTY = 7, BAR_S_FULL = 9,
+  BAR_P_FULL = 11, BAR_PV_DONE = 13, NBARS = 15
+};
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return pack_bf16(a, b); }
 
@@ -113,14 +120,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[BAR_Q], 128);
-    mbar_init(&bars[BAR_KV_FULL], 1);
-    mbar_init(&bars[BAR_KV_FULL + 1], 1);
-    mbar_init(&bars[BAR_KV_EMPTY], 1);
-    mbar_init(&bars[BAR_KV_EMPTY + 1], 1);
-    mbar_init(&bars[BAR_S_FULL], 1);
-    mbar_init(&bars[BAR_S_FULL + 1], 1);
+    for (int b = BAR_K_FULL; b < BAR_P_FULL; ++b) mbar_init(&bars[b], 1);
     mbar_init(&bars[BAR_P_FULL], 128);
+    mbar_init(&bars[BAR_P_FULL + 1], 128);
     mbar_init(&bars[BAR_PV_DONE], 1);
+    mbar_init(&bars[BAR_PV_DONE + 1], 1);
     *dead = 0;
     fence_mbar_init();
   }
@@ -145,11 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       const int32_t *bt_row = a.bt + (size_t)r * a.max_blocks;
-      for (int j = 0; j < T; ++j) {
-        const int st = j & 1;
-        if (j >= 2 && !wait(BAR_KV_EMPTY + st, (uint32_t)(((j >> 1) - 1) & 1))) break;
-        int pages[PAGES];
-        int n = 0;
+      auto page_ids = [&](int j, int (&pages)[PAGES]) {  // validated ids of tile j, -1 = none
 #pragma unroll
         for (int i = 0; i < PAGES; ++i) {
           const int pi = j * PAGES + i;
@@ -162,26 +162,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           pages[i] = pg;
-          n += pg >= 0;
         }
-        uint64_t *bar = &bars[BAR_KV_FULL + st];
+      };
+      auto load = [&](const int (&pages)[PAGES], uint64_t *bar, uint8_t *dst, const CUtensorMap *map) {
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < PAGES; ++i) n += pages[i] >= 0;
         if (n == 0) {
           mbar_arrive(bar);
-          continue;
+          return;
         }
-        mbar_arrive_expect_tx(bar, (uint32_t)n * B * 128 * 4);
-        uint8_t *kd = smem + kOffK + st * kTile;
-        uint8_t *vd = smem + kOffV + st * kTile;
+        mbar_arrive_expect_tx(bar, (uint32_t)n * B * 256);
 #pragma unroll
         for (int i = 0; i < PAGES; ++i) {
           if (pages[i] < 0) continue;
           const int row = (pages[i] * a.Hkv + g) * B;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tma_load_2d_hint(kd + h * kHalf + i * B * 128, &tmK, h * 64, row, bar, pol);
-            tma_load_2d_hint(vd + h * kHalf + i * B * 128, &tmV, h * 64, row, bar, pol);
-          }
+          tma_load_2d_hint(dst + i * B * 128, map, 0, row, bar, pol);
+          tma_load_2d_hint(dst + kHalf + i * B * 128, map, 64, row, bar, pol);
         }
+      };
+      int cur[PAGES], nxt[PAGES];
+      page_ids(0, cur);
+      for (int j = 0; j < T; ++j) {
+        const int st = j & 1;
+        const uint32_t par = (uint32_t)(((j >> 1) - 1) & 1);
+        if (j + 1 < T) page_ids(j + 1, nxt);  // table reads of the next tile overlap this one
+        if (j >= 2 && !wait(BAR_K_EMPTY + st, par)) break;
+        load(cur, &bars[BAR_K_FULL + st], smem + kOffK + st * kTile, &tmK);
+        if (j >= 2 && !wait(BAR_V_EMPTY + st, par)) break;
+        load(cur, &bars[BAR_V_FULL + st], smem + kOffV + st * kTile, &tmV);
+#pragma unroll
+        for (int i = 0; i < PAGES; ++i) cur[i] = nxt[i];
       }
     }
   } else if (warp == 5) {
@@ -199,29 +210,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kIdS, kk > 0);
         }
         umma_commit(&bars[BAR_S_FULL + st]);
+        umma_commit(&bars[BAR_K_EMPTY + st]);
       };
-      bool ok = wait(BAR_Q, 0) && wait(BAR_KV_FULL, 0);
+      bool ok = wait(BAR_Q, 0) && wait(BAR_K_FULL, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
       for (int j = 0; ok && j < T; ++j) {
         if (j + 1 < T) {
-          if (!wait(BAR_KV_FULL + ((j + 1) & 1), (uint32_t)(((j + 1) >> 1) & 1))) break;
+          if (!wait(BAR_K_FULL + ((j + 1) & 1), (uint32_t)(((j + 1) >> 1) & 1))) break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!wait(BAR_P_FULL, (uint32_t)(j & 1))) break;
+        if (!wait(BAR_V_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_P_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
         tc_fence_after();
         const uint32_t vb = sv + (j & 1) * kTile;
+        const uint32_t pb = sp + (j & 1) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + 256, umma_desc_sw128(sp + aoff, 16, 1024),
+          umma_bf16(tmem + 256, umma_desc_sw128(pb + aoff, 16, 1024),
                     umma_desc_sw128(vb + kk * 2048, kHalf, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars[BAR_PV_DONE]);
-        umma_commit(&bars[BAR_KV_EMPTY + (j & 1)]);
+        umma_commit(&bars[BAR_PV_DONE + (j & 1)]);
+        umma_commit(&bars[BAR_V_EMPTY + (j & 1)]);
       }
     }
   } else {
@@ -245,7 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     float m_run = -INFINITY, l_run = 0.f;
-    uint8_t *pd = smem + kOffP;
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
       if (!wait(BAR_S_FULL + st, (uint32_t)((j >> 1) & 1))) break;
@@ -260,27 +273,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
       const int key0 = j * kBN;
-      float mx = -INFINITY;
-      if (key0 + kBN - 1 <= pos_lo) {  // every key visible to every row of the tile
+      float mx = -INFINITY;  // max of the raw scores (scale > 0 keeps the order)
+      if (key0 + kBN - 1 > pos_lo) {  // some key past some row's position: mask
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          s[i] *= a.scale_log2;
-          mx = fmaxf(mx, s[i]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          s[i] = (key0 + i <= pos) ? s[i] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[i]);
-        }
+        for (int i = 0; i < kBN; ++i) s[i] = (key0 + i <= pos) ? s[i] : -INFINITY;
       }
-      const float m_new = fmaxf(m_run, mx);
+#pragma unroll
+      for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      const float m_new = fmaxf(m_run, mx * a.scale_log2);
       const bool rescale = m_new > m_run + 8.f;
       const float m_use = rescale ? m_new : m_run;
       const float alpha = rescale ? exp2f(m_run - m_new) : 1.f;
       // value rows of keys past the context must not carry NaNs into 0 * v
       if (key0 + kBN > ctx) {
-        if (!wait(BAR_KV_FULL + st, (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_V_FULL + st, (uint32_t)((j >> 1) & 1))) break;
         if (key0 + m >= ctx) {
           uint8_t *vd = smem + kOffV + st * kTile;
 #pragma unroll
@@ -290,40 +296,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (j >= 1) {
-        if (!wait(BAR_PV_DONE, (uint32_t)((j - 1) & 1))) break;  // O stable, P buffer free
-        tc_fence_after();
-        if (rescale) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t v[32];
-            tmem_ld32(lane_base + 256 + c * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(lane_base + 256 + c * 32, v);
-          }
-          tmem_wait_st();
-        }
-      }
+      // P buffer j%2 was last read by PV_{j-2}
+      if (j >= 2 && !wait(BAR_PV_DONE + st, (uint32_t)(((j - 2) >> 1) & 1))) break;
+      uint8_t *pd = smem + kOffP + st * kTile;
       float lsum = 0.f;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          w[e] = pack2(exp2f(s[c * 8 + 2 * e] - m_use), exp2f(s[c * 8 + 2 * e + 1] - m_use));
+          w[e] = pack2(exp2f(fmaf(s[c * 8 + 2 * e], a.scale_log2, -m_use)),
+                       exp2f(fmaf(s[c * 8 + 2 * e + 1], a.scale_log2, -m_use)));
           lsum += bf16_lo(w[e]) + bf16_hi(w[e]);
         }
         *reinterpret_cast<uint4 *>(pd + (c >> 3) * kHalf + sw128(m, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      if (rescale && j >= 1) {  // O accumulated through PV_{j-1} must be final before scaling
+        if (!wait(BAR_PV_DONE + (st ^ 1), (uint32_t)(((j - 1) >> 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + 256 + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(lane_base + 256 + c * 32, v);
+        }
+        tmem_wait_st();
       }
       l_run = l_run * alpha + lsum;
       m_run = m_use;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[BAR_P_FULL]);
+      mbar_arrive(&bars[BAR_P_FULL + st]);
     }
-    if (wait(BAR_PV_DONE, (uint32_t)((T - 1) & 1))) {
+    if (wait(BAR_PV_DONE + ((T - 1) & 1), (uint32_t)(((T - 1) >> 1) & 1))) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
