@@ -11,18 +11,25 @@
 // query tokens over a context of ctx tokens (the chunk included) places query
 // row i at position ctx - C + i; it attends keys 0 .. ctx - C + i.
 //
-// One CTA per (query tile, kv head, chunk).  A query tile is 128 MMA rows:
-// 128/G consecutive positions x the G query heads that share the kv head, so
-// each K/V tile serves the whole GQA group.  Roles (6 warps):
-//   warps 0-3  load the Q tile, run the softmax of one row each (TMEM lane =
-//              row), write P (bf16) into one of two shared-memory buffers,
-//              rescale O, and store the output;
-//   warp 4     gathers 128-key K and V tiles page by page with 2-D TMA
+// One CTA per (pair of query tiles, kv head, chunk).  A query tile is 128 MMA
+// rows: 128/G consecutive positions x the G query heads that share the kv
+// head; the CTA holds two consecutive tiles (A and B), so every K/V tile it
+// loads serves 256 rows.  Roles (10 warps):
+//   warps 0-3  tile A: load its Q rows, softmax of one row each (TMEM lane =
+//              row), write P (bf16) back into TMEM over its S, rescale O,
+//              store the output;
+//   warps 4-7  the same for tile B;
+//   warp 8     gathers 128-key K and V tiles page by page with 2-D TMA
 //              (128-byte swizzle) into two-stage rings; a K stage is refilled
-//              as soon as its S MMA is done, a V stage once its PV MMA is;
-//   warp 5     owns the TMEM allocation and issues the MMAs:
-//              S_j = Q K_j^T (fp32, TMEM, double buffered) and
-//              O += P_j V_j (fp32, TMEM; V read MN-major).
+//              once both S MMAs of its tile are done, a V stage once both PV
+//              MMAs are;
+//   warp 9     owns the TMEM allocation and issues the MMAs in the order
+//              S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...:
+//              S = Q K^T (A and B from shared memory, fp32 into TMEM) and
+//              O += P V (P from TMEM, V MN-major from shared memory).
+// MMAs issued by one thread complete in order, so an S MMA that reuses the
+// TMEM columns of the previous tile's P runs after the PV MMA that read them,
+// and a completed S tells the softmax that the previous PV is done.
 // The softmax keeps a running max per row in base 2 and rescales O only when
 // the max grows by more than 8 (2^8); until then probabilities are taken
 // against the stale max, which the final normalisation by the same running
@@ -53,25 +60,23 @@ struct PrefillArgs {
 };
 
 constexpr int kD = 128;         // head_dim
-constexpr int kBM = 128;        // MMA rows per tile
-constexpr int kBN = 128;        // keys per tile
+constexpr int kBM = 128;        // MMA rows per query tile (two tiles per CTA)
+constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kHalf = 16384;    // one 64-column half of a 128 x 128 bf16 tile
 constexpr int kTile = 32768;    // 128 x 128 bf16
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;      // 2 stages
+constexpr int kOffQ = 0;                  // tiles A, B
+constexpr int kOffK = kOffQ + 2 * kTile;  // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr int kOffP = kOffV + 2 * kTile;     // 2 buffers
-constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kOffBar = kOffV + 2 * kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;
-constexpr int kTmemCols = 512;  // S0 [0,128), S1 [128,256), O [256,384)
-constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;  // S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512)
+constexpr int kThreads = 320;
 
-// Barriers (pairs are indexed by tile parity): Q loaded; K stage full / free
-// (free once S_j is done); V stage full / free (free once PV_j is done); S
-// buffer full; P buffer written; PV MMA of the tile done.
+// Barriers: Q rows stored (both tiles); K and V stage full / free (pairs by
+// tile parity); S of tile A / B ready; P of tile A / B written; all MMAs done.
 enum {
   BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = 3, BAR_V_FULL = 5, BAR_V_EMPTY = 7, BAR_S_FULL = 9,
-  BAR_P_FULL = 11, BAR_PV_DONE = 13, NBARS = 15
+  BAR_P_FULL = 11, BAR_O_DONE = 13, NBARS = 14
 };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return pack_bf16(a, b); }
@@ -80,7 +85,7 @@ template <int B, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const PrefillArgs a) {
-  constexpr int TP = kBM / G;        // positions per tile
+  constexpr int TP = kBM / G;        // positions per query tile
   constexpr int PAGES = kBN / B;     // pages per key tile
   constexpr uint32_t kIdS = umma_idesc_bf16(128, 128, false, false);
   constexpr uint32_t kIdPV = umma_idesc_bf16(128, 128, false, true);
@@ -97,13 +102,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int c0 = __ldg(a.cu_q + r), c1 = __ldg(a.cu_q + r + 1);
   const int C = c1 - c0;
   const int ctx = __ldg(a.ctx + r);
-  const int q0 = qt * TP;
+  const int q0 = qt * 2 * TP;  // first position index of tile A
   if (C <= 0 || q0 >= C) return;
   const bool bad = ctx <= 0 || C > ctx || ctx > a.max_blocks * B || ctx > a.max_ctx || c0 < 0 ||
                    c1 > a.total_q;
-  if (bad) {  // zero this tile's rows, report
+  if (bad) {  // zero this CTA's rows, report
     if (c0 >= 0 && c1 <= a.total_q) {
-      for (int m = threadIdx.x; m < kBM; m += kThreads) {
+      for (int m = threadIdx.x; m < 2 * kBM; m += kThreads) {
         const int t = q0 + m / G;
         if (t >= C) continue;
         uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + t) * a.Hq + g * G + m % G) * kD);
@@ -114,21 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
   const int npages = (ctx + B - 1) / B;
-  const int pos_lo = ctx - C + q0;                     // first position of the tile
-  const int pos_hi = ctx - C + min(C, q0 + TP) - 1;    // last valid position
-  const int T = pos_hi / kBN + 1;                      // key tiles
+  const int pos_hi = ctx - C + min(C, q0 + 2 * TP) - 1;  // last valid position of the CTA
+  const int T = pos_hi / kBN + 1;                         // key tiles
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[BAR_Q], 128);
+    mbar_init(&bars[BAR_Q], 256);
     for (int b = BAR_K_FULL; b < BAR_P_FULL; ++b) mbar_init(&bars[b], 1);
     mbar_init(&bars[BAR_P_FULL], 128);
     mbar_init(&bars[BAR_P_FULL + 1], 128);
-    mbar_init(&bars[BAR_PV_DONE], 1);
-    mbar_init(&bars[BAR_PV_DONE + 1], 1);
+    mbar_init(&bars[BAR_O_DONE], 1);
     *dead = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(tslot, kTmemCols);
     tmem_relinquish();
   }
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -195,59 +198,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < PAGES; ++i) cur[i] = nxt[i];
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t sq = smem_u32(smem + kOffQ), sk = smem_u32(smem + kOffK);
-      const uint32_t sv = smem_u32(smem + kOffV), sp = smem_u32(smem + kOffP);
-      auto issue_s = [&](int j) {
-        const int st = j & 1;
-        const uint32_t kb = sk + st * kTile;
+      const uint32_t sv = smem_u32(smem + kOffV);
+      auto issue_s = [&](int x, int j) {  // S of tile x (0 = A, 1 = B) against K tile j
+        const uint32_t kb = sk + (j & 1) * kTile, qb = sq + x * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + st * 128, umma_desc_sw128(sq + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
+          umma_bf16(tmem + x * 128, umma_desc_sw128(qb + off, 16, 1024), umma_desc_sw128(kb + off, 16, 1024),
                     kIdS, kk > 0);
         }
-        umma_commit(&bars[BAR_S_FULL + st]);
-        umma_commit(&bars[BAR_K_EMPTY + st]);
+        umma_commit(&bars[BAR_S_FULL + x]);
+      };
+      auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j, P_x from TMEM
+        const uint32_t vb = sv + (j & 1) * kTile;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, umma_desc_sw128(vb + kk * 2048, kHalf, 1024),
+                       kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = wait(BAR_Q, 0) && wait(BAR_K_FULL, 0);
       if (ok) {
         tc_fence_after();
-        issue_s(0);
+        issue_s(0, 0);
+        issue_s(1, 0);
+        umma_commit(&bars[BAR_K_EMPTY]);
       }
       for (int j = 0; ok && j < T; ++j) {
-        if (j + 1 < T) {
+        const bool more = j + 1 < T;
+        const uint32_t par = (uint32_t)(j & 1);
+        if (!wait(BAR_V_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_P_FULL, par)) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (more) {
           if (!wait(BAR_K_FULL + ((j + 1) & 1), (uint32_t)(((j + 1) >> 1) & 1))) break;
           tc_fence_after();
-          issue_s(j + 1);
+          issue_s(0, j + 1);
         }
-        if (!wait(BAR_V_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
-        if (!wait(BAR_P_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_P_FULL + 1, par)) break;
         tc_fence_after();
-        const uint32_t vb = sv + (j & 1) * kTile;
-        const uint32_t pb = sp + (j & 1) * kTile;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + 256, umma_desc_sw128(pb + aoff, 16, 1024),
-                    umma_desc_sw128(vb + kk * 2048, kHalf, 1024), kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars[BAR_PV_DONE + (j & 1)]);
+        issue_pv(1, j);
         umma_commit(&bars[BAR_V_EMPTY + (j & 1)]);
+        if (more) {
+          issue_s(1, j + 1);
+          umma_commit(&bars[BAR_K_EMPTY + ((j + 1) & 1)]);
+        }
       }
+      umma_commit(&bars[BAR_O_DONE]);
     }
   } else {
-    // ---------------------------------------------------- softmax (row = m)
-    const int m = warp * 32 + lane;
-    const int tloc = q0 + m / G;                 // position index within the chunk
+    // ------------------------------------- softmax: tile x, row m = TMEM lane
+    const int x = warp >> 2;
+    const int m = (warp & 3) * 32 + lane;
+    const int tloc = q0 + x * TP + m / G;  // position index within the chunk
     const bool row_valid = tloc < C;
     const int pos = row_valid ? ctx - C + tloc : ctx - 1;
+    const int pos_lo = ctx - C + q0 + x * TP;  // first position of this tile
     const int head = g * G + m % G;
-    // Q row -> shared memory (128-byte swizzle, two 64-column halves)
-    {
-      uint8_t *qd = smem + kOffQ;
+    {  // Q row -> shared memory (128-byte swizzle, two 64-column halves)
+      uint8_t *qd = smem + kOffQ + x * kTile;
       const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
@@ -257,27 +270,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars[BAR_Q]);
     }
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t s_col = x * 128, o_col = 256 + x * 128;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
-      if (!wait(BAR_S_FULL + st, (uint32_t)((j >> 1) & 1))) break;
+      if (!wait(BAR_S_FULL + x, (uint32_t)(j & 1))) break;
       tc_fence_after();
       float s[kBN];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + st * 128 + c * 32, v);
+        tmem_ld32(lane_base + s_col + c * 32, v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
       const int key0 = j * kBN;
-      float mx = -INFINITY;  // max of the raw scores (scale > 0 keeps the order)
       if (key0 + kBN - 1 > pos_lo) {  // some key past some row's position: mask
 #pragma unroll
         for (int i = 0; i < kBN; ++i) s[i] = (key0 + i <= pos) ? s[i] : -INFINITY;
       }
+      float mx = -INFINITY;  // max of the raw scores (scale > 0 keeps the order)
 #pragma unroll
       for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
       const float m_new = fmaxf(m_run, mx * a.scale_log2);
@@ -285,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_use = rescale ? m_new : m_run;
       const float alpha = rescale ? exp2f(m_run - m_new) : 1.f;
       // value rows of keys past the context must not carry NaNs into 0 * v
-      if (key0 + kBN > ctx) {
+      // (tile A's PV runs first, so tile A's threads clear them)
+      if (x == 0 && key0 + kBN > ctx) {
         if (!wait(BAR_V_FULL + st, (uint32_t)((j >> 1) & 1))) break;
         if (key0 + m >= ctx) {
           uint8_t *vd = smem + kOffV + st * kTile;
@@ -294,51 +309,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4 *>(vd + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4 *>(vd + kHalf + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async_smem();
         }
       }
-      // P buffer j%2 was last read by PV_{j-2}
-      if (j >= 2 && !wait(BAR_PV_DONE + st, (uint32_t)(((j - 2) >> 1) & 1))) break;
-      uint8_t *pd = smem + kOffP + st * kTile;
+      // P (bf16 pairs) over the first 64 columns of this tile's S
       float lsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        uint32_t w[4];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          w[e] = pack2(exp2f(fmaf(s[c * 8 + 2 * e], a.scale_log2, -m_use)),
-                       exp2f(fmaf(s[c * 8 + 2 * e + 1], a.scale_log2, -m_use)));
+        for (int e = 0; e < 32; ++e) {
+          const int k = c * 64 + 2 * e;
+          w[e] = pack2(exp2f(fmaf(s[k], a.scale_log2, -m_use)), exp2f(fmaf(s[k + 1], a.scale_log2, -m_use)));
           lsum += bf16_lo(w[e]) + bf16_hi(w[e]);
         }
-        *reinterpret_cast<uint4 *>(pd + (c >> 3) * kHalf + sw128(m, c & 7)) = make_uint4(w[0], w[1], w[2], w[3]);
+        tmem_st32(lane_base + s_col + c * 32, w);
       }
-      if (rescale && j >= 1) {  // O accumulated through PV_{j-1} must be final before scaling
-        if (!wait(BAR_PV_DONE + (st ^ 1), (uint32_t)(((j - 1) >> 1) & 1))) break;
-        tc_fence_after();
+      if (rescale && j >= 1) {  // the previous PV of this tile is done (S of tile j followed it)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
-          tmem_ld32(lane_base + 256 + c * 32, v);
+          tmem_ld32(lane_base + o_col + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(lane_base + 256 + c * 32, v);
+          tmem_st32(lane_base + o_col + c * 32, v);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       l_run = l_run * alpha + lsum;
       m_run = m_use;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars[BAR_P_FULL + st]);
+      mbar_arrive(&bars[BAR_P_FULL + x]);
     }
-    if (wait(BAR_PV_DONE + ((T - 1) & 1), (uint32_t)(((T - 1) >> 1) & 1))) {
+    if (wait(BAR_O_DONE, 0)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        tmem_ld32(lane_base + 256 + c * 32, v);
+        tmem_ld32(lane_base + o_col + c * 32, v);
         tmem_wait_ld();
         if (row_valid) {
 #pragma unroll
@@ -356,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -404,7 +415,7 @@ extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const v
   if (!q || !cu_q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PA_ERR_INVALID;
   if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
-  const long long tiles = ((long long)max_q_len * G + kBM - 1) / kBM;
+  const long long tiles = ((long long)max_q_len * G + 2 * kBM - 1) / (2 * kBM);
   if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
   const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
   CUtensorMap tk, tv;
