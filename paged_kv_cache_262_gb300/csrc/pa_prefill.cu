@@ -20,7 +20,8 @@
 //              store the output;
 //   warps 4-7  the same for tile B;
 //   warp 8     gathers 128-key K and V tiles page by page with 2-D TMA
-//              (128-byte swizzle) into two-stage rings; a K stage is refilled
+//              (128-byte swizzle) into two-stage K and V rings; a K
+//              stage is refilled
 //              once both S MMAs of its tile are done, a V stage once both PV
 //              MMAs are;
 //   warp 9     owns the TMEM allocation and issues the MMAs in the order
@@ -64,20 +65,28 @@ constexpr int kBM = 128;        // MMA rows per query tile (two tiles per CTA)
 constexpr int kBN = 128;        // keys per K/V tile
 constexpr int kHalf = 16384;    // one 64-column half of a 128 x 128 bf16 tile
 constexpr int kTile = 32768;    // 128 x 128 bf16
+#ifndef PA_PREFILL_KST
+#define PA_PREFILL_KST 2
+#endif
+constexpr int KST = PA_PREFILL_KST;       // K ring depth
+constexpr int VST = 2;                    // V ring depth
 constexpr int kOffQ = 0;                  // tiles A, B
-constexpr int kOffK = kOffQ + 2 * kTile;  // 2 stages
-constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr int kOffBar = kOffV + 2 * kTile;
+constexpr int kOffK = kOffQ + 2 * kTile;
+constexpr int kOffV = kOffK + KST * kTile;
+constexpr int kOffBar = kOffV + VST * kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr int kTmemCols = 512;  // S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512)
 constexpr int kThreads = 320;
 
-// Barriers: Q rows stored (both tiles); K and V stage full / free (pairs by
-// tile parity); S of tile A / B ready; P of tile A / B written; all MMAs done.
+// Barriers: Q rows stored (both tiles); K and V stage full / free (one per
+// ring slot); S of tile A / B ready; P of tile A / B written; all MMAs done.
 enum {
-  BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = 3, BAR_V_FULL = 5, BAR_V_EMPTY = 7, BAR_S_FULL = 9,
-  BAR_P_FULL = 11, BAR_O_DONE = 13, NBARS = 14
+  BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST, BAR_V_FULL = BAR_K_EMPTY + KST,
+  BAR_V_EMPTY = BAR_V_FULL + VST, BAR_S_FULL = BAR_V_EMPTY + VST, BAR_P_FULL = BAR_S_FULL + 2,
+  BAR_O_DONE = BAR_P_FULL + 2, NBARS = BAR_O_DONE + 1
 };
+static_assert(NBARS * 8 + 8 <= 256, "barrier area");
+static_assert(kOffBar + 256 + 1024 <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return pack_bf16(a, b); }
 
@@ -187,13 +196,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int cur[PAGES], nxt[PAGES];
       page_ids(0, cur);
       for (int j = 0; j < T; ++j) {
-        const int st = j & 1;
-        const uint32_t par = (uint32_t)(((j >> 1) - 1) & 1);
+        const int ks = j % KST, vs = j % VST;
         if (j + 1 < T) page_ids(j + 1, nxt);  // table reads of the next tile overlap this one
-        if (j >= 2 && !wait(BAR_K_EMPTY + st, par)) break;
-        load(cur, &bars[BAR_K_FULL + st], smem + kOffK + st * kTile, &tmK);
-        if (j >= 2 && !wait(BAR_V_EMPTY + st, par)) break;
-        load(cur, &bars[BAR_V_FULL + st], smem + kOffV + st * kTile, &tmV);
+        if (j >= KST && !wait(BAR_K_EMPTY + ks, (uint32_t)((j / KST - 1) & 1))) break;
+        load(cur, &bars[BAR_K_FULL + ks], smem + kOffK + ks * kTile, &tmK);
+        if (j >= VST && !wait(BAR_V_EMPTY + vs, (uint32_t)((j / VST - 1) & 1))) break;
+        load(cur, &bars[BAR_V_FULL + vs], smem + kOffV + vs * kTile, &tmV);
 #pragma unroll
         for (int i = 0; i < PAGES; ++i) cur[i] = nxt[i];
       }
@@ -204,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sq = smem_u32(smem + kOffQ), sk = smem_u32(smem + kOffK);
       const uint32_t sv = smem_u32(smem + kOffV);
       auto issue_s = [&](int x, int j) {  // S of tile x (0 = A, 1 = B) against K tile j
-        const uint32_t kb = sk + (j & 1) * kTile, qb = sq + x * kTile;
+        const uint32_t kb = sk + (j % KST) * kTile, qb = sq + x * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&bars[BAR_S_FULL + x]);
       };
       auto issue_pv = [&](int x, int j) {  // O_x += P_x V_j, P_x from TMEM
-        const uint32_t vb = sv + (j & 1) * kTile;
+        const uint32_t vb = sv + (j % VST) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_bf16_ts(tmem + 256 + x * 128, tmem + x * 128 + kk * 8, umma_desc_sw128(vb + kk * 2048, kHalf, 1024),
@@ -230,22 +238,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < T; ++j) {
         const bool more = j + 1 < T;
         const uint32_t par = (uint32_t)(j & 1);
-        if (!wait(BAR_V_FULL + (j & 1), (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_V_FULL + j % VST, (uint32_t)((j / VST) & 1))) break;
         if (!wait(BAR_P_FULL, par)) break;
         tc_fence_after();
         issue_pv(0, j);
         if (more) {
-          if (!wait(BAR_K_FULL + ((j + 1) & 1), (uint32_t)(((j + 1) >> 1) & 1))) break;
+          if (!wait(BAR_K_FULL + (j + 1) % KST, (uint32_t)(((j + 1) / KST) & 1))) break;
           tc_fence_after();
           issue_s(0, j + 1);
         }
         if (!wait(BAR_P_FULL + 1, par)) break;
         tc_fence_after();
         issue_pv(1, j);
-        umma_commit(&bars[BAR_V_EMPTY + (j & 1)]);
+        umma_commit(&bars[BAR_V_EMPTY + j % VST]);
         if (more) {
           issue_s(1, j + 1);
-          umma_commit(&bars[BAR_K_EMPTY + ((j + 1) & 1)]);
+          umma_commit(&bars[BAR_K_EMPTY + (j + 1) % KST]);
         }
       }
       umma_commit(&bars[BAR_O_DONE]);
@@ -274,26 +282,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_col = x * 128, o_col = 256 + x * 128;
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < T; ++j) {
-      const int st = j & 1;
       if (!wait(BAR_S_FULL + x, (uint32_t)(j & 1))) break;
       tc_fence_after();
       float s[kBN];
+      {
+        uint32_t v[4][32];  // four loads in flight, one wait
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + s_col + c * 32, v);
+        for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + c * 32, v[c]);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
       }
       const int key0 = j * kBN;
       if (key0 + kBN - 1 > pos_lo) {  // some key past some row's position: mask
 #pragma unroll
         for (int i = 0; i < kBN; ++i) s[i] = (key0 + i <= pos) ? s[i] : -INFINITY;
       }
-      float mx = -INFINITY;  // max of the raw scores (scale > 0 keeps the order)
+      float mx;  // max of the raw scores (scale > 0 keeps the order), 8 independent chains
+      {
+        float pm[8];
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+        for (int u = 0; u < 8; ++u) pm[u] = s[u];
+#pragma unroll
+        for (int i = 8; i < kBN; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
+        mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      }
       const float m_new = fmaxf(m_run, mx * a.scale_log2);
       const bool rescale = m_new > m_run + 8.f;
       const float m_use = rescale ? m_new : m_run;
@@ -301,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // value rows of keys past the context must not carry NaNs into 0 * v
       // (tile A's PV runs first, so tile A's threads clear them)
       if (x == 0 && key0 + kBN > ctx) {
-        if (!wait(BAR_V_FULL + st, (uint32_t)((j >> 1) & 1))) break;
+        if (!wait(BAR_V_FULL + j % VST, (uint32_t)((j / VST) & 1))) break;
         if (key0 + m >= ctx) {
-          uint8_t *vd = smem + kOffV + st * kTile;
+          uint8_t *vd = smem + kOffV + (j % VST) * kTile;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             *reinterpret_cast<uint4 *>(vd + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
@@ -313,18 +328,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P (bf16 pairs) over the first 64 columns of this tile's S
-      float lsum = 0.f;
+      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int k = c * 64 + 2 * e;
-          w[e] = pack2(exp2f(fmaf(s[k], a.scale_log2, -m_use)), exp2f(fmaf(s[k + 1], a.scale_log2, -m_use)));
-          lsum += bf16_lo(w[e]) + bf16_hi(w[e]);
+          const float2 t = fma2(make_float2(s[k], s[k + 1]), sc2, nm2);
+          w[e] = pack2(exp2f(t.x), exp2f(t.y));
+          ls[e & 7] += bf16_lo(w[e]) + bf16_hi(w[e]);
         }
         tmem_st32(lane_base + s_col + c * 32, w);
       }
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       if (rescale && j >= 1) {  // the previous PV of this tile is done (S of tile j followed it)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
