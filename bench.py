@@ -67,6 +67,8 @@ def parse():
     ap.add_argument("--chunks", type=int, default=16, help="mixed_step: prefill chunks")
     ap.add_argument("--decodes", type=int, default=240, help="mixed_step: decode sequences")
     ap.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0 = auto, > 4x L2)")
+    ap.add_argument("--plain-decode", action="store_true",
+                    help="prefix_sharing: plain decode instead of the shared-prefix path")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
@@ -286,13 +288,25 @@ def build_prefix(args, torch, pa, dev):
     stream = torch.cuda.current_stream()
     outs = {"out": torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)}
 
+    npre = plan.prefix_len // B
+    groups = {"gs": np.array([0, S], np.int32), "gp": np.array([plan.prefix_len], np.int32),
+              "pt": np.ascontiguousarray(bt[:1, :npre])}
+    shared = not args.plain_decode
+    sp_ws = torch.empty(pa._binding.load().pa_shared_prefix_workspace_bytes(pa._binding._c.byref(desc)),
+                        dtype=torch.uint8, device=dev)
+
     def step(i, x, ev):
         l = i % NL
         pa.copy_blocks([kps[l]], [vps[l]], x["pairs"], stream=stream)
         pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
         ev and ev[0].record(stream)
-        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], outs["out"],
-                                  max_context_len=int(ctx.max()), workspace=ws, stream=stream)
+        if shared:
+            pa.paged_attention_decode_shared_prefix(
+                x["q"], kps[l], vps[l], x["bt"], x["ctx"], x["gs"], x["gp"], x["pt"], outs["out"], max_group_size=S,
+                max_prefix_len=plan.prefix_len, max_context_len=int(ctx.max()), workspace=sp_ws, stream=stream)
+        else:
+            pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], outs["out"],
+                                      max_context_len=int(ctx.max()), workspace=ws, stream=stream)
         ev and ev[1].record(stream)
         return [outs["out"]]
 
@@ -311,11 +325,16 @@ def build_prefix(args, torch, pa, dev):
     dec_unique = kv_unique + 2 * S * Hq * D * 2 + int(((ctx.astype(np.int64) + B - 1) // B).sum()) * 4 + S * 4
     dec_logical = decode_bytes(ctx, Hq, Hkv, D, B)
     copy = len(pairs) * Hkv * B * D * 2 * 2 * 2
+    mode = "shared-prefix decode (prefix attended once on the tensor cores + per-sequence suffix)" if shared \
+        else "plain decode"
+    inputs = {"q": q, "new_k": nk, "new_v": nv, "slots": slots, "pairs": pairs, "bt": bt, "ctx": ctx}
+    if shared:
+        inputs.update(groups)
     return Bench("prefix_sharing", f"prefix_sharing: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
                  f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512], {Hq}q/{Hkv}kv, D={D}, B={B}; "
-                 f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + decode",
-                 {"q": q, "new_k": nk, "new_v": nv, "slots": slots, "pairs": pairs, "bt": bt, "ctx": ctx},
-                 step, dec_unique + copy + cache_bytes(S, Hkv, D), 3, "decode_kernel", "hbm", dec_unique, S,
+                 f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + {mode}",
+                 inputs, step, dec_unique + copy + cache_bytes(S, Hkv, D), 4 if shared else 3,
+                 "shared_prefix_decode" if shared else "decode_kernel", "hbm", dec_unique, S,
                  extra={"unique_pages": int(len(unique_pages)), "logical_decode_bytes": dec_logical,
                         "unique_decode_bytes": dec_unique, "cow_pairs": int(len(pairs))},
                  layers=NL, pool_mb=kp.nbytes * 2 / 1e6)

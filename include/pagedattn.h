@@ -127,6 +127,40 @@ int pa_paged_attention_decode(const pa_decode_desc *desc, const void *q, const v
                               const int32_t *context_lens, void *out, void *workspace,
                               size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/* Bytes of device workspace pa_paged_attention_decode_shared_prefix needs for
+ * `desc` on the current device (decode split-K scratch plus one fp32 partial
+ * softmax state per (sequence, query head)); 0 for an invalid desc. */
+size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc);
+
+/* Shared-prefix-aware decode [ATT][PHASE][SHARE]: the same result as
+ * pa_paged_attention_decode (within rounding), for batches in which groups of
+ * sequences point at the same physical pages for a common prefix (shared
+ * system prompts, parallel samples, beam candidates).  Group k is the
+ * sequences group_starts[k] .. group_starts[k+1]-1 (consecutive, groups
+ * disjoint and ordered; sequences outside every group are decoded normally);
+ * they share their first group_prefix_lens[k] tokens, a positive multiple of
+ * block_size, held in blocks prefix_tables[k][0 ..] -- the same blocks that
+ * lead every member's own block-table row.  The prefix is attended once for
+ * all of the group's query rows on the tensor cores (fp32 partial softmax
+ * state), then each sequence attends its own keys prefix .. ctx-1 and merges.
+ *   group_starts       device int32 [num_groups + 1]
+ *   group_prefix_lens  device int32 [num_groups], <= each member's context
+ *   prefix_tables      device int32 [num_groups][prefix_max_blocks]
+ *   max_group_size     bound on every group's size (sizes the grid)
+ *   max_prefix_len     bound on every group_prefix_lens[k], <= max_context_len
+ *   workspace          >= pa_shared_prefix_workspace_bytes(desc), any contents
+ * head_dim must be 128 and the GQA group 1, 2, 4, 8 or 16 when num_groups > 0;
+ * num_groups == 0 is plain decode.  Other arguments and errors as in
+ * pa_paged_attention_decode; a prefix length that is not a multiple of B or
+ * exceeds a member's context sets PA_DEVERR_CTX for that member. */
+int pa_paged_attention_decode_shared_prefix(const pa_decode_desc *desc, const void *q, const void *k_pool,
+                                            const void *v_pool, const int32_t *block_tables,
+                                            const int32_t *context_lens, int num_groups,
+                                            const int32_t *group_starts, const int32_t *group_prefix_lens,
+                                            const int32_t *prefix_tables, int prefix_max_blocks,
+                                            int max_group_size, int max_prefix_len, void *out, void *workspace,
+                                            size_t workspace_bytes, int32_t *err_flag, void *stream);
+
 /* Size of the fixed device scratch array of pa_paged_attention_decode_noalloc
  * (8 MiB, held on every GPU that loads the library until the process exits). */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

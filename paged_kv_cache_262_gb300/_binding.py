@@ -23,7 +23,8 @@ DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 
 # Every symbol include/pagedattn.h declares.
 EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
-    "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk",
+    "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
 )
@@ -68,6 +69,11 @@ def load(path: Optional[str] = None):
                                                   _P, _P]
         lib.pa_paged_attention_decode_noalloc.restype = i
         lib.pa_paged_attention_decode_noalloc.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P]
+        lib.pa_shared_prefix_workspace_bytes.restype = sz
+        lib.pa_shared_prefix_workspace_bytes.argtypes = [_c.POINTER(DecodeDesc)]
+        lib.pa_paged_attention_decode_shared_prefix.restype = i
+        lib.pa_paged_attention_decode_shared_prefix.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, i, _P, _P,
+                                                                _P, i, i, i, _P, _P, sz, _P, _P]
         lib.pa_paged_attention_prefill_chunk.restype = i
         lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, i, _P, _P, _P,
                                                          _P, _P, _P, _P]
@@ -198,6 +204,41 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=No
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
+
+_WS_SP = {}
+
+
+def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, context_lens, group_starts,
+                                         group_prefix_lens, prefix_tables, out=None, *, max_group_size,
+                                         max_prefix_len, scale=None, max_context_len=None, workspace=None,
+                                         err_flag=None, stream=None):
+    """Decode with each group's shared prefix attended once (see pagedattn.h)."""
+    import torch
+    for t, n, dt, nd in ((q, "q", torch.bfloat16, 3), (k_pool, "k_pool", torch.bfloat16, 4),
+                         (v_pool, "v_pool", torch.bfloat16, 4), (block_tables, "block_tables", torch.int32, 2),
+                         (context_lens, "context_lens", torch.int32, 1), (group_starts, "group_starts", torch.int32, 1),
+                         (group_prefix_lens, "group_prefix_lens", torch.int32, 1),
+                         (prefix_tables, "prefix_tables", torch.int32, 2)):
+        _need(t, dt, n, nd)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
+    if workspace is None:
+        need = int(load().pa_shared_prefix_workspace_bytes(_c.byref(desc)))
+        key = q.device.index
+        workspace = _WS_SP.get(key)
+        if workspace is None or workspace.numel() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            _WS_SP[key] = workspace
+    ng = int(group_prefix_lens.shape[0])
+    st = load().pa_paged_attention_decode_shared_prefix(
+        _c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), ng,
+        _ptr(group_starts), _ptr(group_prefix_lens), _ptr(prefix_tables), int(prefix_tables.shape[1]),
+        int(max_group_size), int(max_prefix_len), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_paged_attention_decode_shared_prefix")
+    return out
 
 
 def paged_attention_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens, out=None, *, scale=None,

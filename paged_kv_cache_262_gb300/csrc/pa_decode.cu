@@ -56,6 +56,15 @@ struct DecodeArgs {
   float scale_log2;
   unsigned int epoch;  // unique per call, never 0
   int lpt;             // order CTAs longest context first
+  // Shared-prefix groups (optional): sequences grp_start[k] .. grp_start[k+1]-1
+  // share their first grp_prefix[k] tokens (whole blocks), whose attention was
+  // computed by a separate pass into the partial states pre_o / pre_ml; this
+  // kernel then covers keys grp_prefix[k] .. ctx-1 and folds that partial in.
+  const int32_t *grp_start;
+  const int32_t *grp_prefix;
+  int ngroups;
+  const float *pre_o;   // [S][Hq][D] o/l of the prefix
+  const float *pre_ml;  // [S][Hq][2] (m, l) of the prefix
 };
 
 // Counts one arrival of this call at *c and returns the arrivals so far.  A
@@ -188,9 +197,22 @@ __global__ void __launch_bounds__(NW * 32)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
   const int ctx = __ldg(a.ctx + s);
-  const bool bad = ctx <= 0 || ctx > a.max_blocks * B || ctx > a.max_ctx;
-  const int npages = bad ? 0 : (ctx + B - 1) / B;
-  const int nparts = bad ? 1 : (npages + a.part_pages - 1) / a.part_pages;
+  int kstart = 0;  // first key this kernel covers (end of a shared prefix)
+  if (a.ngroups > 0 && s >= __ldg(a.grp_start) && s < __ldg(a.grp_start + a.ngroups)) {
+    int lo = 0, hi = a.ngroups;  // grp_start[lo] <= s < grp_start[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(a.grp_start + mid) <= s) lo = mid;
+      else hi = mid;
+    }
+    kstart = __ldg(a.grp_prefix + lo);
+  }
+  const bool has_pre = kstart > 0;
+  const bool bad = ctx <= 0 || ctx > a.max_blocks * B || ctx > a.max_ctx || kstart < 0 || kstart > ctx ||
+                   kstart % B != 0;
+  const int kp0 = bad ? 0 : kstart / B;  // first page of this kernel's key range
+  const int npages = bad ? 0 : (ctx + B - 1) / B - kp0;
+  const int nparts = bad ? 1 : max(1, (npages + a.part_pages - 1) / a.part_pages);
   if (part >= nparts) return;
   __nv_bfloat16 *out_base = a.out + ((size_t)s * a.Hq + (size_t)kvh * G) * D;
   if (bad) {
@@ -201,8 +223,8 @@ __global__ void __launch_bounds__(NW * 32)
 
   // ---- stage this part's block-table entries; init this warp's barriers
   const int p0 = part * a.part_pages;
-  const int np = min(npages - p0, a.part_pages);
-  const int32_t *bt_row = a.bt + (size_t)s * a.max_blocks + p0;
+  const int np = max(0, min(npages - p0, a.part_pages));
+  const int32_t *bt_row = a.bt + (size_t)s * a.max_blocks + kp0 + p0;
   for (int i = tid; i < np; i += NW * 32) {
     int pg = __ldg(bt_row + i);
     if (pg < 0 || pg >= a.num_blocks) {
@@ -283,7 +305,7 @@ __global__ void __launch_bounds__(NW * 32)
     if (tbl[lp] >= 0) {
       const uint32_t kb = smem_u32(ring + stg * L::kSlotBytes);
       const uint32_t vb = kb + L::kPageBytes;
-      const int tok0 = (p0 + lp) * B;
+      const int tok0 = (kp0 + p0 + lp) * B;
 
       // S^T[token][head] = K Q^T
       float sc[MT][NT][4];
@@ -428,7 +450,15 @@ __global__ void __launch_bounds__(NW * 32)
     }
     const float val = l > 0.f ? acc / l : 0.f;
     if (!split) {
-      out_base[idx] = __float2bfloat16(val);
+      float res = val;
+      if (has_pre) {  // fold in the shared prefix's partial state
+        const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
+        const float mp = __ldg(a.pre_ml + 2 * row), lp = __ldg(a.pre_ml + 2 * row + 1);
+        const float M = fmaxf(l > 0.f ? mx : -INFINITY, lp > 0.f ? mp : -INFINITY);
+        const float w1 = l > 0.f ? l * exp2f(mx - M) : 0.f, w2 = lp > 0.f ? lp * exp2f(mp - M) : 0.f;
+        res = (w1 + w2) > 0.f ? (w1 * val + w2 * __ldg(a.pre_o + row * D + d)) / (w1 + w2) : 0.f;
+      }
+      out_base[idx] = __float2bfloat16(res);
     } else {
       const size_t u = (unit * a.max_parts + part) * G + g;
       a.ws_o[u * D + d] = val;
@@ -448,9 +478,13 @@ __global__ void __launch_bounds__(NW * 32)
   if (!misc[0]) return;
   __threadfence();
   const size_t ubase = unit * a.max_parts;
+  float *wpre = reinterpret_cast<float *>(misc + 8);  // prefix weight per head (histogram area, free now)
   if (tid < G) {
     const int g = tid;
-    float M = -INFINITY;
+    const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
+    const float mp = has_pre ? __ldg(a.pre_ml + 2 * row) : -INFINITY;
+    const float lp = has_pre ? __ldg(a.pre_ml + 2 * row + 1) : 0.f;
+    float M = lp > 0.f ? mp : -INFINITY;
     for (int p = 0; p < nparts; ++p) {
       const float l = __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g) + 1);
       if (l > 0.f) M = fmaxf(M, __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g)));
@@ -463,14 +497,18 @@ __global__ void __launch_bounds__(NW * 32)
       wts[p * 16 + g] = w;
       den += w;
     }
+    const float w_pre = lp > 0.f ? lp * exp2f(mp - M) : 0.f;
+    den += w_pre;
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int p = 0; p < nparts; ++p) wts[p * 16 + g] *= inv;
+    wpre[g] = w_pre * inv;
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += NW * 32) {
     const int g = idx / D, d = idx - g * D;
     float acc = 0.f;
     for (int p = 0; p < nparts; ++p) acc += wts[p * 16 + g] * __ldcg(a.ws_o + ((ubase + p) * G + g) * D + d);
+    if (has_pre) acc += wpre[g] * __ldg(a.pre_o + ((size_t)s * a.Hq + (size_t)kvh * G + g) * D + d);
     out_base[idx] = __float2bfloat16(acc);
   }
   if (tid == 0) a.ws_cnt[unit] = 0ull;
@@ -509,11 +547,11 @@ int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const Decod
 }  // namespace
 }  // namespace pa
 
-extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q, const void *k_pool,
-                                         const void *v_pool, const int32_t *block_tables,
-                                         const int32_t *context_lens, void *out, void *workspace,
-                                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
-  using namespace pa;
+namespace pa {
+
+int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_tables, const int32_t *context_lens, void *out, void *workspace,
+                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre) {
   int st = validate_decode_desc(d);
   if (st != PA_OK) return st;
   if (d->num_seqs == 0) return PA_OK;
@@ -558,6 +596,11 @@ extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q,
   a.part_pages = plan.part_pages;
   a.max_parts = plan.max_parts;
   a.scale_log2 = d->scale * 1.4426950408889634f;
+  a.grp_start = pre ? pre->grp_start : nullptr;
+  a.grp_prefix = pre ? pre->grp_prefix : nullptr;
+  a.ngroups = pre ? pre->ngroups : 0;
+  a.pre_o = pre ? pre->pre_o : nullptr;
+  a.pre_ml = pre ? pre->pre_ml : nullptr;
   const dim3 grid(plan.max_parts, d->num_kv_heads, d->num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d->head_dim == 128)
@@ -565,4 +608,14 @@ extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q,
                                : dispatch_nt<128, 32>(a.G, tk, tv, a, grid, s);
   return d->block_size == 16 ? dispatch_nt<64, 16>(a.G, tk, tv, a, grid, s)
                              : dispatch_nt<64, 32>(a.G, tk, tv, a, grid, s);
+}
+
+}  // namespace pa
+
+extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q, const void *k_pool,
+                                         const void *v_pool, const int32_t *block_tables,
+                                         const int32_t *context_lens, void *out, void *workspace,
+                                         size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  return pa::decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes,
+                           err_flag, stream, nullptr);
 }

@@ -48,4 +48,25 @@ int validate_decode_desc(const pa_decode_desc *d);
 // The plan used by both pa_decode_workspace_bytes and the launcher.
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count);
 
+// Shared-prefix information for the decode kernel (see pa_shared_prefix.cu).
+struct DecodePrefix {
+  const int32_t *grp_start;   // device [ngroups + 1]
+  const int32_t *grp_prefix;  // device [ngroups], tokens, multiples of B
+  int ngroups;
+  const float *pre_o;         // device [S][Hq][D]
+  const float *pre_ml;        // device [S][Hq][2]
+};
+
+// The decode launcher behind pa_paged_attention_decode (pre may be null).
+int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_tables, const int32_t *context_lens, void *out, void *workspace,
+                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre);
+
+// Launches the chunked-prefill kernel (pa_prefill.cu).  causal = 0 lets every
+// row see all ctx keys; with part_o/part_ml set, rows are written as fp32
+// partial softmax states (o/l, m, l) instead of bf16 outputs.
+int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, int max_q_len, int total_q,
+                   const void *k_pool, const void *v_pool, const int32_t *block_tables, const int32_t *context_lens,
+                   void *out, float *part_o, float *part_ml, int causal, int32_t *err_flag, void *stream);
+
 }  // namespace pa

@@ -58,6 +58,9 @@ struct PrefillArgs {
   int32_t *err;
   int R, Hq, Hkv, num_blocks, max_blocks, max_ctx, total_q;
   float scale_log2;
+  int causal;       // 0: every row sees all ctx keys (shared-prefix pass)
+  float *part_o;    // non-null: write fp32 o/l [total_q][Hq][128] ...
+  float *part_ml;   // ... and (m, l) [total_q][Hq][2] instead of bf16 out
 };
 
 constexpr int kD = 128;         // head_dim
@@ -113,22 +116,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ctx = __ldg(a.ctx + r);
   const int q0 = qt * 2 * TP;  // first position index of tile A
   if (C <= 0 || q0 >= C) return;
-  const bool bad = ctx <= 0 || C > ctx || ctx > a.max_blocks * B || ctx > a.max_ctx || c0 < 0 ||
+  const bool bad = ctx <= 0 || (a.causal && C > ctx) || ctx > a.max_blocks * B || ctx > a.max_ctx || c0 < 0 ||
                    c1 > a.total_q;
-  if (bad) {  // zero this CTA's rows, report
+  if (bad) {  // zero this CTA's rows (an empty partial state), report
     if (c0 >= 0 && c1 <= a.total_q) {
       for (int m = threadIdx.x; m < 2 * kBM; m += kThreads) {
         const int t = q0 + m / G;
         if (t >= C) continue;
-        uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + t) * a.Hq + g * G + m % G) * kD);
-        for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        const size_t row = (size_t)(c0 + t) * a.Hq + g * G + m % G;
+        if (a.part_o) {
+          for (int i = 0; i < kD; ++i) a.part_o[row * kD + i] = 0.f;
+          a.part_ml[2 * row] = -INFINITY;
+          a.part_ml[2 * row + 1] = 0.f;
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kD);
+          for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        }
       }
     }
     if (threadIdx.x == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
     return;
   }
   const int npages = (ctx + B - 1) / B;
-  const int pos_hi = ctx - C + min(C, q0 + 2 * TP) - 1;  // last valid position of the CTA
+  // last valid position of the CTA (non-causal rows all sit at ctx - 1)
+  const int pos_hi = a.causal ? ctx - C + min(C, q0 + 2 * TP) - 1 : ctx - 1;
   const int T = pos_hi / kBN + 1;                         // key tiles
 
   if (threadIdx.x == 0) {
@@ -264,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = (warp & 3) * 32 + lane;
     const int tloc = q0 + x * TP + m / G;  // position index within the chunk
     const bool row_valid = tloc < C;
-    const int pos = row_valid ? ctx - C + tloc : ctx - 1;
-    const int pos_lo = ctx - C + q0 + x * TP;  // first position of this tile
+    const int pos = (row_valid && a.causal) ? ctx - C + tloc : ctx - 1;
+    const int pos_lo = a.causal ? ctx - C + q0 + x * TP : ctx - 1;  // first position of this tile
     const int head = g * G + m % G;
     {  // Q row -> shared memory (128-byte swizzle, two 64-column halves)
       uint8_t *qd = smem + kOffQ + x * kTile;
@@ -363,13 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wait(BAR_O_DONE, 0)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
+      const size_t row = (size_t)(c0 + tloc) * a.Hq + head;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32(lane_base + o_col + c * 32, v);
         tmem_wait_ld();
-        if (row_valid) {
+        if (!row_valid) continue;
+        if (a.part_o) {
+          float4 *dst = reinterpret_cast<float4 *>(a.part_o + row * kD);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[c * 8 + i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                                         __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+        } else {
+          uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kD);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 o;
@@ -380,6 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[c * 4 + i] = o;
           }
         }
+      }
+      if (row_valid && a.part_o) {
+        a.part_ml[2 * row] = m_run;
+        a.part_ml[2 * row + 1] = l_run;
       }
     }
   }
@@ -415,14 +438,10 @@ int dispatch_g(int G, const CUtensorMap &tk, const CUtensorMap &tv, const Prefil
 }
 
 }  // namespace
-}  // namespace pa
 
-extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const void *q, const int32_t *cu_q,
-                                                int max_q_len, int total_q, const void *k_pool,
-                                                const void *v_pool, const int32_t *block_tables,
-                                                const int32_t *context_lens, void *out, int32_t *err_flag,
-                                                void *stream) {
-  using namespace pa;
+int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, int max_q_len, int total_q,
+                   const void *k_pool, const void *v_pool, const int32_t *block_tables, const int32_t *context_lens,
+                   void *out, float *part_o, float *part_ml, int causal, int32_t *err_flag, void *stream) {
   int st = validate_decode_desc(d);
   if (st != PA_OK) return st;
   if (d->head_dim != 128) return PA_ERR_UNSUPPORTED;
@@ -430,8 +449,11 @@ extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const v
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return PA_ERR_UNSUPPORTED;
   if (max_q_len < 0 || total_q < 0) return PA_ERR_INVALID;
   if (d->num_seqs == 0 || max_q_len == 0 || total_q == 0) return PA_OK;
-  if (!q || !cu_q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
-  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PA_ERR_INVALID;
+  if (!q || !cu_q || !k_pool || !v_pool || !block_tables || !context_lens || (!out && !part_o))
+    return PA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out && !aligned16(out)) ||
+      (part_o && (!aligned16(part_o) || !part_ml)))
+    return PA_ERR_INVALID;
   if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   const long long tiles = ((long long)max_q_len * G + 2 * kBM - 1) / (2 * kBM);
   if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
@@ -455,7 +477,21 @@ extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const v
   a.max_ctx = d->max_context_len;
   a.total_q = total_q;
   a.scale_log2 = d->scale * 1.4426950408889634f;
+  a.causal = causal;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
   const dim3 grid((unsigned)tiles, d->num_kv_heads, d->num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d->block_size == 16 ? dispatch_g<16>(G, tk, tv, a, grid, s) : dispatch_g<32>(G, tk, tv, a, grid, s);
+}
+
+}  // namespace pa
+
+extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const void *q, const int32_t *cu_q,
+                                                int max_q_len, int total_q, const void *k_pool,
+                                                const void *v_pool, const int32_t *block_tables,
+                                                const int32_t *context_lens, void *out, int32_t *err_flag,
+                                                void *stream) {
+  return pa::prefill_launch(d, q, cu_q, max_q_len, total_q, k_pool, v_pool, block_tables, context_lens, out,
+                            nullptr, nullptr, 1, err_flag, stream);
 }

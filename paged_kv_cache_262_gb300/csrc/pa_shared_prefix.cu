@@ -1,0 +1,76 @@
+// Shared-prefix-aware decode.
+//
+// "Configuring vLLM and PagedAttention for High Throughput Enterprise LLM
+// Serving" ("Zero-Copy Prefix Caching & Shared Sampling") has requests that
+// share a prompt prefix point at the same physical pages, and decode is bound
+// by reading the cache from HBM ("Memory Bottlenecks in Autoregressive LLM
+// Inference").  Plain decode reads a shared prefix once per sharer.  Here a
+// group of sequences that share their first P tokens has that prefix attended
+// once, for all of the group's query rows together (sequences x query heads),
+// as a dense contraction on the tensor cores; each sequence's decode then
+// covers only its own keys P .. ctx-1 and merges the prefix's partial softmax
+// state (m, l, o/l) exactly as split-K parts are merged.
+#include <cuda_runtime.h>
+
+#include "pa_internal.h"
+#include "pagedattn.h"
+
+namespace {
+
+size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t decode, pre_o, pre_ml;
+  size_t total() const { return decode + pre_o + pre_ml; }
+};
+
+Layout layout(const pa_decode_desc *d) {
+  Layout l;
+  l.decode = up256(pa::make_decode_plan(d, pa::current_sm_count()).total());
+  l.pre_o = up256((size_t)d->num_seqs * d->num_q_heads * d->head_dim * sizeof(float));
+  l.pre_ml = up256((size_t)d->num_seqs * d->num_q_heads * 2 * sizeof(float));
+  return l;
+}
+
+}  // namespace
+
+extern "C" size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc) {
+  if (pa::validate_decode_desc(desc) != PA_OK) return 0;
+  return layout(desc).total();
+}
+
+extern "C" int pa_paged_attention_decode_shared_prefix(
+    const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_tables,
+    const int32_t *context_lens, int num_groups, const int32_t *group_starts, const int32_t *group_prefix_lens,
+    const int32_t *prefix_tables, int prefix_max_blocks, int max_group_size, int max_prefix_len, void *out,
+    void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  using namespace pa;
+  int st = validate_decode_desc(d);
+  if (st != PA_OK) return st;
+  if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0 || prefix_max_blocks < 0) return PA_ERR_INVALID;
+  if (d->num_seqs == 0) return PA_OK;
+  if (num_groups == 0)
+    return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes, err_flag,
+                         stream, nullptr);
+  if (!group_starts || !group_prefix_lens || !prefix_tables || prefix_max_blocks == 0 || max_group_size == 0 ||
+      max_prefix_len == 0)
+    return PA_ERR_INVALID;
+  if (max_prefix_len > d->max_context_len || (int64_t)prefix_max_blocks * d->block_size < max_prefix_len)
+    return PA_ERR_INVALID;
+  const Layout l = layout(d);
+  if (!workspace || workspace_bytes < l.total() || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *pre_o = reinterpret_cast<float *>(ws + l.decode);
+  float *pre_ml = reinterpret_cast<float *>(ws + l.decode + l.pre_o);
+  // 1. each group's shared prefix, all of its rows at once, on the tensor cores
+  pa_decode_desc pd = *d;
+  pd.num_seqs = num_groups;
+  pd.max_blocks_per_seq = prefix_max_blocks;
+  pd.max_context_len = max_prefix_len;
+  st = prefill_launch(&pd, q, group_starts, max_group_size, d->num_seqs, k_pool, v_pool, prefix_tables,
+                      group_prefix_lens, nullptr, pre_o, pre_ml, /*causal=*/0, err_flag, stream);
+  if (st != PA_OK) return st;
+  // 2. every sequence's own keys, merged with its group's prefix state
+  const DecodePrefix pre{group_starts, group_prefix_lens, num_groups, pre_o, pre_ml};
+  return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, ws, l.decode, err_flag, stream, &pre);
+}
