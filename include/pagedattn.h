@@ -128,8 +128,9 @@ int pa_paged_attention_decode(const pa_decode_desc *desc, const void *q, const v
                               size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /* Bytes of device workspace pa_paged_attention_decode_shared_prefix needs for
- * `desc` on the current device (decode split-K scratch plus one fp32 partial
- * softmax state per (sequence, query head)); 0 for an invalid desc. */
+ * `desc` on the current device (decode split-K scratch plus up to eight fp32
+ * partial softmax states per (sequence, query head), one per key range of the
+ * prefix); 0 for an invalid desc. */
 size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc);
 
 /* Shared-prefix-aware decode [ATT][PHASE][SHARE]: the same result as
@@ -142,7 +143,9 @@ size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc);
  * block_size, held in blocks prefix_tables[k][0 ..] -- the same blocks that
  * lead every member's own block-table row.  The prefix is attended once for
  * all of the group's query rows on the tensor cores (fp32 partial softmax
- * state), then each sequence attends its own keys prefix .. ctx-1 and merges.
+ * states, the prefix cut into up to 8 key ranges when the groups alone would
+ * not fill the GPU), then each sequence attends its own keys prefix .. ctx-1
+ * and merges.
  *   group_starts       device int32 [num_groups + 1]
  *   group_prefix_lens  device int32 [num_groups], <= each member's context
  *   prefix_tables      device int32 [num_groups][prefix_max_blocks]

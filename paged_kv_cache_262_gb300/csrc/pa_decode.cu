@@ -63,8 +63,9 @@ struct DecodeArgs {
   const int32_t *grp_start;
   const int32_t *grp_prefix;
   int ngroups;
-  const float *pre_o;   // [S][Hq][D] o/l of the prefix
-  const float *pre_ml;  // [S][Hq][2] (m, l) of the prefix
+  const float *pre_o;   // [npre][S][Hq][D] o/l of the prefix's key ranges
+  const float *pre_ml;  // [npre][S][Hq][2] (m, l) of the prefix's key ranges
+  int npre;
 };
 
 // Counts one arrival of this call at *c and returns the arrivals so far.  A
@@ -451,12 +452,24 @@ __global__ void __launch_bounds__(NW * 32)
     const float val = l > 0.f ? acc / l : 0.f;
     if (!split) {
       float res = val;
-      if (has_pre) {  // fold in the shared prefix's partial state
+      if (has_pre) {  // fold in the shared prefix's partial states
         const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
-        const float mp = __ldg(a.pre_ml + 2 * row), lp = __ldg(a.pre_ml + 2 * row + 1);
-        const float M = fmaxf(l > 0.f ? mx : -INFINITY, lp > 0.f ? mp : -INFINITY);
-        const float w1 = l > 0.f ? l * exp2f(mx - M) : 0.f, w2 = lp > 0.f ? lp * exp2f(mp - M) : 0.f;
-        res = (w1 + w2) > 0.f ? (w1 * val + w2 * __ldg(a.pre_o + row * D + d)) / (w1 + w2) : 0.f;
+        const size_t slab = (size_t)a.S * a.Hq;
+        float M = l > 0.f ? mx : -INFINITY;
+        for (int p = 0; p < a.npre; ++p) {
+          const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
+          if (lp > 0.f) M = fmaxf(M, __ldg(a.pre_ml + 2 * (p * slab + row)));
+        }
+        float w = l > 0.f ? l * exp2f(mx - M) : 0.f;
+        float num = w * val, den = w;
+        for (int p = 0; p < a.npre; ++p) {
+          const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
+          if (!(lp > 0.f)) continue;
+          const float wp = lp * exp2f(__ldg(a.pre_ml + 2 * (p * slab + row)) - M);
+          num += wp * __ldg(a.pre_o + (p * slab + row) * D + d);
+          den += wp;
+        }
+        res = den > 0.f ? num / den : 0.f;
       }
       out_base[idx] = __float2bfloat16(res);
     } else {
@@ -478,13 +491,17 @@ __global__ void __launch_bounds__(NW * 32)
   if (!misc[0]) return;
   __threadfence();
   const size_t ubase = unit * a.max_parts;
-  float *wpre = reinterpret_cast<float *>(misc + 8);  // prefix weight per head (histogram area, free now)
+  float *wpre = reinterpret_cast<float *>(misc + 8);  // [npre][16] prefix weights (histogram area, free now)
+  const size_t slab = (size_t)a.S * a.Hq;
   if (tid < G) {
     const int g = tid;
     const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
-    const float mp = has_pre ? __ldg(a.pre_ml + 2 * row) : -INFINITY;
-    const float lp = has_pre ? __ldg(a.pre_ml + 2 * row + 1) : 0.f;
-    float M = lp > 0.f ? mp : -INFINITY;
+    const int npre = has_pre ? a.npre : 0;
+    float M = -INFINITY;
+    for (int p = 0; p < npre; ++p) {
+      const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
+      if (lp > 0.f) M = fmaxf(M, __ldg(a.pre_ml + 2 * (p * slab + row)));
+    }
     for (int p = 0; p < nparts; ++p) {
       const float l = __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g) + 1);
       if (l > 0.f) M = fmaxf(M, __ldcg(a.ws_ml + 2 * ((ubase + p) * G + g)));
@@ -497,18 +514,24 @@ __global__ void __launch_bounds__(NW * 32)
       wts[p * 16 + g] = w;
       den += w;
     }
-    const float w_pre = lp > 0.f ? lp * exp2f(mp - M) : 0.f;
-    den += w_pre;
+    for (int p = 0; p < npre; ++p) {
+      const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
+      const float w = lp > 0.f ? lp * exp2f(__ldg(a.pre_ml + 2 * (p * slab + row)) - M) : 0.f;
+      wpre[p * 16 + g] = w;
+      den += w;
+    }
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int p = 0; p < nparts; ++p) wts[p * 16 + g] *= inv;
-    wpre[g] = w_pre * inv;
+    for (int p = 0; p < npre; ++p) wpre[p * 16 + g] *= inv;
   }
   __syncthreads();
   for (int idx = tid; idx < G * D; idx += NW * 32) {
     const int g = idx / D, d = idx - g * D;
     float acc = 0.f;
     for (int p = 0; p < nparts; ++p) acc += wts[p * 16 + g] * __ldcg(a.ws_o + ((ubase + p) * G + g) * D + d);
-    if (has_pre) acc += wpre[g] * __ldg(a.pre_o + ((size_t)s * a.Hq + (size_t)kvh * G + g) * D + d);
+    if (has_pre)
+      for (int p = 0; p < a.npre; ++p)
+        acc += wpre[p * 16 + g] * __ldg(a.pre_o + (p * slab + (size_t)s * a.Hq + (size_t)kvh * G + g) * D + d);
     out_base[idx] = __float2bfloat16(acc);
   }
   if (tid == 0) a.ws_cnt[unit] = 0ull;
@@ -601,6 +624,7 @@ int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, co
   a.ngroups = pre ? pre->ngroups : 0;
   a.pre_o = pre ? pre->pre_o : nullptr;
   a.pre_ml = pre ? pre->pre_ml : nullptr;
+  a.npre = pre ? pre->npre : 0;
   const dim3 grid(plan.max_parts, d->num_kv_heads, d->num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d->head_dim == 128)

@@ -53,8 +53,9 @@ struct DecodePrefix {
   const int32_t *grp_start;   // device [ngroups + 1]
   const int32_t *grp_prefix;  // device [ngroups], tokens, multiples of B
   int ngroups;
-  const float *pre_o;         // device [S][Hq][D]
-  const float *pre_ml;        // device [S][Hq][2]
+  const float *pre_o;         // device [npre][S][Hq][D]
+  const float *pre_ml;        // device [npre][S][Hq][2]
+  int npre;                   // partial states per row (key ranges of the prefix)
 };
 
 // The decode launcher behind pa_paged_attention_decode (pre may be null).
@@ -64,9 +65,14 @@ int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, co
 
 // Launches the chunked-prefill kernel (pa_prefill.cu).  causal = 0 lets every
 // row see all ctx keys; with part_o/part_ml set, rows are written as fp32
-// partial softmax states (o/l, m, l) instead of bf16 outputs.
+// partial softmax states (o/l, m, l) instead of bf16 outputs, one state per
+// key range when kparts > 1 (ranges of kpart_len keys, a multiple of 128).
 int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, int max_q_len, int total_q,
                    const void *k_pool, const void *v_pool, const int32_t *block_tables, const int32_t *context_lens,
-                   void *out, float *part_o, float *part_ml, int causal, int32_t *err_flag, void *stream);
+                   void *out, float *part_o, float *part_ml, int causal, int kparts, int kpart_len,
+                   int32_t *err_flag, void *stream);
+
+// Most key ranges the shared-prefix pass splits a prefix into.
+constexpr int kMaxPrefixParts = 8;
 
 }  // namespace pa

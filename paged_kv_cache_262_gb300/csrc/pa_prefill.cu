@@ -59,8 +59,10 @@ struct PrefillArgs {
   int R, Hq, Hkv, num_blocks, max_blocks, max_ctx, total_q;
   float scale_log2;
   int causal;       // 0: every row sees all ctx keys (shared-prefix pass)
-  float *part_o;    // non-null: write fp32 o/l [total_q][Hq][128] ...
-  float *part_ml;   // ... and (m, l) [total_q][Hq][2] instead of bf16 out
+  float *part_o;    // non-null: write fp32 o/l [kparts][total_q][Hq][128] ...
+  float *part_ml;   // ... and (m, l) [kparts][total_q][Hq][2] instead of bf16 out
+  int kparts;       // non-causal: keys split into kparts ranges of kpart_len
+  int kpart_len;    // (a multiple of 128), one partial state per range
 };
 
 constexpr int kD = 128;         // head_dim
@@ -110,34 +112,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = gridDim.x - 1 - blockIdx.x;  // later tiles see more keys: start them first
-  const int g = blockIdx.y, r = blockIdx.z;
+  const int g = blockIdx.y, r = blockIdx.z / a.kparts, kpart = blockIdx.z % a.kparts;
   const int c0 = __ldg(a.cu_q + r), c1 = __ldg(a.cu_q + r + 1);
   const int C = c1 - c0;
-  const int ctx = __ldg(a.ctx + r);
+  const int ctx_full = __ldg(a.ctx + r);
+  // key range of this CTA: all keys, or one of the non-causal key ranges
+  const int key_lo = a.kparts > 1 ? kpart * a.kpart_len : 0;
+  const int ctx = a.kparts > 1 ? max(0, min(ctx_full - key_lo, a.kpart_len)) : ctx_full;
+  float *part_o = a.part_o ? a.part_o + (size_t)kpart * a.total_q * a.Hq * kD : nullptr;
+  float *part_ml = a.part_ml ? a.part_ml + (size_t)kpart * a.total_q * a.Hq * 2 : nullptr;
   const int q0 = qt * 2 * TP;  // first position index of tile A
   if (C <= 0 || q0 >= C) return;
-  const bool bad = ctx <= 0 || (a.causal && C > ctx) || ctx > a.max_blocks * B || ctx > a.max_ctx || c0 < 0 ||
-                   c1 > a.total_q;
-  if (bad) {  // zero this CTA's rows (an empty partial state), report
+  const bool empty = a.kparts > 1 && ctx_full > 0 && ctx == 0;  // range past a shorter prefix
+  const bool bad = ctx_full <= 0 || (a.causal && C > ctx) || ctx_full > a.max_blocks * B || ctx_full > a.max_ctx ||
+                   c0 < 0 || c1 > a.total_q;
+  if (bad || empty) {  // zero this CTA's rows (an empty partial state); report bad ones
     if (c0 >= 0 && c1 <= a.total_q) {
       for (int m = threadIdx.x; m < 2 * kBM; m += kThreads) {
         const int t = q0 + m / G;
         if (t >= C) continue;
         const size_t row = (size_t)(c0 + t) * a.Hq + g * G + m % G;
-        if (a.part_o) {
-          for (int i = 0; i < kD; ++i) a.part_o[row * kD + i] = 0.f;
-          a.part_ml[2 * row] = -INFINITY;
-          a.part_ml[2 * row + 1] = 0.f;
+        if (part_o) {
+          for (int i = 0; i < kD; ++i) part_o[row * kD + i] = 0.f;
+          part_ml[2 * row] = -INFINITY;
+          part_ml[2 * row + 1] = 0.f;
         } else {
           uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kD);
           for (int i = 0; i < kD / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
         }
       }
     }
-    if (threadIdx.x == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
+    if (bad && threadIdx.x == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
     return;
   }
-  const int npages = (ctx + B - 1) / B;
+  const int npages = (ctx + B - 1) / B;  // pages of this CTA's key range
   // last valid position of the CTA (non-causal rows all sit at ctx - 1)
   const int pos_hi = a.causal ? ctx - C + min(C, q0 + 2 * TP) - 1 : ctx - 1;
   const int T = pos_hi / kBN + 1;                         // key tiles
@@ -171,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      const int32_t *bt_row = a.bt + (size_t)r * a.max_blocks;
+      const int32_t *bt_row = a.bt + (size_t)r * a.max_blocks + key_lo / B;
       auto page_ids = [&](int j, int (&pages)[PAGES]) {  // validated ids of tile j, -1 = none
 #pragma unroll
         for (int i = 0; i < PAGES; ++i) {
@@ -381,8 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + o_col + c * 32, v);
         tmem_wait_ld();
         if (!row_valid) continue;
-        if (a.part_o) {
-          float4 *dst = reinterpret_cast<float4 *>(a.part_o + row * kD);
+        if (part_o) {
+          float4 *dst = reinterpret_cast<float4 *>(part_o + row * kD);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             dst[c * 8 + i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
@@ -400,9 +408,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_valid && a.part_o) {
-        a.part_ml[2 * row] = m_run;
-        a.part_ml[2 * row + 1] = l_run;
+      if (row_valid && part_o) {
+        part_ml[2 * row] = m_run;
+        part_ml[2 * row + 1] = l_run;
       }
     }
   }
@@ -441,7 +449,8 @@ int dispatch_g(int G, const CUtensorMap &tk, const CUtensorMap &tv, const Prefil
 
 int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, int max_q_len, int total_q,
                    const void *k_pool, const void *v_pool, const int32_t *block_tables, const int32_t *context_lens,
-                   void *out, float *part_o, float *part_ml, int causal, int32_t *err_flag, void *stream) {
+                   void *out, float *part_o, float *part_ml, int causal, int kparts, int kpart_len,
+                   int32_t *err_flag, void *stream) {
   int st = validate_decode_desc(d);
   if (st != PA_OK) return st;
   if (d->head_dim != 128) return PA_ERR_UNSUPPORTED;
@@ -454,7 +463,9 @@ int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, 
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || (out && !aligned16(out)) ||
       (part_o && (!aligned16(part_o) || !part_ml)))
     return PA_ERR_INVALID;
-  if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  if (kparts < 1 || (kparts > 1 && (causal || !part_o || kpart_len <= 0 || kpart_len % 128 != 0)))
+    return PA_ERR_INVALID;
+  if ((long long)d->num_seqs * kparts > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
   const long long tiles = ((long long)max_q_len * G + 2 * kBM - 1) / (2 * kBM);
   if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
   const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
@@ -480,7 +491,9 @@ int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, 
   a.causal = causal;
   a.part_o = part_o;
   a.part_ml = part_ml;
-  const dim3 grid((unsigned)tiles, d->num_kv_heads, d->num_seqs);
+  a.kparts = kparts;
+  a.kpart_len = kpart_len;
+  const dim3 grid((unsigned)tiles, d->num_kv_heads, d->num_seqs * kparts);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d->block_size == 16 ? dispatch_g<16>(G, tk, tv, a, grid, s) : dispatch_g<32>(G, tk, tv, a, grid, s);
 }
@@ -493,5 +506,5 @@ extern "C" int pa_paged_attention_prefill_chunk(const pa_decode_desc *d, const v
                                                 const int32_t *context_lens, void *out, int32_t *err_flag,
                                                 void *stream) {
   return pa::prefill_launch(d, q, cu_q, max_q_len, total_q, k_pool, v_pool, block_tables, context_lens, out,
-                            nullptr, nullptr, 1, err_flag, stream);
+                            nullptr, nullptr, 1, 1, 0, err_flag, stream);
 }

@@ -9,8 +9,12 @@
 // once, for all of the group's query rows together (sequences x query heads),
 // as a dense contraction on the tensor cores; each sequence's decode then
 // covers only its own keys P .. ctx-1 and merges the prefix's partial softmax
-// state (m, l, o/l) exactly as split-K parts are merged.
+// states (m, l, o/l) exactly as split-K parts are merged.  When the groups
+// alone would not fill the GPU, the prefix is cut into up to 8 key ranges of
+// whole 128-key tiles, each attended by its own CTAs into its own state.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "pa_internal.h"
 #include "pagedattn.h"
@@ -27,8 +31,8 @@ struct Layout {
 Layout layout(const pa_decode_desc *d) {
   Layout l;
   l.decode = up256(pa::make_decode_plan(d, pa::current_sm_count()).total());
-  l.pre_o = up256((size_t)d->num_seqs * d->num_q_heads * d->head_dim * sizeof(float));
-  l.pre_ml = up256((size_t)d->num_seqs * d->num_q_heads * 2 * sizeof(float));
+  l.pre_o = up256((size_t)pa::kMaxPrefixParts * d->num_seqs * d->num_q_heads * d->head_dim * sizeof(float));
+  l.pre_ml = up256((size_t)pa::kMaxPrefixParts * d->num_seqs * d->num_q_heads * 2 * sizeof(float));
   return l;
 }
 
@@ -62,15 +66,24 @@ extern "C" int pa_paged_attention_decode_shared_prefix(
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *pre_o = reinterpret_cast<float *>(ws + l.decode);
   float *pre_ml = reinterpret_cast<float *>(ws + l.decode + l.pre_o);
-  // 1. each group's shared prefix, all of its rows at once, on the tensor cores
+  // 1. each group's shared prefix, all of its rows at once, on the tensor cores;
+  //    key ranges so that the pass has about one CTA per SM
+  const int G = d->num_q_heads / d->num_kv_heads;
+  const long long base = (long long)num_groups * d->num_kv_heads * (((long long)max_group_size * G + 255) / 256);
+  const int sms = std::max(current_sm_count(), 1);
+  int kparts = (int)std::min<long long>(kMaxPrefixParts, std::max<long long>(1, (sms + base - 1) / base));
+  kparts = std::min(kparts, (max_prefix_len + 127) / 128);
+  const int kpart_len = ((max_prefix_len + kparts - 1) / kparts + 127) / 128 * 128;
+  kparts = (max_prefix_len + kpart_len - 1) / kpart_len;
   pa_decode_desc pd = *d;
   pd.num_seqs = num_groups;
   pd.max_blocks_per_seq = prefix_max_blocks;
   pd.max_context_len = max_prefix_len;
   st = prefill_launch(&pd, q, group_starts, max_group_size, d->num_seqs, k_pool, v_pool, prefix_tables,
-                      group_prefix_lens, nullptr, pre_o, pre_ml, /*causal=*/0, err_flag, stream);
+                      group_prefix_lens, nullptr, pre_o, pre_ml, /*causal=*/0, kparts, kparts > 1 ? kpart_len : 0,
+                      err_flag, stream);
   if (st != PA_OK) return st;
-  // 2. every sequence's own keys, merged with its group's prefix state
-  const DecodePrefix pre{group_starts, group_prefix_lens, num_groups, pre_o, pre_ml};
+  // 2. every sequence's own keys, merged with its group's prefix states
+  const DecodePrefix pre{group_starts, group_prefix_lens, num_groups, pre_o, pre_ml, kparts};
   return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, ws, l.decode, err_flag, stream, &pre);
 }
