@@ -238,6 +238,23 @@ int pa_copy_blocks(void *const *k_pools, void *const *v_pools, int num_layers,
                    const int64_t *block_pairs, int num_pairs, int num_blocks, size_t block_bytes,
                    int32_t *err_flag, void *stream);
 
+/* Block moves between two pools for preemptive swapping [CHUNK] (a paused
+ * request's pages go to host RAM and come back later): for every layer l and
+ * pair i, block pairs[i][1] of dst_*_pools[l] := block pairs[i][0] of
+ * src_*_pools[l], K and V.  Either side may be device memory or pinned host
+ * memory the GPU can address (cudaHostAlloc / cudaHostRegister; on
+ * Grace-Blackwell the kernel reads and writes it over the chip-to-chip link).
+ * Bit-exact.  Destination blocks must be distinct.
+ *   *_pools      HOST arrays of num_layers pointers (1..256 layers)
+ *   block_pairs  device int64 [num_pairs][2] (src block, dst block)
+ *   src_num_blocks / dst_num_blocks  blocks in each source / destination pool
+ *   block_bytes  num_kv_heads*block_size*head_dim*2, a multiple of 16
+ * A pair outside either pool is skipped with PA_DEVERR_PAIR. */
+int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *const *dst_k_pools,
+                   void *const *dst_v_pools, int num_layers, const int64_t *block_pairs, int num_pairs,
+                   int src_num_blocks, int dst_num_blocks, size_t block_bytes, int32_t *err_flag,
+                   void *stream);
+
 /* ------------------------------------------------------------------------
  * Host block manager [TABLE][SHARE][CHUNK] (plain C++, no GPU): a free list
  * of num_blocks physical blocks of block_size tokens, per-sequence block
@@ -251,6 +268,9 @@ typedef struct pa_bm pa_bm;
 
 /* NULL on bad arguments (num_blocks <= 0 or block_size <= 0) or no memory. */
 pa_bm *pa_bm_create(int num_blocks, int block_size);
+
+/* The same with num_host_blocks (>= 0) host blocks for swapped-out sequences. */
+pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_size);
 void pa_bm_destroy(pa_bm *bm);
 
 /* New sequence seq_id (>= 0, unused) holding num_tokens (>= 0) tokens:
@@ -274,6 +294,38 @@ int pa_bm_free_seq(pa_bm *bm, int seq_id);
 /* Copies seq_id's block table into out[0..cap-1]; *n = its length.  Returns
  * PA_ERR_INVALID if cap < *n (nothing copied beyond cap). */
 int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n);
+
+/* Automatic prefix caching [SHARE]: like pa_bm_add_seq for a prompt of
+ * num_tokens token ids, but every full block of the prompt is registered by
+ * content (the block before it and its block_size token ids, compared
+ * exactly), and a new prompt reuses the longest chain of registered full
+ * blocks from its start (ref_count + 1 each; a registered block keeps its
+ * content after its last user frees it, until the block is handed out
+ * again).  *cached_tokens (may be NULL) gets the number of leading tokens
+ * whose K/V are already in the cache: the caller writes and prefills only
+ * tokens cached_tokens .. num_tokens-1.  A block registered here holds valid
+ * K/V once this sequence's prefill of it has run.  PA_ERR_OOM leaves no
+ * trace. */
+int pa_bm_add_seq_tokens(pa_bm *bm, int seq_id, const int32_t *tokens, int num_tokens, int *cached_tokens);
+
+/* Number of blocks currently registered in the prefix cache. */
+int pa_bm_num_cached_blocks(const pa_bm *bm);
+
+/* Moves seq_id to host blocks (preemption): every block must be unshared
+ * (ref_count 1, else PA_ERR_STATE).  Writes *n (device block, host block)
+ * pairs for pa_swap_blocks (device pools -> host pools) into pairs_out
+ * [cap][2] and frees the device blocks.  PA_ERR_OOM (not enough free host
+ * blocks) and PA_ERR_INVALID (cap < *n) leave everything unchanged.  While
+ * swapped, the sequence cannot be forked, appended to or listed. */
+int pa_bm_swap_out(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n);
+
+/* Brings a swapped-out seq_id back: new device blocks, *n (host block, device
+ * block) pairs for pa_swap_blocks (host pools -> device pools); the host
+ * blocks are freed.  PA_ERR_OOM leaves everything unchanged. */
+int pa_bm_swap_in(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n);
+
+/* Number of free host blocks. */
+int pa_bm_num_free_host(const pa_bm *bm);
 
 /* Tokens held by seq_id, or -1 if unknown. */
 int pa_bm_seq_len(const pa_bm *bm, int seq_id);

@@ -24,7 +24,9 @@ DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 
 EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
     "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk",
-    "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_reshape_and_cache", "pa_copy_blocks",
+    "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_swap_blocks",
+    "pa_bm_create_with_host", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_host",
+    "pa_bm_add_seq_tokens", "pa_bm_num_cached_blocks", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
 )
@@ -83,6 +85,21 @@ def load(path: Optional[str] = None):
         lib.pa_copy_blocks.argtypes = [_c.POINTER(_P), _c.POINTER(_P), i, _P, i, i, sz, _P, _P]
         lib.pa_bm_create.restype = _P
         lib.pa_bm_create.argtypes = [i, i]
+        lib.pa_bm_create_with_host.restype = _P
+        lib.pa_bm_create_with_host.argtypes = [i, i, i]
+        lib.pa_bm_swap_out.restype = i
+        lib.pa_bm_swap_out.argtypes = [_P, i, _c.POINTER(i64), i, _c.POINTER(i)]
+        lib.pa_bm_swap_in.restype = i
+        lib.pa_bm_swap_in.argtypes = [_P, i, _c.POINTER(i64), i, _c.POINTER(i)]
+        lib.pa_bm_add_seq_tokens.restype = i
+        lib.pa_bm_add_seq_tokens.argtypes = [_P, i, _c.POINTER(_c.c_int32), i, _c.POINTER(i)]
+        lib.pa_bm_num_cached_blocks.restype = i
+        lib.pa_bm_num_cached_blocks.argtypes = [_P]
+        lib.pa_bm_num_free_host.restype = i
+        lib.pa_bm_num_free_host.argtypes = [_P]
+        lib.pa_swap_blocks.restype = i
+        lib.pa_swap_blocks.argtypes = [_c.POINTER(_P), _c.POINTER(_P), _c.POINTER(_P), _c.POINTER(_P), i, _P, i, i,
+                                       i, sz, _P, _P]
         lib.pa_bm_destroy.restype = None
         lib.pa_bm_destroy.argtypes = [_P]
         lib.pa_bm_add_seq.restype = i
@@ -318,13 +335,36 @@ def copy_blocks(k_pools: Sequence, v_pools: Sequence, block_pairs, *, err_flag=N
     _check(st, "pa_copy_blocks")
 
 
+def swap_blocks(src_k_pools: Sequence, src_v_pools: Sequence, dst_k_pools: Sequence, dst_v_pools: Sequence,
+                block_pairs, *, err_flag=None, stream=None):
+    """dst block pairs[i][1] := src block pairs[i][0] for every layer, K and V;
+    pools are CUDA tensors or pinned host tensors (see pagedattn.h)."""
+    import torch
+    L = len(src_k_pools)
+    pools = [list(src_k_pools), list(src_v_pools), list(dst_k_pools), list(dst_v_pools)]
+    if L == 0 or any(len(p) != L for p in pools):
+        raise ValueError("pool lists must be non-empty and of equal length")
+    for p in pools:
+        for t in p:
+            if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+                raise TypeError("pools must be contiguous 4-D bf16 tensors")
+            if not t.is_cuda and not t.is_pinned():
+                raise ValueError("host pools must be pinned")
+    _need(block_pairs, torch.int64, "block_pairs", 2)
+    arr = [(_P * L)(*[t.data_ptr() for t in p]) for p in pools]
+    st = load().pa_swap_blocks(arr[0], arr[1], arr[2], arr[3], L, _ptr(block_pairs), int(block_pairs.shape[0]),
+                               int(src_k_pools[0].shape[0]), int(dst_k_pools[0].shape[0]),
+                               int(src_k_pools[0][0].numel() * 2), _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_swap_blocks")
+
+
 # --------------------------------------------------------------- block manager
 class BlockManager:
     """Host block manager (free list, block tables, ref counts, copy-on-write)."""
 
-    def __init__(self, num_blocks: int, block_size: int):
+    def __init__(self, num_blocks: int, block_size: int, num_host_blocks: int = 0):
         self._lib = load()
-        self._h = self._lib.pa_bm_create(int(num_blocks), int(block_size))
+        self._h = self._lib.pa_bm_create_with_host(int(num_blocks), int(num_host_blocks), int(block_size))
         if not self._h:
             raise PaError(PA_ERR_INVALID, "pa_bm_create")
         self.num_blocks = num_blocks
@@ -366,6 +406,41 @@ class BlockManager:
         _check(self._lib.pa_bm_block_table(self._h, int(seq_id), buf, n.value, _c.byref(n)),
                "pa_bm_block_table")
         return list(buf[: n.value])
+
+    def _swap(self, fn, seq_id):
+        n = _c.c_int()
+        cap = 1
+        while True:
+            buf = (_c.c_int64 * (2 * cap))()
+            st = fn(self._h, int(seq_id), buf, cap, _c.byref(n))
+            if st == PA_ERR_INVALID and n.value > cap:
+                cap = n.value
+                continue
+            _check(st, fn.__name__)
+            return [(buf[2 * i], buf[2 * i + 1]) for i in range(n.value)]
+
+    def swap_out(self, seq_id: int):
+        """Returns the (device block, host block) pairs to copy."""
+        return self._swap(self._lib.pa_bm_swap_out, seq_id)
+
+    def swap_in(self, seq_id: int):
+        """Returns the (host block, device block) pairs to copy."""
+        return self._swap(self._lib.pa_bm_swap_in, seq_id)
+
+    def add_seq_tokens(self, seq_id: int, tokens) -> int:
+        """New sequence holding the prompt `tokens` (ints); returns how many
+        leading tokens were found in the prefix cache."""
+        arr = (_c.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+        cached = _c.c_int()
+        _check(self._lib.pa_bm_add_seq_tokens(self._h, int(seq_id), arr, len(tokens), _c.byref(cached)),
+               "pa_bm_add_seq_tokens")
+        return cached.value
+
+    def num_cached_blocks(self) -> int:
+        return self._lib.pa_bm_num_cached_blocks(self._h)
+
+    def num_free_host(self) -> int:
+        return self._lib.pa_bm_num_free_host(self._h)
 
     def seq_len(self, seq_id: int) -> int:
         return self._lib.pa_bm_seq_len(self._h, int(seq_id))

@@ -7,8 +7,11 @@
 // Multi-GPU LLM Serving with PagedAttention" ("What Is PagedAttention?": blocks
 // allocated on demand, shared prefixes with copy-on-write) and "Configuring
 // vLLM and PagedAttention for High Throughput Enterprise LLM Serving"
-// ("High-Throughput Batching": pages go back to the free pool on <eos>).
+// ("High-Throughput Batching": pages go back to the free pool on <eos>, and
+// the preemptive-swapping answer: a paused request's pages move to host RAM
+// and come back when device blocks free up).
 #include <algorithm>
+#include <cstdint>
 #include <new>
 #include <unordered_map>
 #include <unordered_set>
@@ -19,8 +22,9 @@
 namespace {
 
 struct Seq {
-  std::vector<int32_t> blocks;
+  std::vector<int32_t> blocks;  // device block ids, or host block ids while swapped out
   int len = 0;
+  bool swapped = false;
 };
 
 }  // namespace
@@ -29,24 +33,86 @@ struct pa_bm {
   int num_blocks = 0;
   int block_size = 0;
   std::vector<int32_t> ref;        // per block, 0 = free
-  std::vector<int32_t> free_list;  // LIFO stack; back() is handed out next
+  std::vector<int32_t> free_list;  // LIFO stack; back() is handed out next (may hold revived entries)
+  std::vector<uint8_t> in_free;    // per block: has an entry in free_list (at most one)
+  int nfree = 0;                   // blocks with ref 0
+  // Prefix cache: full blocks registered by content.  A block's key is its
+  // parent (the block before it in the sequence, -1 for the first) and its B
+  // token ids; lookups compare both exactly, the hash only picks the bucket.
+  // A cached block keeps its content after its last user frees it, until the
+  // block is handed out again.
+  std::unordered_map<uint64_t, std::vector<int32_t>> cache;
+  std::vector<int32_t> c_parent;             // per block, -2 = not cached
+  std::vector<std::vector<int32_t>> c_tokens;
+  int ncached = 0;
+  std::vector<int32_t> host_free;  // free host blocks (LIFO), for swapped-out sequences
+  int num_host_blocks = 0;
   std::unordered_map<int, Seq> seqs;
 
-  int32_t take() {
-    int32_t b = free_list.back();
-    free_list.pop_back();
-    ref[b] = 1;
-    return b;
+  static uint64_t key_hash(int32_t parent, const int32_t *tok, int n) {
+    uint64_t h = 0x9E3779B97F4A7C15ull ^ (uint64_t)(uint32_t)parent;
+    for (int i = 0; i < n; ++i) {
+      h ^= (uint64_t)(uint32_t)tok[i] + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+      h = (h ^ (h >> 31)) * 0xBF58476D1CE4E5B9ull;
+    }
+    return h ^ (h >> 29);
+  }
+  void uncache(int32_t b) {
+    if (c_parent[b] == -2) return;
+    auto it = cache.find(key_hash(c_parent[b], c_tokens[b].data(), block_size));
+    if (it != cache.end()) {
+      auto &v = it->second;
+      for (size_t i = 0; i < v.size(); ++i)
+        if (v[i] == b) {
+          v.erase(v.begin() + i);
+          break;
+        }
+      if (v.empty()) cache.erase(it);
+    }
+    c_parent[b] = -2;
+    c_tokens[b].clear();
+    --ncached;
+  }
+  int32_t take() {  // caller checked nfree > 0
+    for (;;) {
+      int32_t b = free_list.back();
+      free_list.pop_back();
+      in_free[b] = 0;
+      if (ref[b] != 0) continue;  // revived by a cache hit after it was freed
+      uncache(b);                 // its old content is about to be overwritten
+      ref[b] = 1;
+      --nfree;
+      return b;
+    }
   }
   void drop(int32_t b) {
-    if (--ref[b] == 0) free_list.push_back(b);
+    if (--ref[b] == 0) {
+      if (!in_free[b]) {  // a revived block still has its old entry: reuse it
+        free_list.push_back(b);
+        in_free[b] = 1;
+      }
+      ++nfree;
+    }
+  }
+  int32_t lookup(int32_t parent, const int32_t *tok) const {
+    auto it = cache.find(key_hash(parent, tok, block_size));
+    if (it == cache.end()) return -1;
+    for (int32_t b : it->second)
+      if (c_parent[b] == parent && std::equal(c_tokens[b].begin(), c_tokens[b].end(), tok)) return b;
+    return -1;
+  }
+  void register_block(int32_t b, int32_t parent, const int32_t *tok) {
+    c_parent[b] = parent;
+    c_tokens[b].assign(tok, tok + block_size);
+    cache[key_hash(parent, tok, block_size)].push_back(b);
+    ++ncached;
   }
 };
 
 extern "C" {
 
-pa_bm *pa_bm_create(int num_blocks, int block_size) {
-  if (num_blocks <= 0 || block_size <= 0) return nullptr;
+pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_size) {
+  if (num_blocks <= 0 || num_host_blocks < 0 || block_size <= 0) return nullptr;
   pa_bm *bm = new (std::nothrow) pa_bm();
   if (!bm) return nullptr;
   bm->num_blocks = num_blocks;
@@ -54,8 +120,17 @@ pa_bm *pa_bm_create(int num_blocks, int block_size) {
   bm->ref.assign(num_blocks, 0);
   bm->free_list.reserve(num_blocks);
   for (int b = num_blocks - 1; b >= 0; --b) bm->free_list.push_back(b);
+  bm->nfree = num_blocks;
+  bm->in_free.assign(num_blocks, 1);
+  bm->c_parent.assign(num_blocks, -2);
+  bm->c_tokens.resize(num_blocks);
+  bm->num_host_blocks = num_host_blocks;
+  bm->host_free.reserve(num_host_blocks);
+  for (int b = num_host_blocks - 1; b >= 0; --b) bm->host_free.push_back(b);
   return bm;
 }
+
+pa_bm *pa_bm_create(int num_blocks, int block_size) { return pa_bm_create_with_host(num_blocks, 0, block_size); }
 
 void pa_bm_destroy(pa_bm *bm) { delete bm; }
 
@@ -63,7 +138,7 @@ int pa_bm_add_seq(pa_bm *bm, int seq_id, int num_tokens) {
   if (!bm || seq_id < 0 || num_tokens < 0) return PA_ERR_INVALID;
   if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
   const int64_t need = ((int64_t)num_tokens + bm->block_size - 1) / bm->block_size;
-  if (need > (int64_t)bm->free_list.size()) return PA_ERR_OOM;
+  if (need > (int64_t)bm->nfree) return PA_ERR_OOM;
   Seq s;
   s.len = num_tokens;
   s.blocks.reserve(need);
@@ -75,7 +150,7 @@ int pa_bm_add_seq(pa_bm *bm, int seq_id, int num_tokens) {
 int pa_bm_fork(pa_bm *bm, int parent_id, int child_id) {
   if (!bm || child_id < 0) return PA_ERR_INVALID;
   auto it = bm->seqs.find(parent_id);
-  if (it == bm->seqs.end() || bm->seqs.count(child_id)) return PA_ERR_STATE;
+  if (it == bm->seqs.end() || bm->seqs.count(child_id) || it->second.swapped) return PA_ERR_STATE;
   Seq c = it->second;
   for (int32_t b : c.blocks) ++bm->ref[b];
   bm->seqs.emplace(child_id, std::move(c));
@@ -85,18 +160,18 @@ int pa_bm_fork(pa_bm *bm, int parent_id, int child_id) {
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]) {
   if (!bm || !slot_out || !cow_pair_out) return PA_ERR_INVALID;
   auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_STATE;
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
   Seq &s = it->second;
   const int B = bm->block_size;
   const int j = s.len;
   cow_pair_out[0] = cow_pair_out[1] = -1;
   if (j % B == 0) {  // the token opens a new block
-    if (bm->free_list.empty()) return PA_ERR_OOM;
+    if (bm->nfree == 0) return PA_ERR_OOM;
     s.blocks.push_back(bm->take());
   } else {
     int32_t &last = s.blocks[j / B];
     if (bm->ref[last] > 1) {  // shared partial block: copy on write
-      if (bm->free_list.empty()) return PA_ERR_OOM;
+      if (bm->nfree == 0) return PA_ERR_OOM;
       int32_t fresh = bm->take();
       cow_pair_out[0] = last;
       cow_pair_out[1] = fresh;
@@ -113,6 +188,12 @@ int pa_bm_free_seq(pa_bm *bm, int seq_id) {
   if (!bm) return PA_ERR_INVALID;
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end()) return PA_ERR_STATE;
+  if (it->second.swapped) {  // its blocks live on the host
+    const auto &hb = it->second.blocks;
+    for (auto r = hb.rbegin(); r != hb.rend(); ++r) bm->host_free.push_back(*r);
+    bm->seqs.erase(it);
+    return PA_OK;
+  }
   for (int32_t b : it->second.blocks) {
     if (bm->ref[b] <= 0) return PA_ERR_STATE;  // cannot happen unless corrupted
   }
@@ -126,7 +207,7 @@ int pa_bm_free_seq(pa_bm *bm, int seq_id) {
 int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n) {
   if (!bm || !n) return PA_ERR_INVALID;
   auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PA_ERR_STATE;
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
   const auto &bl = it->second.blocks;
   *n = (int)bl.size();
   if (cap < *n || (!out && *n > 0)) return PA_ERR_INVALID;
@@ -145,7 +226,92 @@ int pa_bm_ref_count(const pa_bm *bm, int block) {
   return bm->ref[block];
 }
 
-int pa_bm_num_free(const pa_bm *bm) { return bm ? (int)bm->free_list.size() : -1; }
+int pa_bm_num_free(const pa_bm *bm) { return bm ? bm->nfree : -1; }
+
+int pa_bm_add_seq_tokens(pa_bm *bm, int seq_id, const int32_t *tokens, int num_tokens, int *cached_tokens) {
+  if (!bm || seq_id < 0 || num_tokens < 0 || (num_tokens > 0 && !tokens)) return PA_ERR_INVALID;
+  if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
+  const int B = bm->block_size;
+  const int nfull = num_tokens / B;
+  const int need = (num_tokens + B - 1) / B;
+  // longest chain of cached full blocks from the start
+  std::vector<int32_t> hit;
+  int32_t parent = -1;
+  for (int i = 0; i < nfull; ++i) {
+    const int32_t b = bm->lookup(parent, tokens + (size_t)i * B);
+    if (b < 0) break;
+    hit.push_back(b);
+    parent = b;
+  }
+  int revive = 0;  // hits that sit in the free pool
+  for (int32_t b : hit) revive += bm->ref[b] == 0;
+  if ((int64_t)(need - (int)hit.size()) > (int64_t)bm->nfree - revive) return PA_ERR_OOM;
+  Seq s;
+  s.len = num_tokens;
+  for (int32_t b : hit) {
+    if (bm->ref[b]++ == 0) --bm->nfree;  // revived: its stale free-list entry is skipped later
+    s.blocks.push_back(b);
+  }
+  parent = hit.empty() ? -1 : hit.back();
+  for (int i = (int)hit.size(); i < need; ++i) {
+    const int32_t b = bm->take();
+    if (i < nfull) {  // a full block of the prompt: findable by later prompts
+      bm->register_block(b, parent, tokens + (size_t)i * B);
+      parent = b;
+    }
+    s.blocks.push_back(b);
+  }
+  if (cached_tokens) *cached_tokens = (int)hit.size() * B;
+  bm->seqs.emplace(seq_id, std::move(s));
+  return PA_OK;
+}
+
+int pa_bm_num_cached_blocks(const pa_bm *bm) { return bm ? bm->ncached : -1; }
+
+int pa_bm_swap_out(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n) {
+  if (!bm || !n) return PA_ERR_INVALID;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
+  Seq &s = it->second;
+  *n = (int)s.blocks.size();
+  if (cap < *n || (!pairs_out && *n > 0)) return PA_ERR_INVALID;
+  for (int32_t b : s.blocks)
+    if (bm->ref[b] != 1) return PA_ERR_STATE;  // shared blocks stay with their other users
+  if ((int)bm->host_free.size() < *n) return PA_ERR_OOM;
+  for (int i = 0; i < *n; ++i) {
+    const int32_t d = s.blocks[i];
+    const int32_t h = bm->host_free.back();
+    bm->host_free.pop_back();
+    pairs_out[2 * i] = d;
+    pairs_out[2 * i + 1] = h;
+    bm->drop(d);
+    s.blocks[i] = h;
+  }
+  s.swapped = true;
+  return PA_OK;
+}
+
+int pa_bm_swap_in(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n) {
+  if (!bm || !n) return PA_ERR_INVALID;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || !it->second.swapped) return PA_ERR_STATE;
+  Seq &s = it->second;
+  *n = (int)s.blocks.size();
+  if (cap < *n || (!pairs_out && *n > 0)) return PA_ERR_INVALID;
+  if (bm->nfree < *n) return PA_ERR_OOM;
+  for (int i = 0; i < *n; ++i) {
+    const int32_t h = s.blocks[i];
+    const int32_t d = bm->take();
+    pairs_out[2 * i] = h;
+    pairs_out[2 * i + 1] = d;
+    bm->host_free.push_back(h);
+    s.blocks[i] = d;
+  }
+  s.swapped = false;
+  return PA_OK;
+}
+
+int pa_bm_num_free_host(const pa_bm *bm) { return bm ? (int)bm->host_free.size() : -1; }
 
 int64_t pa_bm_wasted_slots(const pa_bm *bm) {
   if (!bm) return -1;
@@ -154,7 +320,7 @@ int64_t pa_bm_wasted_slots(const pa_bm *bm) {
   std::unordered_map<int32_t, int> fill;
   for (const auto &kv : bm->seqs) {
     const Seq &s = kv.second;
-    if (s.blocks.empty()) continue;
+    if (s.blocks.empty() || s.swapped) continue;
     int f = s.len - (int)(s.blocks.size() - 1) * bm->block_size;
     auto it = fill.find(s.blocks.back());
     if (it == fill.end())

@@ -187,3 +187,96 @@ def test_random_operations_keep_invariants():
     for s in list(live):
         bm.free_seq(s)
     assert bm.num_free() == N
+
+
+def test_swap_out_and_in_move_blocks_between_pools():
+    bm = pa.BlockManager(8, 16, num_host_blocks=6)
+    bm.add_seq(1, 40)   # 3 blocks
+    bm.add_seq(2, 20)   # 2 blocks
+    t1 = bm.block_table(1)
+    out = bm.swap_out(1)
+    assert [d for d, _ in out] == t1 and len({h for _, h in out}) == 3
+    assert bm.num_free() == 8 - 2 and bm.num_free_host() == 3
+    assert all(bm.ref_count(b) == 0 for b in t1)
+    with pytest.raises(pa.PaError) as e:
+        bm.append(1)
+    assert e.value.status == pa.PA_ERR_STATE
+    with pytest.raises(pa.PaError):
+        bm.block_table(1)
+    back = bm.swap_in(1)
+    assert [h for h, _ in back] == [h for _, h in out]
+    assert bm.block_table(1) == [d for _, d in back] and bm.seq_len(1) == 40
+    assert bm.num_free_host() == 6 and bm.num_free() == 8 - 5
+    slot, _ = bm.append(1)  # usable again
+    assert slot == bm.block_table(1)[2] * 16 + 8
+
+
+def test_swap_refuses_shared_blocks_and_reports_oom_without_trace():
+    bm = pa.BlockManager(10, 16, num_host_blocks=2)
+    bm.add_seq(0, 32)
+    bm.fork(0, 1)
+    with pytest.raises(pa.PaError) as e:
+        bm.swap_out(1)
+    assert e.value.status == pa.PA_ERR_STATE
+    bm.add_seq(5, 48)  # 3 blocks > 2 host blocks
+    with pytest.raises(pa.PaError) as e:
+        bm.swap_out(5)
+    assert e.value.status == pa.PA_ERR_OOM
+    assert bm.num_free_host() == 2 and len(bm.block_table(5)) == 3
+    bm.add_seq(6, 20)
+    bm.swap_out(6)
+    bm.free_seq(6)  # freeing a swapped sequence returns its host blocks
+    assert bm.num_free_host() == 2
+
+
+def test_prefix_cache_reuses_full_blocks_of_identical_prefixes():
+    """Automatic prefix caching: a prompt that repeats another prompt's leading
+    full blocks points at the same physical blocks."""
+    B = 16
+    bm = pa.BlockManager(64, B)
+    st = wl.Stream(40, 1)
+    a = [int(x) for x in st.integers(0, 50000, 100)]       # 6 full blocks + 4 tokens
+    assert bm.add_seq_tokens(0, a) == 0
+    assert bm.num_cached_blocks() == 6
+    assert bm.add_seq_tokens(1, a) == 96                    # every full block found
+    ta, tb = bm.block_table(0), bm.block_table(1)
+    assert ta[:6] == tb[:6] and ta[6] != tb[6]              # the partial block is private
+    assert all(bm.ref_count(b) == 2 for b in ta[:6])
+    c = a[:40] + [a[40] + 1] + a[41:]                       # differs inside block 2
+    assert bm.add_seq_tokens(2, c) == 32
+    assert bm.block_table(2)[:2] == ta[:2] and bm.block_table(2)[2] != ta[2]
+    d = a[:5] + [a[5] + 1] + a[6:]                          # differs in block 0: no reuse at all
+    assert bm.add_seq_tokens(3, d) == 0
+
+
+def test_prefix_cache_survives_free_until_reallocated():
+    B = 16
+    bm = pa.BlockManager(10, B)
+    p = list(range(64))                                     # 4 full blocks
+    assert bm.add_seq_tokens(0, p) == 0
+    t0 = bm.block_table(0)
+    bm.free_seq(0)
+    assert bm.num_free() == 10
+    assert bm.add_seq_tokens(1, p) == 64                    # content still there
+    assert bm.block_table(1) == t0 and bm.num_free() == 6
+    bm.free_seq(1)
+    bm.add_seq(2, 10 * B)                                   # takes every block: the cache is evicted
+    assert bm.num_cached_blocks() == 0
+    bm.free_seq(2)
+    assert bm.add_seq_tokens(3, p) == 0
+
+
+def test_prefix_cache_never_hands_out_a_block_twice():
+    """Blocks freed, revived by a cache hit and freed again keep one free-list
+    entry each."""
+    B = 4
+    bm = pa.BlockManager(6, B)
+    p = list(range(8))
+    for rnd in range(5):
+        bm.add_seq_tokens(10 + rnd, p)
+        bm.free_seq(10 + rnd)
+    bm.add_seq(1, 6 * B)
+    t = bm.block_table(1)
+    assert sorted(t) == list(range(6))
+    with pytest.raises(pa.PaError):
+        bm.add_seq(2, 1)

@@ -146,3 +146,53 @@ def test_prefix_sharing_cow_flow(torch, ora, independent):
     heads = [(s, h) for s in range(0, S, 9) for h in (0, 13, 31)]
     ref = np.stack([ora.decode_head(q, kp, vp, bt, ctx, 1 / np.sqrt(128), s, h)[0] for s, h in heads])
     assert_close(np.stack([got[s, h] for s, h in heads]), ref, "prefix sharing")
+
+
+def test_swap_out_and_back_in_is_bit_exact(torch, ora):
+    """Preemption round trip: a sequence's pages go to a pinned host pool,
+    the device blocks are reused, and the pages come back to new device
+    blocks bit for bit; decode over the new table is bit-identical."""
+    case = wl.make_decode_case("swap", [300, 77, 500], 16, 4, 128, 16, seed=14, pool_blocks=120,
+                               with_new_tokens=False)
+    L = 2
+    st = wl.Stream(14, 2)
+    kps = [case.k_pool] + [wl.normal_bf16(st, case.k_pool.shape) for _ in range(L - 1)]
+    vps = [case.v_pool] + [wl.normal_bf16(st, case.v_pool.shape) for _ in range(L - 1)]
+    dk = [bf16_dev(a, torch) for a in kps]
+    dv = [bf16_dev(a, torch) for a in vps]
+    nhost = 64
+    hk = [torch.zeros((nhost,) + tuple(case.k_pool.shape[1:]), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    hv = [torch.zeros_like(h).pin_memory() for h in hk]
+    # sequence 2 is preempted
+    table2 = [int(b) for b in case.block_tables[2] if b >= 0]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = bf16_host(pa.paged_attention_decode(bf16_dev(case.q, torch), dk[0], dv[0],
+                                              torch.from_numpy(case.block_tables).cuda(),
+                                              torch.from_numpy(case.context_lens).cuda(), scale=case.scale,
+                                              max_context_len=case.max_context_len))
+    out_pairs = np.array([(d, h) for h, d in enumerate(table2)], np.int64)  # device block -> host block
+    pa.swap_blocks(dk, dv, hk, hv, torch.from_numpy(out_pairs).cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    for l in range(L):
+        got_k = hk[l].view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got_k[: len(table2)], kps[l][table2])
+    # the device blocks get reused by someone else
+    for l in range(L):
+        dk[l][table2] = 0
+        dv[l][table2] = 0
+    # bring the pages back into other (free) device blocks
+    used = set(int(b) for b in case.block_tables.flatten() if b >= 0)
+    free = [b for b in range(case.num_blocks) if b not in used][: len(table2)]
+    in_pairs = np.array([(h, free[h]) for h in range(len(table2))], np.int64)
+    pa.swap_blocks(hk, hv, dk, dv, torch.from_numpy(in_pairs).cuda(), err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for l in range(L):
+        assert np.array_equal(bf16_host(dk[l])[free], kps[l][table2])
+        assert np.array_equal(bf16_host(dv[l])[free], vps[l][table2])
+    bt = case.block_tables.copy()
+    bt[2, : len(table2)] = free
+    again = bf16_host(pa.paged_attention_decode(bf16_dev(case.q, torch), dk[0], dv[0], torch.from_numpy(bt).cuda(),
+                                                torch.from_numpy(case.context_lens).cuda(), scale=case.scale,
+                                                max_context_len=case.max_context_len))
+    assert np.array_equal(again, ref)
