@@ -14,20 +14,21 @@
 // One CTA per (pair of query tiles, kv head, chunk).  A query tile is 128 MMA
 // rows: 128/G consecutive positions x the G query heads that share the kv
 // head; the CTA holds two consecutive tiles (A and B), so every K/V tile it
-// loads serves 256 rows.  Roles (10 warps):
+// loads serves 256 rows.  Roles (12 warps, three warpgroups):
 //   warps 0-3  tile A: load its Q rows, softmax of one row each (TMEM lane =
 //              row), write P (bf16) back into TMEM over its S, rescale O,
 //              store the output;
 //   warps 4-7  the same for tile B;
 //   warp 8     gathers 128-key K and V tiles page by page with 2-D TMA
-//              (128-byte swizzle) into two-stage K and V rings; a K
-//              stage is refilled
-//              once both S MMAs of its tile are done, a V stage once both PV
-//              MMAs are;
+//              (128-byte swizzle) into two-stage K and V rings; a K stage
+//              is refilled once both S MMAs of its tile are done, a V stage
+//              once both PV MMAs are;
 //   warp 9     owns the TMEM allocation and issues the MMAs in the order
 //              S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...:
 //              S = Q K^T (A and B from shared memory, fp32 into TMEM) and
-//              O += P V (P from TMEM, V MN-major from shared memory).
+//              O += P V (P from TMEM, V MN-major from shared memory);
+//   warps 10-11 idle (they complete the third warpgroup, whose registers go
+//              to the softmax warpgroups).
 // MMAs issued by one thread complete in order, so an S MMA that reuses the
 // TMEM columns of the previous tile's P runs after the PV MMA that read them,
 // and a completed S tells the softmax that the previous PV is done.
@@ -36,7 +37,8 @@
 // against the stale max, which the final normalisation by the same running
 // sum makes exact.  Value rows of keys past the context are zeroed in shared
 // memory before they meet a zero probability (unused cache slots may hold
-// NaNs).  Every wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+// NaNs).  Chunks start in order of decreasing context.  Every wait is
+// bounded; a timeout sets PA_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -81,7 +83,18 @@ constexpr int kOffV = kOffK + KST * kTile;
 constexpr int kOffBar = kOffV + VST * kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr int kTmemCols = 512;  // S/P of A [0,128), of B [128,256); O of A [256,384), of B [384,512)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // three warpgroups
+#ifndef PA_PREFILL_LPT_MAX
+#define PA_PREFILL_LPT_MAX 256
+#endif
+constexpr int kLptMaxSeqs = PA_PREFILL_LPT_MAX;  // longest-first chunk order up to this many chunks
+// Register split (setmaxnreg): the two softmax warpgroups hold a 128-column
+// row of scores each and take kRegsSoftmax per thread; the third warpgroup
+// (producer, MMA issuer, two idle warps) gives its registers back.  The sum
+// equals the launch allocation of kThreads x kRegsLaunch, which the host
+// checks before every launch (a larger sum would wait forever).
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsOther = 72;
+static_assert(256 * kRegsSoftmax + 128 * kRegsOther <= kThreads * kRegsLaunch, "register split");
 
 // Barriers: Q rows stored (both tiles); K and V stage full / free (one per
 // ring slot); S of tile A / B ready; P of tile A / B written; all MMAs done.
@@ -94,6 +107,26 @@ static_assert(NBARS * 8 + 8 <= 256, "barrier area");
 static_assert(kOffBar + 256 + 1024 <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return pack_bf16(a, b); }
+
+// P of one row: 2^(s * scale_log2 - m) for the 128 scores, packed to bf16
+// pairs into TMEM columns [col, col + 64); the row sum adds the unrounded
+// fp32 probabilities in four packed chains (acc).
+__device__ __forceinline__ void probabilities(const float (&s)[kBN], float2 sc2, float2 nm2, uint32_t col,
+                                              float2 (&acc)[4]) {
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t w[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int k = c * 64 + 2 * e;
+      const float2 t = fma2(make_float2(s[k], s[k + 1]), sc2, nm2);
+      const float2 p = make_float2(ex2_ftz(t.x), ex2_ftz(t.y));
+      w[e] = pack2(p.x, p.y);
+      acc[e & 3] = add2(acc[e & 3], p);
+    }
+    tmem_st32(col + c * 32, w);
+  }
+}
 
 template <int B, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -112,7 +145,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = gridDim.x - 1 - blockIdx.x;  // later tiles see more keys: start them first
-  const int g = blockIdx.y, r = blockIdx.z / a.kparts, kpart = blockIdx.z % a.kparts;
+  const int g = blockIdx.y, kpart = blockIdx.z % a.kparts;
+  // Chunks in order of decreasing context (the longest work first), so that
+  // the last CTAs to start are short ones; ties in chunk order.
+  int r = blockIdx.z / a.kparts;
+  if (a.R > 1 && a.R <= kLptMaxSeqs) {
+    __shared__ int s_r;
+    for (int i = threadIdx.x; i < a.R; i += kThreads) {
+      const int ci = __ldg(a.ctx + i);
+      int rank = 0;
+      for (int k = 0; k < a.R; ++k) {
+        const int ck = __ldg(a.ctx + k);
+        rank += (ck > ci) || (ck == ci && k < i);
+      }
+      if (rank == r) s_r = i;
+    }
+    __syncthreads();
+    r = s_r;
+  }
   const int c0 = __ldg(a.cu_q + r), c1 = __ldg(a.cu_q + r + 1);
   const int C = c1 - c0;
   const int ctx_full = __ldg(a.ctx + r);
@@ -175,9 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     return false;
   };
 
-  if (warp == 8) {
-    // ------------------------------------------------------------- producer
-    if (lane == 0) {
+  if (warp >= 8) {
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == 8 && lane == 0) {
+      // ----------------------------------------------------------- producer
       const uint64_t pol = policy_evict_first();
       const int32_t *bt_row = a.bt + (size_t)r * a.max_blocks + key_lo / B;
       auto page_ids = [&](int j, int (&pages)[PAGES]) {  // validated ids of tile j, -1 = none
@@ -224,10 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < PAGES; ++i) cur[i] = nxt[i];
       }
-    }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 9 && lane == 0) {
+      // --------------------------------------------------------- MMA issuer
       const uint32_t sq = smem_u32(smem + kOffQ), sk = smem_u32(smem + kOffK);
       const uint32_t sv = smem_u32(smem + kOffV);
       auto issue_s = [&](int x, int j) {  // S of tile x (0 = A, 1 = B) against K tile j
@@ -279,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------- softmax: tile x, row m = TMEM lane
+    setmaxnreg_inc<kRegsSoftmax>();
     const int x = warp >> 2;
     const int m = (warp & 3) * 32 + lane;
     const int tloc = q0 + x * TP + m / G;  // position index within the chunk
@@ -315,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[c][i]);
       }
       const int key0 = j * kBN;
-      if (key0 + kBN - 1 > pos_lo) {  // some key past some row's position: mask
+      const bool masked = key0 + kBN - 1 > pos_lo;  // some key past some row's position
+      if (masked) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i) s[i] = (key0 + i <= pos) ? s[i] : -INFINITY;
       }
@@ -325,8 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 8; ++u) pm[u] = s[u];
 #pragma unroll
-        for (int i = 8; i < kBN; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
-        mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int i = 8; i < kBN; i += 2) pm[(i >> 1) & 7] = max3f(pm[(i >> 1) & 7], s[i], s[i + 1]);
+        mx = max3f(max3f(pm[0], pm[1], pm[2]), max3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       }
       const float m_new = fmaxf(m_run, mx * a.scale_log2);
       const bool rescale = m_new > m_run + 8.f;
@@ -347,21 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P (bf16 pairs) over the first 64 columns of this tile's S
-      float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nm2 = make_float2(-m_use, -m_use);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int k = c * 64 + 2 * e;
-          const float2 t = fma2(make_float2(s[k], s[k + 1]), sc2, nm2);
-          w[e] = pack2(exp2f(t.x), exp2f(t.y));
-          ls[e & 7] += bf16_lo(w[e]) + bf16_hi(w[e]);
-        }
-        tmem_st32(lane_base + s_col + c * 32, w);
-      }
-      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      probabilities(s, make_float2(a.scale_log2, a.scale_log2), make_float2(-m_use, -m_use), lane_base + s_col, acc);
+      const float2 acc2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+      const float lsum = acc2.x + acc2.y;
       if (rescale && j >= 1) {  // the previous PV of this tile is done (S of tile j followed it)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -428,6 +468,9 @@ int launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillAr
   auto kern = prefill_kernel<B, G>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return PA_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PA_ERR_CUDA;
+  if (fa.numRegs < kRegsLaunch) return PA_ERR_UNSUPPORTED;  // the register split would not fit
   kern<<<grid, kThreads, kSmem, st>>>(tk, tv, a);
   return launch_status(cudaGetLastError());
 }
