@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float2 acc2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
       const float lsum = acc2.x + acc2.y;
       if (rescale && j >= 1) {  // the previous PV of this tile is done (S of tile j followed it)
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_base + o_col + c * 32, v);
