@@ -506,9 +506,9 @@ def run_ours(args, rank, world, local_rank):
 def run_e2e(args, b, torch, dev, stream, world):
     """The same steps through the C ABI with host buffers: each step's inputs
     are packed in one pinned staging buffer and copied host->device, and its
-    outputs copied device->host, inside the timed region.  Two staging slots
-    and a copy stream let step i+1's transfers overlap step i's kernels, as a
-    serving loop would."""
+    outputs copied device->host, inside the timed region.  Two staging slots,
+    an upload stream and a download stream let step i+1's inputs and step
+    i-1's outputs move while step i's kernels run, as a serving loop would."""
     names = list(b.host_inputs)
     arrs = [np.ascontiguousarray(b.host_inputs[k]) for k in names]
     offs, pos = [], 0
@@ -532,26 +532,27 @@ def run_e2e(args, b, torch, dev, stream, world):
     probe = b.step(0, xs[0], None)
     d_out = [[torch.empty_like(t) for t in probe] for _ in range(2)]
     h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in probe] for _ in range(2)]
-    copy = torch.cuda.Stream(device=dev)
+    up = torch.cuda.Stream(device=dev)
+    down = torch.cuda.Stream(device=dev)
     h2d_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
     d2h_done = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):
         k = i & 1
-        with torch.cuda.stream(copy):
-            copy.wait_event(comp_done[k])       # slot k's inputs no longer in use (step i-2)
+        with torch.cuda.stream(up):
+            up.wait_event(comp_done[k])         # slot k's inputs no longer in use (step i-2)
             d_stage[k].copy_(h_stage, non_blocking=True)
-            h2d_done[k].record(copy)
+            h2d_done[k].record(up)
         stream.wait_event(h2d_done[k])
         stream.wait_event(d2h_done[k])          # slot k's outputs of step i-2 copied out
         b.step(i, xs[k], None, d_out[k])
         comp_done[k].record(stream)
-        with torch.cuda.stream(copy):
-            copy.wait_event(comp_done[k])
+        with torch.cuda.stream(down):
+            down.wait_event(comp_done[k])
             for hd, dd in zip(h_out[k], d_out[k]):
                 hd.copy_(dd, non_blocking=True)
-            d2h_done[k].record(copy)
+            d2h_done[k].record(down)
 
     for ev in comp_done + d2h_done:
         ev.record(stream)
@@ -573,7 +574,7 @@ def run_e2e(args, b, torch, dev, stream, world):
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
     return {"value": round(job_throughput(b.step_bytes, args.steps, world, e2e_ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps,
-            "transfers": "one pinned staging buffer H2D + outputs D2H per step, double-buffered on a copy stream"}
+            "transfers": "one pinned staging buffer H2D + outputs D2H per step, double-buffered on upload and download streams"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
