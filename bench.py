@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--plain-decode", action="store_true",
                     help="prefix_sharing: plain decode instead of the shared-prefix path")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every timed step from the host (default: replay the K steps from a CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -194,6 +196,9 @@ class Bench:
     extra: Dict = dataclasses.field(default_factory=dict)
     layers: int = 1
     pool_mb: float = 0.0
+    # launches of each timed kernel alone: name -> fn(i, inputs) (the interval
+    # between consecutive events of step); [0] is the dominant kernel
+    kernels: Dict[str, Callable] = dataclasses.field(default_factory=dict)
 
 
 def decode_bytes(ctx, Hq, Hkv, D, B):
@@ -220,17 +225,20 @@ def build_decode(args, torch, pa, dev, case):
     desc = pa.make_desc(up(case.q), kp0, torch.from_numpy(case.block_tables), scale=case.scale,
                         max_context_len=case.max_context_len)
     ws = pa.decode_workspace(desc, dev)
-    stream = torch.cuda.current_stream()
     outs = {"out": torch.empty((case.num_seqs, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device=dev)}
 
-    def step(i, x, ev, o=None):
+    def decode(i, x, out=None):
+        l = i % NL
+        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out if out is not None else outs["out"],
+                                  scale=case.scale, max_context_len=case.max_context_len, workspace=ws)
+
+    def step(i, x, ev, o=None):  # on the current stream
         l = i % NL
         out = o[0] if o else outs["out"]
-        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
-        ev and ev[0].record(stream)
-        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out, scale=case.scale,
-                                  max_context_len=case.max_context_len, workspace=ws, stream=stream)
-        ev and ev[1].record(stream)
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
+        ev and ev[0].record()
+        decode(i, x, out)
+        ev and ev[1].record()
         return [out]
 
     dec = decode_bytes(case.context_lens, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size)
@@ -241,7 +249,7 @@ def build_decode(args, torch, pa, dev, case):
                  {"q": case.q, "new_k": case.new_k, "new_v": case.new_v, "slots": case.slot_mapping,
                   "bt": case.block_tables, "ctx": case.context_lens},
                  step, dec + cache_bytes(T, case.num_kv_heads, case.head_dim), 2, "decode_kernel", "hbm", dec,
-                 case.num_seqs, layers=NL, pool_mb=case.k_pool.nbytes * 2 / 1e6)
+                 case.num_seqs, layers=NL, pool_mb=case.k_pool.nbytes * 2 / 1e6, kernels={"decode_kernel": decode})
 
 
 def prefix_sharing_setup(pa):
@@ -286,7 +294,6 @@ def build_prefix(args, torch, pa, dev):
     S, Hq, Hkv, D, B = len(ctx), plan.Hq, plan.Hkv, plan.D, plan.B
     desc = pa.make_desc(up(q), kp0, torch.from_numpy(bt), max_context_len=int(ctx.max()))
     ws = pa.decode_workspace(desc, dev)
-    stream = torch.cuda.current_stream()
     outs = {"out": torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)}
 
     npre = plan.prefix_len // B
@@ -296,20 +303,25 @@ def build_prefix(args, torch, pa, dev):
     sp_ws = torch.empty(pa._binding.load().pa_shared_prefix_workspace_bytes(pa._binding._c.byref(desc)),
                         dtype=torch.uint8, device=dev)
 
-    def step(i, x, ev, o=None):
+    def attend(i, x, out=None):
         l = i % NL
-        out = o[0] if o else outs["out"]
-        pa.copy_blocks([kps[l]], [vps[l]], x["pairs"], stream=stream)
-        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
-        ev and ev[0].record(stream)
+        out = out if out is not None else outs["out"]
         if shared:
             pa.paged_attention_decode_shared_prefix(
                 x["q"], kps[l], vps[l], x["bt"], x["ctx"], x["gs"], x["gp"], x["pt"], out, max_group_size=S,
-                max_prefix_len=plan.prefix_len, max_context_len=int(ctx.max()), workspace=sp_ws, stream=stream)
+                max_prefix_len=plan.prefix_len, max_context_len=int(ctx.max()), workspace=sp_ws)
         else:
             pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out,
-                                      max_context_len=int(ctx.max()), workspace=ws, stream=stream)
-        ev and ev[1].record(stream)
+                                      max_context_len=int(ctx.max()), workspace=ws)
+
+    def step(i, x, ev, o=None):  # on the current stream
+        l = i % NL
+        out = o[0] if o else outs["out"]
+        pa.copy_blocks([kps[l]], [vps[l]], x["pairs"])
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
+        ev and ev[0].record()
+        attend(i, x, out)
+        ev and ev[1].record()
         return [out]
 
     unique_pages = np.unique(bt[bt >= 0])
@@ -339,7 +351,8 @@ def build_prefix(args, torch, pa, dev):
                  "shared_prefix_decode" if shared else "decode_kernel", "hbm", dec_unique, S,
                  extra={"unique_pages": int(len(unique_pages)), "logical_decode_bytes": dec_logical,
                         "unique_decode_bytes": dec_unique, "cow_pairs": int(len(pairs))},
-                 layers=NL, pool_mb=kp.nbytes * 2 / 1e6)
+                 layers=NL, pool_mb=kp.nbytes * 2 / 1e6,
+                 kernels={"shared_prefix_decode" if shared else "decode_kernel": attend})
 
 
 def build_mixed(args, torch, pa, dev):
@@ -355,23 +368,31 @@ def build_mixed(args, torch, pa, dev):
     vps = [vp0] + [vp0.clone() for _ in range(NL - 1)]
     desc = pa.make_desc(up(dec.q), kp0, torch.from_numpy(dec.block_tables), max_context_len=dec.max_context_len)
     ws = pa.decode_workspace(desc, dev)
-    stream = torch.cuda.current_stream()
     T = int(m.cu_q[-1])
     outs = {"pout": torch.empty((T, 32, 128), dtype=torch.bfloat16, device=dev),
             "dout": torch.empty((dec.num_seqs, 32, 128), dtype=torch.bfloat16, device=dev)}
     max_cctx = int(m.chunk_ctx.max())
 
-    def step(i, x, ev, o=None):
+    def prefill(i, x, pout=None):
+        l = i % NL
+        pa.paged_attention_prefill_chunk(x["q_chunk"], x["cu_q"], kps[l], vps[l], x["chunk_bt"], x["chunk_ctx"],
+                                         pout if pout is not None else outs["pout"], max_q_len=512,
+                                         max_context_len=max_cctx)
+
+    def decode(i, x, dout=None):
+        l = i % NL
+        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], dout if dout is not None else outs["dout"],
+                                  max_context_len=dec.max_context_len, workspace=ws)
+
+    def step(i, x, ev, o=None):  # on the current stream
         l = i % NL
         pout, dout = o if o else (outs["pout"], outs["dout"])
-        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"], stream=stream)
-        ev and ev[0].record(stream)
-        pa.paged_attention_prefill_chunk(x["q_chunk"], x["cu_q"], kps[l], vps[l], x["chunk_bt"], x["chunk_ctx"],
-                                         pout, max_q_len=512, max_context_len=max_cctx, stream=stream)
-        ev and ev[1].record(stream)
-        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], dout,
-                                  max_context_len=dec.max_context_len, workspace=ws, stream=stream)
-        ev and ev[2].record(stream)
+        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
+        ev and ev[0].record()
+        prefill(i, x, pout)
+        ev and ev[1].record()
+        decode(i, x, dout)
+        ev and ev[2].record()
         return [pout, dout]
 
     flops = 0
@@ -393,7 +414,8 @@ def build_mixed(args, torch, pa, dev):
                   "slots": slots},
                  step, pre_bytes + dbytes + cache_bytes(Tn, 8, 128), 3, "prefill_kernel", "tensor", flops,
                  dec.num_seqs, extra={"prefill_flops": flops, "decode_bytes": dbytes, "prefill_kv_bytes": pre_bytes},
-                 layers=NL, pool_mb=dec.k_pool.nbytes * 2 / 1e6)
+                 layers=NL, pool_mb=dec.k_pool.nbytes * 2 / 1e6,
+                 kernels={"prefill_kernel": prefill, "decode_kernel": decode})
 
 
 def build(args, torch, pa, dev):
@@ -438,26 +460,74 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    e0.record(stream)
-    for i in range(args.steps):
-        b.step(i, x, evs[i])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
+    side = {}
+    if args.eager:
+        # every launch from the host, an event pair around each timed kernel
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        e0.record(stream)
+        for i in range(args.steps):
+            b.step(i, x, evs[i])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        ms = e0.elapsed_time(e1)
+        k_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+        k_mean, k_median = statistics.mean(k_ms), statistics.median(k_ms)
+        if nev == 3:
+            d_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
+            side["decode_launch_ms_mean"] = statistics.mean(d_ms)
+        timing = "eager launches, CUDA events around each timed kernel"
+    else:
+        # the K steps replayed from one CUDA graph (the launches of a serving
+        # loop); each timed kernel from a graph of its K launches alone
+        cap = torch.cuda.Stream(device=dev)
+
+        def capture(fn):
+            g = torch.cuda.CUDAGraph()
+            cap.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(args.steps):
+                    fn(i)
+            stream.wait_stream(cap)
+            return g
+
+        g_step = capture(lambda i: b.step(i, x, None))
+        g_kern = [(name, capture(lambda i, f=f: f(i, x))) for name, f in b.kernels.items()]
+        g_step.replay()  # untimed: first replay of each graph
+        for _, g in g_kern:
+            g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        e0.record(stream)
+        g_step.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        ms = e0.elapsed_time(e1)
+        per = {}
+        for name, g in g_kern:
+            k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            k0.record(stream)
+            g.replay()
+            k1.record(stream)
+            torch.cuda.synchronize()
+            per[name] = k0.elapsed_time(k1) / args.steps
+        k_mean = k_median = per[b.kernel]
+        if "decode_kernel" in per and b.kernel != "decode_kernel":
+            side["decode_launch_ms_mean"] = per["decode_kernel"]
+        timing = (f"CUDA graph of the {args.steps} steps; per-kernel launch time from a graph of the kernel's "
+                  f"{args.steps} launches alone")
+    if "decode_launch_ms_mean" in side:
+        side["decode_gbs"] = round(b.extra["decode_bytes"] / (side["decode_launch_ms_mean"] / 1e3) / 1e9, 1)
     if world > 1:
         torch.distributed.barrier()
-    ms = e0.elapsed_time(e1)
-    k_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
-    k_mean, k_median = statistics.mean(k_ms), statistics.median(k_ms)
-    side = {}
-    if nev == 3:
-        d_ms = [ev[1].elapsed_time(ev[2]) for ev in evs]
-        side["decode_launch_ms_mean"] = statistics.mean(d_ms)
-        side["decode_gbs"] = round(b.extra["decode_bytes"] / (side["decode_launch_ms_mean"] / 1e3) / 1e9, 1)
     clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
 
     e2e = None
@@ -492,6 +562,7 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": kernel_traffic(b.kernel, b.name), "algorithmic_per_launch": b.kernel_work,
                      "launch_ms_mean": k_mean, "launch_ms_median": k_median},
         "clocks": clocks,
+        "timing": timing,
     }
     res.update(side)
     if b.extra:
@@ -541,40 +612,64 @@ def run_e2e(args, b, torch, dev, stream, world):
     def e2e_step(i):
         k = i & 1
         with torch.cuda.stream(up):
-            up.wait_event(comp_done[k])         # slot k's inputs no longer in use (step i-2)
+            if i >= 2:
+                up.wait_event(comp_done[k])     # slot k's inputs no longer in use (step i-2)
             d_stage[k].copy_(h_stage, non_blocking=True)
             h2d_done[k].record(up)
-        stream.wait_event(h2d_done[k])
-        stream.wait_event(d2h_done[k])          # slot k's outputs of step i-2 copied out
+        cur = torch.cuda.current_stream()
+        cur.wait_event(h2d_done[k])
+        if i >= 2:
+            cur.wait_event(d2h_done[k])         # slot k's outputs of step i-2 copied out
         b.step(i, xs[k], None, d_out[k])
-        comp_done[k].record(stream)
+        comp_done[k].record(cur)
         with torch.cuda.stream(down):
             down.wait_event(comp_done[k])
             for hd, dd in zip(h_out[k], d_out[k]):
                 hd.copy_(dd, non_blocking=True)
             d2h_done[k].record(down)
 
-    for ev in comp_done + d2h_done:
-        ev.record(stream)
-    for i in range(args.warmup):
-        e2e_step(i)
+    def run_steps(n):
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(cur)
+        up.wait_event(start)  # the transfer streams fork from (and, in a capture, join) this stream
+        down.wait_event(start)
+        for i in range(n):
+            e2e_step(i)
+        for k in range(min(n, 2)):
+            cur.wait_event(d2h_done[k])         # every transfer joins the stream
+
+    run_steps(max(args.warmup, 2))
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for i in range(args.steps):
-        e2e_step(i)
-    stream.wait_event(d2h_done[0])
-    stream.wait_event(d2h_done[1])
-    f1.record(stream)
+    if args.eager:
+        if world > 1:
+            torch.distributed.barrier()
+        f0.record(stream)
+        run_steps(args.steps)
+        f1.record(stream)
+    else:  # the same calls captured once and replayed, as a serving loop would
+        cap = torch.cuda.Stream(device=dev)
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            run_steps(args.steps)
+        stream.wait_stream(cap)
+        g.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        f0.record(stream)
+        g.replay()
+        f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world, dev)
     h2d = int(pos)
     d2h = sum(t.numel() * t.element_size() for t in h_out[0])
     return {"value": round(job_throughput(b.step_bytes, args.steps, world, e2e_ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms / args.steps,
-            "transfers": "one pinned staging buffer H2D + outputs D2H per step, double-buffered on upload and download streams"}
+            "transfers": "one pinned staging buffer H2D + outputs D2H per step, double-buffered on upload and download streams",
+            "launch": "host launches" if args.eager else "the K steps' copies and kernels captured in one CUDA graph"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
