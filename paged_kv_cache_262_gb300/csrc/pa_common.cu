@@ -103,14 +103,15 @@ int validate_decode_desc(const pa_decode_desc *d) {
 }
 
 // Split policy.  Each CTA streams one part (part_pages pages of one
-// (sequence, kv head)); two CTAs are resident per SM.  Long parts amortise the
+// (sequence, kv head)); two CTAs (16-token pages) or three (32-token pages)
+// are resident per SM.  Long parts amortise the
 // per-CTA set-up and the split-K merge, so parts are sized for about 1.5 CTAs
 // per resident slot over the longest-context bound (never below
 // kMinPartPages pages unless the context is shorter); CTAs start longest
 // context first, which keeps the ragged tail short.  PA_PARTITION_PAGES in the
 // environment overrides the part length (tuning).
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
-  constexpr int kCtasPerSm = 2;
+  const int kCtasPerSm = d->block_size == 16 ? 2 : 3;  // resident decode CTAs per SM (shared memory)
   constexpr int kMinPartPages = 32;
   DecodePlan p;
   const int B = d->block_size;

@@ -550,8 +550,11 @@ unsigned int next_epoch() {
 template <int D, int B, int NT>
 int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                   cudaStream_t st) {
+  // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM); 32-token pages:
+  // 1 slot a warp (64 KB, 3 CTAs per SM) -- with 2 slots a CTA would hold
+  // 128 KB and one CTA per SM could not hide its own set-up and merge.
   constexpr int NW = 4;
-  constexpr int NST = (B == 16) ? 3 : 2;
+  constexpr int NST = (B == 16) ? 3 : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
   auto kern = decode_kernel<D, B, NT, NW, NST>;
