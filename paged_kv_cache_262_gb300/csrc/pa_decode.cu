@@ -362,6 +362,21 @@ __global__ void __launch_bounds__(NW * 32)
         }
       }
 
+      // Value rows past the context (the tail of the last page) may hold
+      // anything a slot was never written with, NaN included, and 0 * NaN
+      // would reach the output: clear them before the product.
+      if (tok0 + B > ctx) {
+        uint8_t *vslot = ring + stg * L::kSlotBytes + L::kPageBytes;
+        const int r0 = ctx - tok0;
+        for (int idx = lane; idx < (B - r0) * L::kHalves * 8; idx += 32) {
+          const int row = r0 + idx / (L::kHalves * 8), rem = idx % (L::kHalves * 8);
+          *reinterpret_cast<uint4 *>(vslot + (rem >> 3) * L::kBoxBytes + row * 128 + (rem & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // the slot is refilled by TMA afterwards
+        __syncwarp();
+      }
+
       // O^T[d][head] += V^T P^T, one 16-token k-tile at a time
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
