@@ -45,6 +45,14 @@
  *    or-ed into *err_flag (device int32, may be NULL) as PA_DEVERR_* bits; the
  *    offending work is skipped (attention rows are written as zeros), nothing
  *    traps.  The flag is never cleared by the library.
+ *  - Attention reads slot j of a sequence only for j < its context length:
+ *    slots past a context (the tail of its last block, blocks no table uses)
+ *    may hold any bits, NaN included, without reaching the output.
+ *  - Every GPU call may be captured into a CUDA graph (stream capture): a
+ *    replay re-runs it with the arguments, launch plan and tensor maps bound
+ *    at capture.  Split-K decode resets its arrival counters itself, so
+ *    replays need no workspace clearing; the allocation-free decode wants its
+ *    first call outside a capture (see below).
  *  - Thread safety: calls are re-entrant; the only global state is a
  *    per-device cache of SM count and of the driver's tensor-map encoder.
  */
