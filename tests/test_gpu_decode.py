@@ -98,9 +98,15 @@ CTX = [1, 2, 15, 16, 17, 31, 32, 33, 100, 257, 513, 1000, 1999]
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "q%dkv%dd%db%d" % s)
 @pytest.mark.parametrize("pp", [None, 1, 3])
-def test_ragged_shapes(torch, ora, parts, shape, pp):
+@pytest.mark.parametrize("lpt", [None, "1", "0"])
+def test_ragged_shapes(torch, ora, parts, monkeypatch, shape, pp, lpt):
+    """Every CTA order: the launcher's choice, longest context first, grid order."""
     Hq, Hkv, D, B = shape
     parts(pp)
+    if lpt is None:
+        monkeypatch.delenv("PA_DECODE_LPT", raising=False)
+    else:
+        monkeypatch.setenv("PA_DECODE_LPT", lpt)
     case = wl.make_decode_case("ragged", CTX, Hq, Hkv, D, B, seed=7, stream=hash(shape) % 1000,
                                scale=1.0 / math.sqrt(D), with_new_tokens=False)
     d = upload_case(case, torch)
@@ -108,7 +114,7 @@ def test_ragged_shapes(torch, ora, parts, shape, pp):
     out = run_step(torch, case, d, err)
     ref, st = ora.decode_case(case)
     assert int(err.item()) == 0 and np.all(st == 0)
-    assert_close(bf16_host(out), ref, f"{shape} pp={pp}")
+    assert_close(bf16_host(out), ref, f"{shape} pp={pp} lpt={lpt}")
 
 
 def _relaid(case, seed):
