@@ -68,20 +68,6 @@ bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-bool encode_3d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[3],
-                    const uint64_t strides_bytes[2], const uint32_t box[3]) {
-  EncodeTiledFn fn = encoder();
-  if (!fn) return false;
-  cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
-  cuuint64_t s[2] = {strides_bytes[0], strides_bytes[1]};
-  cuuint32_t b[3] = {box[0], box[1], box[2]};
-  cuuint32_t e[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), d, s, b, e,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 int validate_decode_desc(const pa_decode_desc *d) {
   if (!d) return PA_ERR_INVALID;
   if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_blocks <= 0 ||

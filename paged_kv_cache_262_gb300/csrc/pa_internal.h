@@ -19,10 +19,6 @@ int current_sm_count();
 bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows, uint32_t box_cols, bool swizzle128);
 
-// Encodes a 3-D bf16 tensor map (dims innermost first) with 128-byte swizzle.
-bool encode_3d_bf16(CUtensorMap *map, const void *base, const uint64_t dims[3],
-                    const uint64_t strides_bytes[2], const uint32_t box[3]);
-
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline int launch_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }

@@ -420,4 +420,20 @@ def pin_errors(ora):
     assert np.array_equal(kp2, kp) and np.array_equal(vp2, vp)
 
 
+def pin_bf16_decoding(ora):
+    """The oracle widens bf16 inputs exactly: a bf16 value is the float32
+    whose upper 16 bits are its bits (sign, 8-bit exponent, 7-bit mantissa)."""
+    cases = {0x0000: 0.0, 0x8000: -0.0, 0x3F80: 1.0, 0xBF80: -1.0, 0x4049: 3.140625, 0x3F81: 1.0078125,
+             0x0001: 2.0 ** -133, 0x0080: 2.0 ** -126, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127,
+             0x7F80: math.inf, 0xFF80: -math.inf}
+    for bits, want in cases.items():
+        got = ora.bf16_to_f64(bits)
+        assert got == want and math.copysign(1.0, got) == math.copysign(1.0, want), (hex(bits), got, want)
+    assert math.isnan(ora.bf16_to_f64(0x7FC0))
+    st = wl.Stream(5, 5)
+    bits = st.integers(0, 0x7F80, 200).astype(np.uint16)  # finite positives
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert all(ora.bf16_to_f64(int(b)) == r for b, r in zip(bits, ref))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
