@@ -42,9 +42,13 @@
  *    passed as void*, NULL = legacy default stream).  The return value reports
  *    host-side validation and launch errors only.
  *  - Errors found on the device (bad context length, page or slot id) are
- *    or-ed into *err_flag (device int32, may be NULL) as PA_DEVERR_* bits; the
- *    offending work is skipped (attention rows are written as zeros), nothing
- *    traps.  The flag is never cleared by the library.
+ *    or-ed into *err_flag (device int32, may be NULL) as PA_DEVERR_* bits and
+ *    nothing traps.  Attention rows of a sequence or chunk with a bad context
+ *    length are written as zeros; a block-table entry outside the pool is not
+ *    read (its keys are left out by decode; a prefill tile holding it computes
+ *    on whatever shared memory held), so rows that need it are unspecified;
+ *    a bad slot or copy pair writes nothing.  The flag is never cleared by the
+ *    library.
  *  - Attention reads slot j of a sequence only for j < its context length:
  *    slots past a context (the tail of its last block, blocks no table uses)
  *    may hold any bits, NaN included, without reaching the output.
