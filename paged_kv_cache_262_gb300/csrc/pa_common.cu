@@ -90,10 +90,10 @@ int validate_decode_desc(const pa_decode_desc *d) {
 
 // Split policy.  Each CTA streams one part (part_pages pages of one
 // (sequence, kv head)); two CTAs (16-token pages) or three (32-token pages)
-// are resident per SM.  Long parts amortise the
-// per-CTA set-up and the split-K merge, so parts are sized for about 1.5 CTAs
-// per resident slot over the longest-context bound (never below
-// kMinPartPages pages unless the context is shorter); CTAs start longest
+// are resident per SM.  Long parts amortise the per-CTA set-up and the
+// split-K merge, so parts are sized for about 1.5 CTAs per resident slot over
+// the longest-context bound (never below kMinPartPages pages unless the
+// context is shorter); when the grid fills a few waves the CTAs start longest
 // context first, which keeps the ragged tail short.  PA_PARTITION_PAGES in the
 // environment overrides the part length (tuning).
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {

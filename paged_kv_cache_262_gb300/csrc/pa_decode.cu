@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(NW * 32)
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
 
   // CTAs are dispatched in linear order; map that order to (sequence rank,
-  // part, kv head) so that the longest contexts start first.
+  // part, kv head), ranks longest context first when a.lpt is set.
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
   const int per_seq = a.max_parts * a.Hkv;
   const int rank = lin / per_seq;
