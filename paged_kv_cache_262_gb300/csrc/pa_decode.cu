@@ -452,6 +452,48 @@ __global__ void __launch_bounds__(NW * 32)
 
   const bool split = nparts > 1;
   const size_t unit = (size_t)s * a.Hkv + kvh;
+  // Whole context in one CTA with a shared prefix before it: per query head,
+  // the weight of this CTA's (unnormalised) sum and of each prefix state,
+  // both divided by the total weight -- computed once per head, so that every
+  // output element only adds up its prefix states (loads issued together).
+  const int npre = (!split && has_pre) ? a.npre : 0;
+  float *coef = wts;  // [0..15] this CTA's sum, [16 (p + 1) + g] prefix state p
+  const size_t slab = (size_t)a.S * a.Hq;
+  if (npre > 0) {
+    if (tid < G) {
+      const int g = tid;
+      const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
+      float mx = -INFINITY, l = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) mx = fmaxf(mx, red_m[w * 16 + g]);
+      if (mx != -INFINITY) {
+#pragma unroll
+        for (int w = 0; w < NW; ++w) l += red_l[w * 16 + g] * exp2f(red_m[w * 16 + g] - mx);
+      }
+      float mp[kMaxPrefixParts], lp[kMaxPrefixParts];
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p) {
+        mp[p] = p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row)) : -INFINITY;
+        lp[p] = p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row) + 1) : 0.f;
+      }
+      float M = l > 0.f ? mx : -INFINITY;
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p)
+        if (lp[p] > 0.f) M = fmaxf(M, mp[p]);
+      const float c = l > 0.f ? exp2f(mx - M) : 0.f;  // on the sum, whose normaliser is l
+      float den = c * l;
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p) {
+        lp[p] = lp[p] > 0.f ? lp[p] * exp2f(mp[p] - M) : 0.f;
+        den += lp[p];
+      }
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      coef[g] = c * inv;
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p) coef[16 * (p + 1) + g] = lp[p] * inv;
+    }
+    __syncthreads();
+  }
   for (int idx = tid; idx < G * D; idx += NW * 32) {
     const int g = idx / D, d = idx - g * D;
     float mx = -INFINITY;
@@ -466,32 +508,23 @@ __global__ void __launch_bounds__(NW * 32)
         acc += red_o[(w * 16 + g) * D + d] * f;
       }
     }
-    const float val = l > 0.f ? acc / l : 0.f;
     if (!split) {
-      float res = val;
-      if (has_pre) {  // fold in the shared prefix's partial states
+      float res;
+      if (npre > 0) {  // fold in the shared prefix's partial states
         const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
-        const size_t slab = (size_t)a.S * a.Hq;
-        float M = l > 0.f ? mx : -INFINITY;
-        for (int p = 0; p < a.npre; ++p) {
-          const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
-          if (lp > 0.f) M = fmaxf(M, __ldg(a.pre_ml + 2 * (p * slab + row)));
-        }
-        float w = l > 0.f ? l * exp2f(mx - M) : 0.f;
-        float num = w * val, den = w;
-        for (int p = 0; p < a.npre; ++p) {
-          const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
-          if (!(lp > 0.f)) continue;
-          const float wp = lp * exp2f(__ldg(a.pre_ml + 2 * (p * slab + row)) - M);
-          num += wp * __ldg(a.pre_o + (p * slab + row) * D + d);
-          den += wp;
-        }
-        res = den > 0.f ? num / den : 0.f;
+        float po[kMaxPrefixParts];
+#pragma unroll
+        for (int p = 0; p < kMaxPrefixParts; ++p) po[p] = p < npre ? __ldg(a.pre_o + (p * slab + row) * D + d) : 0.f;
+        res = coef[g] * acc;
+#pragma unroll
+        for (int p = 0; p < kMaxPrefixParts; ++p) res += coef[16 * (p + 1) + g] * po[p];
+      } else {
+        res = l > 0.f ? acc / l : 0.f;
       }
       out_base[idx] = __float2bfloat16(res);
     } else {
       const size_t u = (unit * a.max_parts + part) * G + g;
-      a.ws_o[u * D + d] = val;
+      a.ws_o[u * D + d] = l > 0.f ? acc / l : 0.f;
       if (d == 0) {
         a.ws_ml[2 * u] = mx;
         a.ws_ml[2 * u + 1] = l;
@@ -509,7 +542,6 @@ __global__ void __launch_bounds__(NW * 32)
   __threadfence();
   const size_t ubase = unit * a.max_parts;
   float *wpre = reinterpret_cast<float *>(misc + 8);  // [npre][16] prefix weights (histogram area, free now)
-  const size_t slab = (size_t)a.S * a.Hq;
   if (tid < G) {
     const int g = tid;
     const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
