@@ -172,7 +172,7 @@ __device__ int seq_of_rank(int r, const int32_t *ctx, int S, int B, int max_bloc
   return misc[2];
 }
 
-template <int D, int B, int NT, int NW, int NST>
+template <int D, int B, int NT, int NW, int NST, bool PRE>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
@@ -281,6 +281,33 @@ __global__ void __launch_bounds__(NW * 32)
       } else {
         qf[nt][kk][0] = qf[nt][kk][1] = 0u;
       }
+    }
+  }
+
+  // A whole context in one CTA after a shared prefix folds the prefix's
+  // partial states in at the end: load them now, so that their latency hides
+  // under the streaming (thread tid: output elements tid + j NW 32, and the
+  // (m, l) of head tid), when a thread's share is small enough for registers.
+  constexpr int kPreElems = 4;
+  const int npre = (has_pre && nparts == 1) ? a.npre : 0;
+  // (PRE: the shared-prefix launch; groups of more than 8 heads never qualify)
+  const bool pre_early = PRE && NT == 1 && npre > 0 && G * D <= kPreElems * NW * 32;
+  const size_t slab = (size_t)a.S * a.Hq;
+  float pre_o_r[kPreElems][kMaxPrefixParts], pre_m_r[kMaxPrefixParts], pre_l_r[kMaxPrefixParts];
+  if (pre_early) {
+#pragma unroll
+    for (int j = 0; j < kPreElems; ++j) {
+      const int idx = tid + j * NW * 32;
+      const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + idx / D;
+#pragma unroll
+      for (int p = 0; p < kMaxPrefixParts; ++p)
+        pre_o_r[j][p] = (idx < G * D && p < npre) ? __ldg(a.pre_o + (p * slab + row) * D + idx % D) : 0.f;
+    }
+    const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + tid;
+#pragma unroll
+    for (int p = 0; p < kMaxPrefixParts; ++p) {
+      pre_m_r[p] = (tid < G && p < npre) ? __ldg(a.pre_ml + 2 * (p * slab + row)) : -INFINITY;
+      pre_l_r[p] = (tid < G && p < npre) ? __ldg(a.pre_ml + 2 * (p * slab + row) + 1) : 0.f;
     }
   }
 
@@ -456,9 +483,7 @@ __global__ void __launch_bounds__(NW * 32)
   // the weight of this CTA's (unnormalised) sum and of each prefix state,
   // both divided by the total weight -- computed once per head, so that every
   // output element only adds up its prefix states (loads issued together).
-  const int npre = (!split && has_pre) ? a.npre : 0;
   float *coef = wts;  // [0..15] this CTA's sum, [16 (p + 1) + g] prefix state p
-  const size_t slab = (size_t)a.S * a.Hq;
   if (npre > 0) {
     if (tid < G) {
       const int g = tid;
@@ -473,8 +498,8 @@ __global__ void __launch_bounds__(NW * 32)
       float mp[kMaxPrefixParts], lp[kMaxPrefixParts];
 #pragma unroll
       for (int p = 0; p < kMaxPrefixParts; ++p) {
-        mp[p] = p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row)) : -INFINITY;
-        lp[p] = p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row) + 1) : 0.f;
+        mp[p] = pre_early ? pre_m_r[p] : p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row)) : -INFINITY;
+        lp[p] = pre_early ? pre_l_r[p] : p < npre ? __ldg(a.pre_ml + 2 * (p * slab + row) + 1) : 0.f;
       }
       float M = l > 0.f ? mx : -INFINITY;
 #pragma unroll
@@ -494,7 +519,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
     __syncthreads();
   }
-  for (int idx = tid; idx < G * D; idx += NW * 32) {
+  for (int idx = tid, j = 0; idx < G * D; idx += NW * 32, ++j) {
     const int g = idx / D, d = idx - g * D;
     float mx = -INFINITY;
 #pragma unroll
@@ -513,8 +538,16 @@ __global__ void __launch_bounds__(NW * 32)
       if (npre > 0) {  // fold in the shared prefix's partial states
         const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
         float po[kMaxPrefixParts];
+        if (pre_early) {
 #pragma unroll
-        for (int p = 0; p < kMaxPrefixParts; ++p) po[p] = p < npre ? __ldg(a.pre_o + (p * slab + row) * D + d) : 0.f;
+          for (int jj = 0; jj < kPreElems; ++jj)
+            if (jj == j)
+#pragma unroll
+              for (int p = 0; p < kMaxPrefixParts; ++p) po[p] = pre_o_r[jj][p];
+        } else {
+#pragma unroll
+          for (int p = 0; p < kMaxPrefixParts; ++p) po[p] = p < npre ? __ldg(a.pre_o + (p * slab + row) * D + d) : 0.f;
+        }
         res = coef[g] * acc;
 #pragma unroll
         for (int p = 0; p < kMaxPrefixParts; ++p) res += coef[16 * (p + 1) + g] * po[p];
@@ -596,7 +629,7 @@ unsigned int next_epoch() {
   return e;
 }
 
-template <int D, int B, int NT>
+template <int D, int B, int NT, bool PRE>
 int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                   cudaStream_t st) {
   // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM); 32-token pages:
@@ -606,7 +639,7 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
   constexpr int NST = (B == 16) ? 3 : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
-  auto kern = decode_kernel<D, B, NT, NW, NST>;
+  auto kern = decode_kernel<D, B, NT, NW, NST, PRE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   kern<<<grid, NW * 32, L::kAlloc, st>>>(tk, tv, a);
@@ -616,7 +649,9 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
 template <int D, int B>
 int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                 cudaStream_t st) {
-  return G <= 8 ? launch_decode<D, B, 1>(tk, tv, a, grid, st) : launch_decode<D, B, 2>(tk, tv, a, grid, st);
+  if (a.ngroups > 0)  // shared-prefix launch: prefix states prefetched (more registers)
+    return G <= 8 ? launch_decode<D, B, 1, true>(tk, tv, a, grid, st) : launch_decode<D, B, 2, true>(tk, tv, a, grid, st);
+  return G <= 8 ? launch_decode<D, B, 1, false>(tk, tv, a, grid, st) : launch_decode<D, B, 2, false>(tk, tv, a, grid, st);
 }
 
 }  // namespace
