@@ -280,3 +280,114 @@ def test_prefix_cache_never_hands_out_a_block_twice():
     assert sorted(t) == list(range(6))
     with pytest.raises(pa.PaError):
         bm.add_seq(2, 1)
+
+
+def test_model_based_contents_through_cow_swap_and_prefix_cache():
+    """Random prompts (some repeating earlier prompts' leading blocks), forks,
+    appends, frees, swap-outs and swap-ins against simulated device and host
+    page pools.  The test plays the caller: it writes each new token into the
+    slot the manager gives, applies every copy-on-write pair and every swap
+    pair to the simulated pools, and after each operation reads every resident
+    sequence back through its block table: the tokens must be exactly the
+    sequence's own, and each block's reference count must equal the number of
+    resident tables holding it."""
+    B, N, H = 8, 64, 24
+    bm = pa.BlockManager(N, B, num_host_blocks=H)
+    dev = np.full((N, B), -1, np.int64)
+    host = np.full((H, B), -1, np.int64)
+    model, swapped = {}, set()
+    st = wl.Stream(77, 3)
+    u = st.uniform(3000)
+    fresh = iter(range(10 ** 6, 10 ** 7))
+    prompts = []
+    nxt = 0
+
+    def write(s, start):
+        t = bm.block_table(s)
+        for j in range(start, len(model[s])):
+            dev[t[j // B], j % B] = model[s][j]
+
+    def check_all():
+        refs = np.zeros(N, int)
+        for s, toks in model.items():
+            if s in swapped:
+                continue
+            t = bm.block_table(s)
+            assert len(t) == (len(toks) + B - 1) // B and bm.seq_len(s) == len(toks)
+            assert [int(dev[t[j // B], j % B]) for j in range(len(toks))] == toks, f"seq {s}"
+            for b in t:
+                refs[b] += 1
+        assert all(bm.ref_count(b) == refs[b] for b in range(N))
+
+    def pick(pred=lambda s: True):
+        c = [s for s in model if pred(s)]
+        return c[int(u[k] * 1e7) % len(c)] if c else None
+
+    for k in range(3000):
+        op = u[(k * 7919) % 3000]
+        try:
+            if op < 0.2 or not model:
+                if prompts and op < 0.12:  # repeat some full blocks of an earlier prompt
+                    base = prompts[int(u[k] * 1e6) % len(prompts)]
+                    keep = (int(u[k] * 1e8) % (len(base) // B + 1)) * B
+                    toks = base[:keep] + [next(fresh) for _ in range(int(u[k] * 1e5) % 20)]
+                else:
+                    toks = [next(fresh) for _ in range(1 + int(u[k] * 1e5) % 40)]
+                if not toks:
+                    toks = [next(fresh)]
+                c = bm.add_seq_tokens(nxt, toks)
+                assert c % B == 0 and 0 <= c <= len(toks)
+                model[nxt] = list(toks)
+                t = bm.block_table(nxt)
+                assert [int(dev[t[j // B], j % B]) for j in range(c)] == toks[:c]  # cached blocks hold the prompt
+                write(nxt, c)
+                prompts.append(list(toks))
+                nxt += 1
+            elif op < 0.27:
+                p = pick(lambda s: s not in swapped)
+                if p is not None:
+                    bm.fork(p, nxt)
+                    model[nxt] = list(model[p])
+                    nxt += 1
+            elif op < 0.6:
+                s = pick(lambda s: s not in swapped)
+                if s is not None:
+                    tok = next(fresh)
+                    slot, cow = bm.append(s)
+                    if cow is not None:
+                        dev[cow[1]] = dev[cow[0]]
+                    dev[slot // B, slot % B] = tok
+                    model[s].append(tok)
+            elif op < 0.78:
+                s = pick()
+                if s is not None:
+                    bm.free_seq(s)
+                    del model[s]
+                    swapped.discard(s)
+            elif op < 0.89:
+                s = pick(lambda s: s not in swapped)
+                if s is not None:
+                    before = bm.block_table(s)
+                    try:
+                        pairs = bm.swap_out(s)
+                    except pa.PaError as e:
+                        assert e.status in (pa.PA_ERR_STATE, pa.PA_ERR_OOM)
+                        assert bm.block_table(s) == before
+                    else:
+                        assert [d for d, _ in pairs] == before
+                        for d, h in pairs:
+                            host[h] = dev[d]
+                        swapped.add(s)
+            else:
+                s = pick(lambda s: s in swapped)
+                if s is not None:
+                    pairs = bm.swap_in(s)
+                    for h, d in pairs:
+                        dev[d] = host[h]
+                    swapped.discard(s)
+        except pa.PaError as e:
+            assert e.status == pa.PA_ERR_OOM
+        check_all()
+    for s in list(model):
+        bm.free_seq(s)
+    assert bm.num_free() == N and bm.num_free_host() == H
