@@ -128,7 +128,7 @@ __device__ __forceinline__ void probabilities(const float (&s)[kBN], float2 sc2,
   }
 }
 
-template <int B, int G>
+template <int B, int G, bool PARTIAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const PrefillArgs a) {
@@ -422,20 +422,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (wait(BAR_O_DONE, 0)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      const size_t row = (size_t)(c0 + tloc) * a.Hq + head;
+      if constexpr (PARTIAL) {
+        // Partial states (fp32, 512-byte rows): the warp stages its 32 rows in
+        // shared memory (free now: every MMA is done), 16-byte chunks
+        // XOR-swizzled by row, then writes whole rows per instruction.
+        uint8_t *stage = smem + warp * (32 * 512);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(lane_base + o_col + c * 32, v);
-        tmem_wait_ld();
-        if (!row_valid) continue;
-        if (part_o) {
-          float4 *dst = reinterpret_cast<float4 *>(part_o + row * kD);
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + o_col + c * 32, v);
+          tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            dst[c * 8 + i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                                         __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
-        } else {
+            *reinterpret_cast<float4 *>(stage + lane * 512 + (((c * 8 + i) ^ lane) & 31) * 16) =
+                make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
+                            __uint_as_float(v[4 * i + 2]) * inv, __uint_as_float(v[4 * i + 3]) * inv);
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int r = 0; r < 32; ++r) {
+          const int mr = (warp & 3) * 32 + r;
+          const int t = q0 + x * TP + mr / G;
+          if (t >= C) continue;
+          const size_t orow = (size_t)(c0 + t) * a.Hq + g * G + mr % G;
+          reinterpret_cast<uint4 *>(part_o + orow * kD)[lane] =
+              *reinterpret_cast<const uint4 *>(stage + r * 512 + ((lane ^ r) & 31) * 16);
+        }
+      } else {
+        const size_t row = (size_t)(c0 + tloc) * a.Hq + head;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + o_col + c * 32, v);
+          tmem_wait_ld();
+          if (!row_valid) continue;
           uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kD);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -448,9 +468,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_valid && part_o) {
-        part_ml[2 * row] = m_run;
-        part_ml[2 * row + 1] = l_run;
+      if constexpr (PARTIAL) {
+        if (row_valid) {
+          const size_t row = (size_t)(c0 + tloc) * a.Hq + head;
+          part_ml[2 * row] = m_run;
+          part_ml[2 * row + 1] = l_run;
+        }
       }
     }
   }
@@ -465,7 +488,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int B, int G>
 int launch_prefill(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &a, dim3 grid,
                    cudaStream_t st) {
-  auto kern = prefill_kernel<B, G>;
+  // partial states (the shared-prefix pass) or bf16 rows: separate kernels,
+  // so that each keeps its own register allocation
+  auto kern = a.part_o ? prefill_kernel<B, G, true> : prefill_kernel<B, G, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
     return PA_ERR_CUDA;
   cudaFuncAttributes fa;
