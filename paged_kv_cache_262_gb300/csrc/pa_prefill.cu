@@ -336,13 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = (row_valid && a.causal) ? ctx - C + tloc : ctx - 1;
     const int pos_lo = a.causal ? ctx - C + q0 + x * TP : ctx - 1;  // first position of this tile
     const int head = g * G + m % G;
-    {  // Q row -> shared memory (128-byte swizzle, two 64-column halves)
+    {  // the tile's Q rows -> shared memory (128-byte swizzle, two 64-column
+       // halves); a warp loads two whole rows per instruction (16-byte chunk
+       // per lane), rows past the chunk as zeros
       uint8_t *qd = smem + kOffQ + x * kTile;
-      const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((size_t)(c0 + tloc) * a.Hq + head) * kD);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 v = row_valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4 *>(qd + (c >> 3) * kHalf + sw128(m, c & 7)) = v;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int k = i * 128 + m, mr = k >> 4, c = k & 15;  // row and chunk of the tile
+        const int t = q0 + x * TP + mr / G;
+        const uint4 v = t < C ? __ldg(reinterpret_cast<const uint4 *>(
+                                    a.q + ((size_t)(c0 + t) * a.Hq + g * G + mr % G) * kD) + c)
+                              : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(qd + (c >> 3) * kHalf + sw128(mr, c & 7)) = v;
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[BAR_Q]);
