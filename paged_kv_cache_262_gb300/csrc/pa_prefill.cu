@@ -454,14 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<const uint4 *>(stage + r * 512 + ((lane ^ r) & 31) * 16);
         }
       } else {
-        const size_t row = (size_t)(c0 + tloc) * a.Hq + head;
+        uint8_t *stage = smem + warp * (32 * 256);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
           tmem_ld32(lane_base + o_col + c * 32, v);
           tmem_wait_ld();
-          if (!row_valid) continue;
-          uint4 *dst = reinterpret_cast<uint4 *>(a.out + row * kD);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             uint4 o;
@@ -469,8 +467,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.y = pack2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
             o.z = pack2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
             o.w = pack2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
-            dst[c * 4 + i] = o;
+            *reinterpret_cast<uint4 *>(stage + lane * 256 + (((c * 4 + i) ^ lane) & 15) * 16) = o;
           }
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int r0 = 0; r0 < 32; r0 += 2) {
+          const int r = r0 + (lane >> 4), ch = lane & 15;
+          const int mr = (warp & 3) * 32 + r;
+          const int t = q0 + x * TP + mr / G;
+          if (t >= C) continue;
+          const size_t orow = (size_t)(c0 + t) * a.Hq + g * G + mr % G;
+          reinterpret_cast<uint4 *>(a.out + orow * kD)[ch] =
+              *reinterpret_cast<const uint4 *>(stage + r * 256 + ((ch ^ r) & 15) * 16);
         }
       }
       if constexpr (PARTIAL) {
