@@ -67,6 +67,7 @@ def parse():
     ap.add_argument("--workload", default="llama8b_decode", choices=WORKLOADS)
     ap.add_argument("--chunks", type=int, default=16, help="mixed_step: prefill chunks")
     ap.add_argument("--decodes", type=int, default=240, help="mixed_step: decode sequences")
+    ap.add_argument("--block-size", type=int, default=32, choices=[16, 32], help="mixed_step: tokens per page")
     ap.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0 = auto, > 4x L2)")
     ap.add_argument("--plain-decode", action="store_true",
                     help="prefix_sharing: plain decode instead of the shared-prefix path")
@@ -360,7 +361,8 @@ def build_mixed(args, torch, pa, dev):
     st = wl.Stream(0, 6)
     cctx = st.integers(512, 8192, 16)[: args.chunks]
     dctx = st.integers(64, 4096, 240)[: args.decodes]
-    m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, 32, seed=0, stream=105)
+    B = args.block_size
+    m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, B, seed=0, stream=105)
     dec = m.decode
     up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
     NL = n_layers(args, dec.k_pool.nbytes * 2)
@@ -402,13 +404,13 @@ def build_mixed(args, torch, pa, dev):
         pos = np.arange(c - 512, c, dtype=np.int64)
         flops += 4 * 128 * 32 * int((pos + 1).sum())
     pre_bytes = int(np.asarray(cctx, np.int64).sum()) * 8 * 128 * 4 + 2 * T * 32 * 128 * 2
-    dbytes = decode_bytes(dec.context_lens, 32, 8, 128, 32)
+    dbytes = decode_bytes(dec.context_lens, 32, 8, 128, B)
     Tn = T + dec.num_seqs
     new_k = np.concatenate([m.chunk_new_k, dec.new_k])
     new_v = np.concatenate([m.chunk_new_v, dec.new_v])
     slots = np.concatenate([m.chunk_slots, dec.slot_mapping])
     return Bench("mixed_step", f"mixed_step: {len(cctx)} prefill chunks x 512 tokens (ctx {int(cctx.min())}..{int(cctx.max())})"
-                 f" + {dec.num_seqs} decodes (ctx {int(dctx.min())}..{int(dctx.max())}), 32q/8kv, D=128, B=32; "
+                 f" + {dec.num_seqs} decodes (ctx {int(dctx.min())}..{int(dctx.max())}), 32q/8kv, D=128, B={B}; "
                  f"reshape_and_cache of {Tn} tokens + prefill + decode",
                  {"q_chunk": m.q_chunk, "cu_q": m.cu_q, "chunk_bt": m.chunk_tables, "chunk_ctx": m.chunk_ctx,
                   "q": dec.q, "bt": dec.block_tables, "ctx": dec.context_lens, "new_k": new_k, "new_v": new_v,
@@ -685,7 +687,8 @@ def oracle_units(args):
         st = wl.Stream(0, 6)
         cctx = st.integers(512, 8192, 16)[: args.chunks]
         dctx = st.integers(64, 4096, 240)[: args.decodes]
-        m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, 32, seed=0, stream=105)
+        m = wl.make_mixed_step("mixed_step", [512] * len(cctx), cctx, dctx, 32, 8, 128, args.block_size, seed=0,
+                               stream=105)
         kp, vp = m.decode.k_pool.copy(), m.decode.v_pool.copy()
         ora.reshape_and_cache(m.chunk_new_k, m.chunk_new_v, kp, vp, m.chunk_slots)
         for r in range(len(cctx)):
