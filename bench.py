@@ -5,7 +5,9 @@ seeded generator in ``workloads``:
 
 * decode workloads (default ``llama8b_decode``: 64 seqs, ctx ~U[128,2048],
   32q/8kv heads, D=128, B=16; also ``long_context_decode``, ``tiny_decode``):
-  reshape_and_cache of the step's new tokens, then paged decode attention;
+  each sequence's new token stored in the cache and paged decode attention, in
+  one decode-with-append launch (``--separate-append``: reshape_and_cache,
+  then decode);
 * ``prefix_sharing``: 64 prompts x 4 samples over a 2048-token prefix built by
   the host block manager; copy_blocks of the copy-on-write pairs,
   reshape_and_cache of the appended tokens, decode over the shared tables;
@@ -68,6 +70,9 @@ def parse():
     ap.add_argument("--chunks", type=int, default=16, help="mixed_step: prefill chunks")
     ap.add_argument("--decodes", type=int, default=240, help="mixed_step: decode sequences")
     ap.add_argument("--block-size", type=int, default=32, choices=[16, 32], help="mixed_step: tokens per page")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="decode workloads: reshape_and_cache and decode as two launches instead of one "
+                         "decode-with-append launch")
     ap.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0 = auto, > 4x L2)")
     ap.add_argument("--plain-decode", action="store_true",
                     help="prefix_sharing: plain decode instead of the shared-prefix path")
@@ -229,15 +234,24 @@ def build_decode(args, torch, pa, dev, case):
     ws = pa.decode_workspace(desc, dev)
     outs = {"out": torch.empty((case.num_seqs, case.num_q_heads, case.head_dim), dtype=torch.bfloat16, device=dev)}
 
+    fused = not args.separate_append  # each sequence's new token written by the decode launch itself
+
     def decode(i, x, out=None):
         l = i % NL
-        pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out if out is not None else outs["out"],
-                                  scale=case.scale, max_context_len=case.max_context_len, workspace=ws)
+        out = out if out is not None else outs["out"]
+        if fused:
+            pa.paged_attention_decode_append(x["q"], x["new_k"], x["new_v"], x["slots"], kps[l], vps[l], x["bt"],
+                                             x["ctx"], out, scale=case.scale, max_context_len=case.max_context_len,
+                                             workspace=ws)
+        else:
+            pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out, scale=case.scale,
+                                      max_context_len=case.max_context_len, workspace=ws)
 
     def step(i, x, ev, o=None):  # on the current stream
         l = i % NL
         out = o[0] if o else outs["out"]
-        pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
+        if not fused:
+            pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
         ev and ev[0].record()
         decode(i, x, out)
         ev and ev[1].record()
@@ -245,12 +259,15 @@ def build_decode(args, torch, pa, dev, case):
 
     dec = decode_bytes(case.context_lens, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size)
     T = len(case.slot_mapping)
+    cache = cache_bytes(T, case.num_kv_heads, case.head_dim)
+    what = (f"decode with append of {T} tokens (one launch)" if fused
+            else f"reshape_and_cache of {T} tokens + decode")
     return Bench(case.name, f"{case.name}: {case.num_seqs} seqs, ctx {int(case.context_lens.min())}.."
                  f"{int(case.context_lens.max())} (mean {case.context_lens.mean():.0f}), {case.num_q_heads}q/"
-                 f"{case.num_kv_heads}kv heads, D={case.head_dim}, B={case.block_size}, reshape_and_cache of {T} tokens",
+                 f"{case.num_kv_heads}kv heads, D={case.head_dim}, B={case.block_size}, {what}",
                  {"q": case.q, "new_k": case.new_k, "new_v": case.new_v, "slots": case.slot_mapping,
                   "bt": case.block_tables, "ctx": case.context_lens},
-                 step, dec + cache_bytes(T, case.num_kv_heads, case.head_dim), 2, "decode_kernel", "hbm", dec,
+                 step, dec + cache, 1 if fused else 2, "decode_kernel", "hbm", dec + (cache if fused else 0),
                  case.num_seqs, layers=NL, pool_mb=case.k_pool.nbytes * 2 / 1e6, kernels={"decode_kernel": decode})
 
 

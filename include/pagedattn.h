@@ -139,6 +139,29 @@ int pa_paged_attention_decode(const pa_decode_desc *desc, const void *q, const v
                               const int32_t *context_lens, void *out, void *workspace,
                               size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/* Decode attention with the step's cache write in the same launch: the
+ * result of pa_reshape_and_cache of one new token per sequence followed by
+ * pa_paged_attention_decode, bit for bit, in one kernel launch.  Sequence s's
+ * new token is the last one it attends to, position ctx_s - 1 [ATT][PHASE];
+ * its K/V go to the next free slot of the sequence's last block [SHARE].
+ *   new_k, new_v  device bf16 [num_seqs][num_kv_heads][head_dim], 16-byte
+ *                 aligned: the new token's K and V
+ *   slot_mapping  device int64 [num_seqs]: the slot of position ctx_s - 1,
+ *                 block_tables[s][(ctx_s-1)/B] * B + (ctx_s-1) % B, or < 0 for
+ *                 no write (attention then reads what the slot holds)
+ *   k_pool, v_pool are written (that slot of every kv head) and read.
+ * A slot >= 0 that is not the slot of position ctx_s - 1 (outside the pool or
+ * elsewhere in it) sets PA_DEVERR_SLOT and writes nothing; so does nothing a
+ * sequence with a bad context length.  The block holding position ctx_s - 1
+ * must not be read at that offset by another sequence of the call (a block
+ * shared by several sequences is copied before it is written: copy-on-write).
+ * Other arguments, the workspace and the errors as in
+ * pa_paged_attention_decode. */
+int pa_paged_attention_decode_append(const pa_decode_desc *desc, const void *q, const void *new_k,
+                                     const void *new_v, const int64_t *slot_mapping, void *k_pool, void *v_pool,
+                                     const int32_t *block_tables, const int32_t *context_lens, void *out,
+                                     void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream);
+
 /* Bytes of device workspace pa_paged_attention_decode_shared_prefix needs for
  * `desc` on the current device (decode split-K scratch plus up to eight fp32
  * partial softmax states per (sequence, query head), one per key range of the

@@ -23,6 +23,7 @@ DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 
 # Every symbol include/pagedattn.h declares.
 EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
+    "pa_paged_attention_decode_append",
     "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk",
     "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_swap_blocks",
     "pa_bm_create_with_host", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_host",
@@ -69,6 +70,9 @@ def load(path: Optional[str] = None):
         lib.pa_paged_attention_decode.restype = i
         lib.pa_paged_attention_decode.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, sz,
                                                   _P, _P]
+        lib.pa_paged_attention_decode_append.restype = i
+        lib.pa_paged_attention_decode_append.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                                         _P, _P, sz, _P, _P]
         lib.pa_paged_attention_decode_noalloc.restype = i
         lib.pa_paged_attention_decode_noalloc.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P]
         lib.pa_shared_prefix_workspace_bytes.restype = sz
@@ -217,6 +221,41 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=No
                                           _ptr(block_tables), _ptr(context_lens), _ptr(out),
                                           _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_append(q, new_k, new_v, slot_mapping, k_pool, v_pool, block_tables, context_lens,
+                                  out=None, *, scale=None, max_context_len=None, workspace=None, err_flag=None,
+                                  stream=None):
+    """The decode step's cache write and attention in one launch: each
+    sequence's new token (new_k/new_v[s], position ctx-1) is stored at
+    slot_mapping[s], then decode attention runs over the cache (see
+    pagedattn.h)."""
+    import torch
+    _need(q, torch.bfloat16, "q", 3)
+    _need(new_k, torch.bfloat16, "new_k", 3)
+    _need(new_v, torch.bfloat16, "new_v", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(context_lens, torch.int32, "context_lens", 1)
+    nblk, hkv, bs, d = k_pool.shape
+    S = q.shape[0]
+    if tuple(new_k.shape) != (S, hkv, d) or tuple(new_v.shape) != (S, hkv, d) or slot_mapping.shape[0] != S:
+        raise ValueError("new_k/new_v must be [num_seqs][num_kv_heads][head_dim] and slot_mapping [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out", 3)
+    desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
+    if workspace is None:
+        workspace = decode_workspace(desc, q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_paged_attention_decode_append(_c.byref(desc), _ptr(q), _ptr(new_k), _ptr(new_v),
+                                                 _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool),
+                                                 _ptr(block_tables), _ptr(context_lens), _ptr(out),
+                                                 _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_paged_attention_decode_append")
     return out
 
 

@@ -30,6 +30,11 @@
 //  * When the grid fills a few waves of the resident slots, CTAs map to
 //    sequences longest context first (an in-kernel rank over the lengths).
 //  * Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+//  * Optionally (decode with append) the CTA that streams a sequence's last
+//    page also stores the step's new token (K/V at position ctx-1) into its
+//    slot of the pools and patches that row of its shared-memory copy of the
+//    page before the products -- the cache write of the decode step rides in
+//    the attention launch instead of a launch of its own.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -68,6 +73,13 @@ struct DecodeArgs {
   const float *pre_o;   // [npre][S][Hq][D] o/l of the prefix's key ranges
   const float *pre_ml;  // [npre][S][Hq][2] (m, l) of the prefix's key ranges
   int npre;
+  // Append (optional): app_k/app_v [S][Hkv][D] hold each sequence's newest
+  // token, which belongs at position ctx-1 in slot app_slots[s] (< 0: none).
+  const uint4 *app_k;
+  const uint4 *app_v;
+  const int64_t *app_slots;
+  uint4 *kp;  // the pools, written through for the append
+  uint4 *vp;
 };
 
 // Counts one arrival of this call at *c and returns the arrivals so far.  A
@@ -99,7 +111,8 @@ struct DecodeSmem {
   static constexpr int kTblOff = kBarOff + NW * NST * 8;
   static constexpr int kMiscOff = kTblOff + kMaxPartPages * 4;
   // misc: [0..3] broadcast words, [4..7] warp totals, [8..135] length histogram
-  static constexpr int kBytes = kMiscOff + 4 * 136;
+  static constexpr int kStageOff = kMiscOff + 4 * 136;  // appended token's K then V row
+  static constexpr int kBytes = kStageOff + 2 * D * 2;
   static constexpr int kAlloc = kBytes + 1024;  // base re-aligned to 1024 in the kernel
 };
 
@@ -172,7 +185,7 @@ __device__ int seq_of_rank(int r, const int32_t *ctx, int S, int B, int max_bloc
   return misc[2];
 }
 
-template <int D, int B, int NT, int NW, int NST, bool PRE>
+template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
@@ -243,6 +256,24 @@ __global__ void __launch_bounds__(NW * 32)
   }
   __syncthreads();
 
+  // ---- append: the part holding the last page owns the new token.  Its slot
+  // must be the one of position ctx-1; any other slot (out of the pool or
+  // elsewhere in it) is refused, so nothing this launch reads is written.
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks in one K or V row: lane c < 2 kRowChunks moves chunk c
+  static_assert(2 * kRowChunks <= 32, "one K and one V row fit a warp's lanes");
+  int app_row = -1;                  // the new token's row in the last page, for the warp streaming it
+  if (APP && part == nparts - 1 && np > 0) {
+    const int64_t slot = __ldg(a.app_slots + s);
+    const int pg = tbl[np - 1];
+    if (slot >= 0 && pg >= 0) {
+      if (slot == (int64_t)pg * B + (ctx - 1) % B) {
+        if (warp == (np - 1) % NW) app_row = (ctx - 1) % B;
+      } else if (tid == 0 && a.err) {
+        atomicOr(a.err, PA_DEVERR_SLOT);
+      }
+    }
+  }
+
   uint8_t *ring = smem + warp * NST * L::kSlotBytes;
   const int nmine = np > warp ? (np - warp + NW - 1) / NW : 0;
   const uint64_t pol = policy_evict_first();
@@ -281,6 +312,19 @@ __global__ void __launch_bounds__(NW * 32)
       } else {
         qf[nt][kk][0] = qf[nt][kk][1] = 0u;
       }
+    }
+  }
+
+  uint4 *stage = reinterpret_cast<uint4 *>(smem + L::kStageOff);
+  if (APP && app_row >= 0) {  // the new token: into its slot, and staged for the patch below
+    const size_t src = ((size_t)s * a.Hkv + kvh) * kRowChunks;
+    const size_t dst = (((size_t)tbl[np - 1] * a.Hkv + kvh) * B + app_row) * kRowChunks;
+    if (lane < 2 * kRowChunks) {
+      const bool isv = lane >= kRowChunks;
+      const int cc = isv ? lane - kRowChunks : lane;
+      const uint4 val = __ldg((isv ? a.app_v : a.app_k) + src + cc);
+      stage[lane] = val;
+      (isv ? a.vp : a.kp)[dst + cc] = val;
     }
   }
 
@@ -336,6 +380,18 @@ __global__ void __launch_bounds__(NW * 32)
       const uint32_t kb = smem_u32(ring + stg * L::kSlotBytes);
       const uint32_t vb = kb + L::kPageBytes;
       const int tok0 = (kp0 + p0 + lp) * B;
+      if (APP && app_row >= 0 && lp == np - 1) {
+        // The gather may have seen the slot before or after the store above:
+        // overwrite the row with the staged copy (each lane its own chunks).
+        uint8_t *slot = ring + stg * L::kSlotBytes;
+        if (lane < 2 * kRowChunks) {
+          const bool isv = lane >= kRowChunks;
+          const int cc = isv ? lane - kRowChunks : lane;
+          *reinterpret_cast<uint4 *>(slot + (isv ? L::kPageBytes : 0) + (cc >> 3) * L::kBoxBytes +
+                                     sw128(app_row, cc & 7)) = stage[lane];
+        }
+        __syncwarp();
+      }
 
       // S^T[token][head] = K Q^T
       float sc[MT][NT][4];
@@ -629,7 +685,7 @@ unsigned int next_epoch() {
   return e;
 }
 
-template <int D, int B, int NT, bool PRE>
+template <int D, int B, int NT, bool PRE, bool APP>
 int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                   cudaStream_t st) {
   // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM); 32-token pages:
@@ -642,7 +698,7 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
   constexpr int NST = (B == 16) ? (PRE ? 2 : 3) : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
-  auto kern = decode_kernel<D, B, NT, NW, NST, PRE>;
+  auto kern = decode_kernel<D, B, NT, NW, NST, PRE, APP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   kern<<<grid, NW * 32, L::kAlloc, st>>>(tk, tv, a);
@@ -652,9 +708,16 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
 template <int D, int B>
 int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                 cudaStream_t st) {
-  if (a.ngroups > 0)  // shared-prefix launch: prefix states prefetched (more registers)
-    return G <= 8 ? launch_decode<D, B, 1, true>(tk, tv, a, grid, st) : launch_decode<D, B, 2, true>(tk, tv, a, grid, st);
-  return G <= 8 ? launch_decode<D, B, 1, false>(tk, tv, a, grid, st) : launch_decode<D, B, 2, false>(tk, tv, a, grid, st);
+  // Separate instances keep the plain decode's registers: the shared-prefix
+  // launch (prefix states prefetched) and the decode with append.
+  if (a.ngroups > 0)
+    return G <= 8 ? launch_decode<D, B, 1, true, false>(tk, tv, a, grid, st)
+                  : launch_decode<D, B, 2, true, false>(tk, tv, a, grid, st);
+  if (a.app_slots)
+    return G <= 8 ? launch_decode<D, B, 1, false, true>(tk, tv, a, grid, st)
+                  : launch_decode<D, B, 2, false, true>(tk, tv, a, grid, st);
+  return G <= 8 ? launch_decode<D, B, 1, false, false>(tk, tv, a, grid, st)
+                : launch_decode<D, B, 2, false, false>(tk, tv, a, grid, st);
 }
 
 }  // namespace
@@ -664,11 +727,14 @@ namespace pa {
 
 int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
                   const int32_t *block_tables, const int32_t *context_lens, void *out, void *workspace,
-                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre) {
+                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre,
+                  const DecodeAppend *app) {
   int st = validate_decode_desc(d);
   if (st != PA_OK) return st;
   if (d->num_seqs == 0) return PA_OK;
   if (!q || !k_pool || !v_pool || !block_tables || !context_lens || !out) return PA_ERR_INVALID;
+  if (app && (pre || !app->new_k || !app->new_v || !app->slots || !aligned16(app->new_k) || !aligned16(app->new_v)))
+    return PA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
     return PA_ERR_INVALID;
   if (d->num_seqs > 65535 || d->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
@@ -724,6 +790,11 @@ int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, co
   a.pre_o = pre ? pre->pre_o : nullptr;
   a.pre_ml = pre ? pre->pre_ml : nullptr;
   a.npre = pre ? pre->npre : 0;
+  a.app_k = app ? static_cast<const uint4 *>(app->new_k) : nullptr;
+  a.app_v = app ? static_cast<const uint4 *>(app->new_v) : nullptr;
+  a.app_slots = app ? app->slots : nullptr;
+  a.kp = app ? static_cast<uint4 *>(const_cast<void *>(k_pool)) : nullptr;
+  a.vp = app ? static_cast<uint4 *>(const_cast<void *>(v_pool)) : nullptr;
   const dim3 grid(plan.max_parts, d->num_kv_heads, d->num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d->head_dim == 128)
@@ -740,5 +811,16 @@ extern "C" int pa_paged_attention_decode(const pa_decode_desc *d, const void *q,
                                          const int32_t *context_lens, void *out, void *workspace,
                                          size_t workspace_bytes, int32_t *err_flag, void *stream) {
   return pa::decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes,
-                           err_flag, stream, nullptr);
+                           err_flag, stream, nullptr, nullptr);
+}
+
+extern "C" int pa_paged_attention_decode_append(const pa_decode_desc *d, const void *q, const void *new_k,
+                                                const void *new_v, const int64_t *slot_mapping, void *k_pool,
+                                                void *v_pool, const int32_t *block_tables,
+                                                const int32_t *context_lens, void *out, void *workspace,
+                                                size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  if (!new_k || !new_v || !slot_mapping) return PA_ERR_INVALID;
+  const pa::DecodeAppend app{new_k, new_v, slot_mapping};
+  return pa::decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes,
+                           err_flag, stream, nullptr, &app);
 }

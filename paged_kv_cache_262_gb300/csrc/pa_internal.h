@@ -54,10 +54,20 @@ struct DecodePrefix {
   int npre;                   // partial states per row (key ranges of the prefix)
 };
 
-// The decode launcher behind pa_paged_attention_decode (pre may be null).
+// The newest token of every sequence, appended by the decode launch itself
+// (pa_paged_attention_decode_append).
+struct DecodeAppend {
+  const void *new_k;     // device bf16 [S][Hkv][D]
+  const void *new_v;     // device bf16 [S][Hkv][D]
+  const int64_t *slots;  // device [S], the slot of position ctx-1 or < 0
+};
+
+// The decode launcher behind pa_paged_attention_decode (pre and app may be
+// null; not both set).
 int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
                   const int32_t *block_tables, const int32_t *context_lens, void *out, void *workspace,
-                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre);
+                  size_t workspace_bytes, int32_t *err_flag, void *stream, const DecodePrefix *pre,
+                  const DecodeAppend *app = nullptr);
 
 // Launches the chunked-prefill kernel (pa_prefill.cu).  causal = 0 lets every
 // row see all ctx keys; with part_o/part_ml set, rows are written as fp32
