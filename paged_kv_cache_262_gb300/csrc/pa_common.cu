@@ -90,27 +90,40 @@ int validate_decode_desc(const pa_decode_desc *d) {
 
 // Split policy.  Each CTA streams one part (part_pages pages of one
 // (sequence, kv head)); two CTAs (16-token pages) or three (32-token pages)
-// are resident per SM.  Long parts amortise the per-CTA set-up and the
-// split-K merge, so parts are sized for about 1.5 CTAs per resident slot over
-// the longest-context bound (never below kMinPartPages pages unless the
-// context is shorter); when the grid fills a few waves the CTAs start longest
-// context first, which keeps the ragged tail short.  PA_PARTITION_PAGES in the
-// environment overrides the part length (tuning).
+// are resident per SM.  The host knows only the longest-context bound, so it
+// plans for every unit at that length.  A context longer than kMaxPartPages
+// pages is always cut.  When the units leave room, each is cut into as many
+// equal parts as fit one wave of the resident slots: the CTAs all start at
+// once, stream equal shares and end together (8 x 32768 tokens, GQA 8:
+// four 512-page parts, 256 CTAs, 166.0 us, against 168.3-169.7 us for
+// eight parts in 1.7 waves; a thin last wave leaves HBM idle: 320 CTAs on
+// 304 slots 218 us, 384 CTAs 190 us).  With more units than that, parts are
+// sized for about 1.5 CTAs per resident slot (ragged batches then start
+// longest context first).  Parts never go below kMinPartPages pages unless
+// the context is shorter.  PA_PARTITION_PAGES in the environment overrides
+// the part length (tuning).
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
   const int kCtasPerSm = d->block_size == 16 ? 2 : 3;  // resident decode CTAs per SM (shared memory)
   constexpr int kMinPartPages = 32;
   DecodePlan p;
   const int B = d->block_size;
   const int64_t max_pages = std::max<int64_t>(1, ((int64_t)d->max_context_len + B - 1) / B);
-  const int64_t units = (int64_t)d->num_seqs * d->num_kv_heads;
+  const int64_t units = std::max<int64_t>(1, (int64_t)d->num_seqs * d->num_kv_heads);
   int64_t pp;
   const char *env = getenv("PA_PARTITION_PAGES");
   if (env && atoi(env) > 0) {
     pp = atoi(env);
   } else {
     const int64_t slots = (int64_t)std::max(sm_count, 1) * kCtasPerSm;
-    pp = (units * max_pages * 2 + slots * 3 - 1) / (slots * 3);
-    pp = std::max<int64_t>(pp, kMinPartPages);
+    const int64_t least = (max_pages + kMaxPartPages - 1) / kMaxPartPages;  // parts of <= kMaxPartPages pages
+    const int64_t most = std::min<int64_t>(kMaxParts, std::max<int64_t>(1, max_pages / kMinPartPages));
+    if (units * least <= slots) {
+      const int64_t np = std::max(least, std::min(slots / units, most));
+      pp = (max_pages + np - 1) / np;
+    } else {
+      pp = (units * max_pages * 2 + slots * 3 - 1) / (slots * 3);
+      pp = std::max<int64_t>(pp, kMinPartPages);
+    }
   }
   pp = std::max<int64_t>(pp, (max_pages + kMaxParts - 1) / kMaxParts);
   pp = std::min<int64_t>(pp, kMaxPartPages);
