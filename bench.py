@@ -11,8 +11,10 @@ seeded generator in ``workloads``:
 * ``prefix_sharing``: 64 prompts x 4 samples over a 2048-token prefix built by
   the host block manager; copy_blocks of the copy-on-write pairs,
   reshape_and_cache of the appended tokens, decode over the shared tables;
-* ``mixed_step``: one reshape_and_cache of every new token, chunked prefill of
-  16 x 512 query tokens (tensor cores), decode of 240 sequences (B=32).
+* ``mixed_step``: one reshape_and_cache of every new token, then chunked
+  prefill of 16 x 512 query tokens (tensor cores) and decode of 240 sequences
+  (B=32) in one mixed-step launch whose CTAs run the two side by side
+  (``--mixed-launch separate``: two launches).
 
 To keep reads coming from HBM, each step uses the next of NL layer pools
 (separate copies of the cache, together several times the 129 MB L2).
@@ -70,6 +72,12 @@ def parse():
     ap.add_argument("--chunks", type=int, default=16, help="mixed_step: prefill chunks")
     ap.add_argument("--decodes", type=int, default=240, help="mixed_step: decode sequences")
     ap.add_argument("--block-size", type=int, default=32, choices=[16, 32], help="mixed_step: tokens per page")
+    ap.add_argument("--mixed-launch", default="fused", choices=["separate", "fused"],
+                    help="mixed_step: one mixed-step launch whose CTAs run the prefill and the decode side by "
+                         "side (default), or the two as separate launches")
+    ap.add_argument("--overlap", default="none", choices=["none", "decode", "decode-hi", "prefill-hi"],
+                    help="mixed_step: run prefill and decode on two streams (forked and joined in the step); "
+                         "which one goes to the side stream and whether that stream has high priority")
     ap.add_argument("--separate-append", action="store_true",
                     help="decode workloads: reshape_and_cache and decode as two launches instead of one "
                          "decode-with-append launch")
@@ -404,14 +412,46 @@ def build_mixed(args, torch, pa, dev):
         pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], dout if dout is not None else outs["dout"],
                                   max_context_len=dec.max_context_len, workspace=ws)
 
+    fused = args.mixed_launch == "fused"
+
+    def mixed(i, x, pout=None, dout=None):
+        l = i % NL
+        pa.paged_attention_mixed(x["q_chunk"], x["cu_q"], x["chunk_bt"], x["chunk_ctx"], x["q"], x["bt"], x["ctx"],
+                                 kps[l], vps[l], pout if pout is not None else outs["pout"],
+                                 dout if dout is not None else outs["dout"], max_q_len=512,
+                                 prefill_max_context_len=max_cctx, decode_max_context_len=dec.max_context_len,
+                                 workspace=ws)
+
+    side = None
+    if args.overlap != "none":
+        side = torch.cuda.Stream(device=dev, priority=-1 if args.overlap.endswith("-hi") else 0)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        side_fn = prefill if args.overlap == "prefill-hi" else decode
+        main_fn = decode if args.overlap == "prefill-hi" else prefill
+
     def step(i, x, ev, o=None):  # on the current stream
         l = i % NL
         pout, dout = o if o else (outs["pout"], outs["dout"])
         pa.reshape_and_cache(x["new_k"], x["new_v"], kps[l], vps[l], x["slots"])
         ev and ev[0].record()
-        prefill(i, x, pout)
-        ev and ev[1].record()
-        decode(i, x, dout)
+        if fused:
+            mixed(i, x, pout, dout)
+            ev and ev[1].record()
+            return [pout, dout]
+        if side is not None:  # the two attention launches side by side, joined before the step ends
+            cur = torch.cuda.current_stream()
+            fork.record(cur)
+            side.wait_event(fork)
+            with torch.cuda.stream(side):
+                side_fn(i, x, pout if side_fn is prefill else dout)
+            main_fn(i, x, pout if main_fn is prefill else dout)
+            join.record(side)
+            cur.wait_event(join)
+            ev and ev[1].record()
+        else:
+            prefill(i, x, pout)
+            ev and ev[1].record()
+            decode(i, x, dout)
         ev and ev[2].record()
         return [pout, dout]
 
@@ -426,16 +466,19 @@ def build_mixed(args, torch, pa, dev):
     new_k = np.concatenate([m.chunk_new_k, dec.new_k])
     new_v = np.concatenate([m.chunk_new_v, dec.new_v])
     slots = np.concatenate([m.chunk_slots, dec.slot_mapping])
+    what = "one mixed-step launch (prefill and decode side by side)" if fused else "prefill + decode"
     return Bench("mixed_step", f"mixed_step: {len(cctx)} prefill chunks x 512 tokens (ctx {int(cctx.min())}..{int(cctx.max())})"
                  f" + {dec.num_seqs} decodes (ctx {int(dctx.min())}..{int(dctx.max())}), 32q/8kv, D=128, B={B}; "
-                 f"reshape_and_cache of {Tn} tokens + prefill + decode",
+                 f"reshape_and_cache of {Tn} tokens + {what}",
                  {"q_chunk": m.q_chunk, "cu_q": m.cu_q, "chunk_bt": m.chunk_tables, "chunk_ctx": m.chunk_ctx,
                   "q": dec.q, "bt": dec.block_tables, "ctx": dec.context_lens, "new_k": new_k, "new_v": new_v,
                   "slots": slots},
-                 step, pre_bytes + dbytes + cache_bytes(Tn, 8, 128), 3, "prefill_kernel", "tensor", flops,
+                 step, pre_bytes + dbytes + cache_bytes(Tn, 8, 128), 2 if fused else 3,
+                 "mixed_kernel" if fused else "prefill_kernel", "hbm" if fused else "tensor",
+                 pre_bytes + dbytes if fused else flops,
                  dec.num_seqs, extra={"prefill_flops": flops, "decode_bytes": dbytes, "prefill_kv_bytes": pre_bytes},
                  layers=NL, pool_mb=dec.k_pool.nbytes * 2 / 1e6,
-                 kernels={"prefill_kernel": prefill, "decode_kernel": decode})
+                 kernels=({"mixed_kernel": mixed} if fused else {}) | {"prefill_kernel": prefill, "decode_kernel": decode})
 
 
 def build(args, torch, pa, dev):
@@ -542,6 +585,9 @@ def run_ours(args, rank, world, local_rank):
         k_mean = k_median = per[b.kernel]
         if "decode_kernel" in per and b.kernel != "decode_kernel":
             side["decode_launch_ms_mean"] = per["decode_kernel"]
+        if "prefill_kernel" in per and b.kernel != "prefill_kernel":
+            side["prefill_launch_ms_mean"] = per["prefill_kernel"]
+            side["prefill_tflops"] = round(b.extra["prefill_flops"] / (per["prefill_kernel"] / 1e3) / 1e12, 1)
         timing = (f"CUDA graph of the {args.steps} steps; per-kernel launch time from a graph of the kernel's "
                   f"{args.steps} launches alone")
     if "decode_launch_ms_mean" in side:
@@ -584,6 +630,13 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "timing": timing,
     }
+    if b.kernel == "mixed_kernel":  # one launch doing both: the prefill's tensor work in the same time
+        tf = b.extra["prefill_flops"] / (k_mean / 1e3) / 1e12
+        res["roofline"]["tensor"] = {"achieved": round(tf, 1), "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                                     "frac": round(tf / peaks["bf16_sustained"], 4)}
+        lower = max(b.extra["prefill_flops"] / (peaks["bf16_sustained"] * 1e12),
+                    b.kernel_work / (peaks["hbm"] * 1e9)) * 1e3
+        res["roofline"]["lower_bound_ms"] = round(lower, 4)
     res.update(side)
     if b.extra:
         res["workload_extra"] = b.extra

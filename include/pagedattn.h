@@ -250,6 +250,31 @@ int pa_paged_attention_prefill_chunk(const pa_decode_desc *desc, const void *q,
                                      const int32_t *block_tables, const int32_t *context_lens,
                                      void *out, int32_t *err_flag, void *stream);
 
+/* The attention of one continuous-batching step [CHUNK] in one launch: the
+ * causal chunked prefill of prefill_desc->num_seqs chunks and the decode of
+ * decode_desc->num_seqs sequences over the same pools, run side by side (the
+ * tensor-bound prefill tiles and the HBM-bound decode units share the GPU
+ * instead of taking turns).  The results are those of
+ *   pa_paged_attention_prefill_chunk(prefill_desc, prefill_q, cu_q, max_q_len,
+ *       total_q, k_pool, v_pool, prefill_tables, prefill_context_lens,
+ *       prefill_out, ...)
+ *   pa_paged_attention_decode(decode_desc, decode_q, k_pool, v_pool,
+ *       decode_tables, decode_context_lens, decode_out, workspace, ...)
+ * bit for bit, with the arguments, layouts and errors of those two calls
+ * (the workspace: pa_decode_workspace_bytes(decode_desc)).  Both descs must
+ * describe the same pools (num_q_heads, num_kv_heads, head_dim = 128,
+ * block_size, num_blocks) and the GQA group must be 1, 2, 4, 8 or 16;
+ * otherwise PA_ERR_INVALID / PA_ERR_UNSUPPORTED.  Either part may be empty
+ * (num_seqs == 0, or no prefill rows).  The K/V of every token attended must
+ * already be cached (pa_reshape_and_cache). */
+int pa_paged_attention_mixed(const pa_decode_desc *prefill_desc, const void *prefill_q, const int32_t *cu_q,
+                             int max_q_len, int total_q, const int32_t *prefill_tables,
+                             const int32_t *prefill_context_lens, void *prefill_out,
+                             const pa_decode_desc *decode_desc, const void *decode_q, const int32_t *decode_tables,
+                             const int32_t *decode_context_lens, void *decode_out, void *workspace,
+                             size_t workspace_bytes, const void *k_pool, const void *v_pool, int32_t *err_flag,
+                             void *stream);
+
 /* Writes the K/V of num_tokens new tokens into their cache slots [PHASE][SHARE]:
  *   k_pool[slot / B][h][slot % B][:] = k[t][h][:]  (same for v), for t in order.
  * Bit-exact copy.  slot < 0: token skipped.  slot >= num_blocks*B: skipped and

@@ -23,7 +23,7 @@ DEVERR_CTX, DEVERR_PAGE, DEVERR_SLOT, DEVERR_PAIR, DEVERR_TIMEOUT = 1, 2, 4, 8, 
 # Every symbol include/pagedattn.h declares.
 EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
-    "pa_paged_attention_decode_append",
+    "pa_paged_attention_decode_append", "pa_paged_attention_mixed",
     "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk",
     "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_swap_blocks",
     "pa_bm_create_with_host", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_host",
@@ -73,6 +73,9 @@ def load(path: Optional[str] = None):
         lib.pa_paged_attention_decode_append.restype = i
         lib.pa_paged_attention_decode_append.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P,
                                                          _P, _P, sz, _P, _P]
+        lib.pa_paged_attention_mixed.restype = i
+        lib.pa_paged_attention_mixed.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, i, _P, _P, _P,
+                                                 _c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, sz, _P, _P, _P, _P]
         lib.pa_paged_attention_decode_noalloc.restype = i
         lib.pa_paged_attention_decode_noalloc.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, _P, _P, _P]
         lib.pa_shared_prefix_workspace_bytes.restype = sz
@@ -339,6 +342,43 @@ def paged_attention_prefill_chunk(q, cu_q, k_pool, v_pool, block_tables, context
                                                  _stream_ptr(stream))
     _check(st, "pa_paged_attention_prefill_chunk")
     return out
+
+
+def paged_attention_mixed(prefill_q, cu_q, prefill_tables, prefill_context_lens, decode_q, decode_tables,
+                          decode_context_lens, k_pool, v_pool, prefill_out=None, decode_out=None, *, max_q_len,
+                          scale=None, prefill_max_context_len=None, decode_max_context_len=None, workspace=None,
+                          err_flag=None, stream=None):
+    """A continuous-batching step's chunked prefill and decode in one launch,
+    side by side (see pagedattn.h); returns (prefill_out, decode_out)."""
+    import torch
+    _need(prefill_q, torch.bfloat16, "prefill_q", 3)
+    _need(cu_q, torch.int32, "cu_q", 1)
+    _need(prefill_tables, torch.int32, "prefill_tables", 2)
+    _need(prefill_context_lens, torch.int32, "prefill_context_lens", 1)
+    _need(decode_q, torch.bfloat16, "decode_q", 3)
+    _need(decode_tables, torch.int32, "decode_tables", 2)
+    _need(decode_context_lens, torch.int32, "decode_context_lens", 1)
+    _need(k_pool, torch.bfloat16, "k_pool", 4)
+    _need(v_pool, torch.bfloat16, "v_pool", 4)
+    if prefill_out is None:
+        prefill_out = torch.empty_like(prefill_q)
+    if decode_out is None:
+        decode_out = torch.empty_like(decode_q)
+    _need(prefill_out, torch.bfloat16, "prefill_out", 3)
+    _need(decode_out, torch.bfloat16, "decode_out", 3)
+    pdesc = make_desc(prefill_q, k_pool, prefill_tables, num_seqs=prefill_context_lens.shape[0], scale=scale,
+                      max_context_len=prefill_max_context_len)
+    ddesc = make_desc(decode_q, k_pool, decode_tables, scale=scale, max_context_len=decode_max_context_len)
+    if workspace is None:
+        workspace = decode_workspace(ddesc, decode_q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().pa_paged_attention_mixed(_c.byref(pdesc), _ptr(prefill_q), _ptr(cu_q), int(max_q_len),
+                                         int(prefill_q.shape[0]), _ptr(prefill_tables), _ptr(prefill_context_lens),
+                                         _ptr(prefill_out), _c.byref(ddesc), _ptr(decode_q), _ptr(decode_tables),
+                                         _ptr(decode_context_lens), _ptr(decode_out), _ptr(workspace), ws_bytes,
+                                         _ptr(k_pool), _ptr(v_pool), _ptr(err_flag), _stream_ptr(stream))
+    _check(st, "pa_paged_attention_mixed")
+    return prefill_out, decode_out
 
 
 def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, *, err_flag=None, stream=None):

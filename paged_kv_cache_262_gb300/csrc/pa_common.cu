@@ -102,6 +102,15 @@ int validate_decode_desc(const pa_decode_desc *d) {
 // longest context first).  Parts never go below kMinPartPages pages unless
 // the context is shorter.  PA_PARTITION_PAGES in the environment overrides
 // the part length (tuning).
+unsigned int next_decode_epoch() {
+  static std::atomic<unsigned int> counter{0};
+  unsigned int e;
+  do {
+    e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);
+  return e;
+}
+
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
   const int kCtasPerSm = d->block_size == 16 ? 2 : 3;  // resident decode CTAs per SM (shared memory)
   constexpr int kMinPartPages = 32;

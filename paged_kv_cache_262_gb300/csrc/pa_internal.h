@@ -44,6 +44,10 @@ int validate_decode_desc(const pa_decode_desc *d);
 // The plan used by both pa_decode_workspace_bytes and the launcher.
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count);
 
+// A new tag for the split-K arrival counters of one decode launch: unique
+// (never 0) across every launcher that may share a workspace.
+unsigned int next_decode_epoch();
+
 // Shared-prefix information for the decode kernel (see pa_shared_prefix.cu).
 struct DecodePrefix {
   const int32_t *grp_start;   // device [ngroups + 1]
