@@ -113,10 +113,14 @@ def kernel_traffic(kernel: str, workload: str):
     j = json.load(open(TRAFFIC_FILE)).get(f"{kernel}@{workload}")
     if not j:
         return None
-    src = os.path.join(CSRC, j["source"])
-    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest() != j["sha256"]:
-        return None
-    return j.get("bytes_per_launch")
+    srcs = j["source"] if isinstance(j["source"], list) else [j["source"]]
+    h = hashlib.sha256()
+    for f in srcs:  # the kernel's sources, hashed in the listed order
+        path = os.path.join(CSRC, f)
+        if not os.path.exists(path):
+            return None
+        h.update(open(path, "rb").read())
+    return j.get("bytes_per_launch") if h.hexdigest() == j["sha256"] else None
 
 
 class ClockSampler:
