@@ -189,8 +189,8 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   const int warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
   const int ctx = __ldg(a.ctx + s);
-  int kstart = 0;  // first key this kernel covers (end of a shared prefix)
-  if (a.ngroups > 0 && s >= __ldg(a.grp_start) && s < __ldg(a.grp_start + a.ngroups)) {
+  int kstart = 0;  // first key this kernel covers (end of a shared prefix; PRE launches only)
+  if (PRE && a.ngroups > 0 && s >= __ldg(a.grp_start) && s < __ldg(a.grp_start + a.ngroups)) {
     int lo = 0, hi = a.ngroups;  // grp_start[lo] <= s < grp_start[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -309,7 +309,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   // under the streaming (thread tid: output elements tid + j NW 32, and the
   // (m, l) of head tid), when a thread's share is small enough for registers.
   constexpr int kPreElems = 4;
-  const int npre = (has_pre && nparts == 1) ? a.npre : 0;
+  const int npre = (PRE && has_pre && nparts == 1) ? a.npre : 0;
   // (PRE: the shared-prefix launch; groups of more than 8 heads never qualify)
   const bool pre_early = PRE && NT == 1 && npre > 0 && G * D <= kPreElems * NW * 32;
   const size_t slab = (size_t)a.S * a.Hq;
@@ -610,7 +610,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   if (tid < G) {
     const int g = tid;
     const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
-    const int npre = has_pre ? a.npre : 0;
+    const int npre = (PRE && has_pre) ? a.npre : 0;
     float M = -INFINITY;
     for (int p = 0; p < npre; ++p) {
       const float lp = __ldg(a.pre_ml + 2 * (p * slab + row) + 1);
@@ -643,7 +643,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     const int g = idx / D, d = idx - g * D;
     float acc = 0.f;
     for (int p = 0; p < nparts; ++p) acc += wts[p * 16 + g] * __ldcg(a.ws_o + ((ubase + p) * G + g) * D + d);
-    if (has_pre)
+    if (PRE && has_pre)
       for (int p = 0; p < a.npre; ++p)
         acc += wpre[p * 16 + g] * __ldg(a.pre_o + (p * slab + (size_t)s * a.Hq + (size_t)kvh * G + g) * D + d);
     out_base[idx] = __float2bfloat16(acc);

@@ -125,9 +125,45 @@ def test_shared_prefix_workload(torch, ora):
 
 
 def test_prefix_not_block_multiple_flagged(torch):
-    case, gs, gp, pt = grouped_case(32, 8, 128, 16, [(3, 64)], 0, seed=5)
+    case, gs, gp, pt = grouped_case(32, 8, 128, 16, [(3, 64)], 2, seed=5)
     gp = gp + 3  # not a whole number of blocks
     pt = np.concatenate([pt, pt[:, :1]], axis=1)  # room for the extra tokens
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    run_both(torch, case, gs, gp, pt, err)
+    shared, plain = run_both(torch, case, gs, gp, pt, err)
     assert int(err.item()) & pa.DEVERR_CTX
+    assert not np.any(shared[:3])                  # the group's rows: zeros, as for any bad context
+    assert np.array_equal(shared[3:], plain[3:])   # sequences outside the group: plain decode
+
+
+@pytest.mark.parametrize("pp", [None, 2])
+def test_shared_prefix_graph_replay(torch, monkeypatch, pp):
+    """Captured once and replayed: the merge counters are reset by each merge,
+    so every replay (same epoch) merges again and gives the same bits."""
+    if pp is None:
+        monkeypatch.delenv("PA_PARTITION_PAGES", raising=False)
+    else:
+        monkeypatch.setenv("PA_PARTITION_PAGES", str(pp))
+    case, gs, gp, pt = grouped_case(32, 8, 128, 16, [(6, 128), (2, 64)], 2, seed=11)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    q, kp, vp = bf16_dev(case.q, torch), bf16_dev(case.k_pool, torch), bf16_dev(case.v_pool, torch)
+    bt, ctx, gsd, gpd, ptd = dev(case.block_tables), dev(case.context_lens), dev(gs), dev(gp), dev(pt)
+    kw = dict(max_group_size=int(np.diff(gs).max()), max_prefix_len=int(gp.max()), scale=case.scale,
+              max_context_len=case.max_context_len)
+    want = bf16_host(pa.paged_attention_decode_shared_prefix(q, kp, vp, bt, ctx, gsd, gpd, ptd, **kw))
+    out = torch.empty_like(q)
+    desc = pa.make_desc(q, kp, bt, scale=case.scale, max_context_len=case.max_context_len)
+    import ctypes
+    need = int(pa.load().pa_shared_prefix_workspace_bytes(ctypes.byref(desc)))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(2):
+            pa.paged_attention_decode_shared_prefix(q, kp, vp, bt, ctx, gsd, gpd, ptd, out, workspace=ws, **kw)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_host(out), want)
