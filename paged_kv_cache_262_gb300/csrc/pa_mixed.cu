@@ -28,13 +28,28 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include "pa_fused.cuh"
+#include "pa_decode_body.cuh"
 #include "pa_internal.h"
+#include "pa_prefill_body.cuh"
 #include "pa_ptx.cuh"
 #include "pagedattn.h"
 
 namespace pa {
 namespace {
+
+constexpr int kUnitsPerCta = kThreads / 128;  // decode units (4 warps each) in one mixed-step CTA
+
+template <int B>
+struct MixedSmem {
+  // 16-token pages: two ring slots a warp (three units must fit one CTA);
+  // 32-token pages: one, as in the decode kernel.
+  static constexpr int kDecodeStages = B == 16 ? 2 : 1;
+  using L = DecodeSmem<128, B, 4, kDecodeStages>;
+  static constexpr int kUnitStride = (L::kBytes + 1023) & ~1023;
+  static constexpr int kDecodeBytes = kUnitsPerCta * kUnitStride + 1024;  // + alignment slack
+  static constexpr int kBytes = kDecodeBytes > kSmem ? kDecodeBytes : kSmem;
+  static_assert(kBytes <= 227 * 1024, "mixed-step shared memory over the per-CTA limit");
+};
 
 // Dispatch order of the two roles (PA_MIXED_ORDER: interleave, decode-first,
 // prefill-first; the last two are for comparison).
@@ -52,7 +67,7 @@ template <int B, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const PrefillArgs pf, const DecodeArgs dc, const MixedPlan m) {
-  using M = FusedSmem<B>;
+  using M = MixedSmem<B>;
   constexpr int NT = G <= 8 ? 1 : 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -86,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int B, int G>
 int launch_mixed(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &pf, const DecodeArgs &dc,
                  const MixedPlan &m, cudaStream_t st) {
-  using M = FusedSmem<B>;
+  using M = MixedSmem<B>;
   auto kern = mixed_kernel<B, G>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kBytes) != cudaSuccess)
     return PA_ERR_CUDA;
