@@ -11,6 +11,10 @@ seeded generator in ``workloads``:
 * ``prefix_sharing``: 64 prompts x 4 samples over a 2048-token prefix built by
   the host block manager; copy_blocks of the copy-on-write pairs,
   reshape_and_cache of the appended tokens, decode over the shared tables;
+* ``parallel_sampling``: 64 prompts of U[1024,4096] tokens x 4 samples, no
+  prefix common to all: each prompt's blocks shared by its samples
+  (sub-groups; ``--sharing one-level``: each prompt a group;
+  ``--plain-decode``);
 * ``mixed_step``: one reshape_and_cache of every new token, then chunked
   prefill of 16 x 512 query tokens (tensor cores) and decode of 240 sequences
   (B=32) in one mixed-step launch whose CTAs run the two side by side
@@ -59,7 +63,8 @@ CSRC = os.path.join(ROOT, "paged_kv_cache_262_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s"
 L2_BYTES = 129e6
-WORKLOADS = ["llama8b_decode", "long_context_decode", "tiny_decode", "prefix_sharing", "mixed_step"]
+WORKLOADS = ["llama8b_decode", "long_context_decode", "tiny_decode", "prefix_sharing", "parallel_sampling",
+             "mixed_step"]
 
 
 def parse():
@@ -78,6 +83,10 @@ def parse():
     ap.add_argument("--overlap", default="none", choices=["none", "decode", "decode-hi", "prefill-hi"],
                     help="mixed_step: run prefill and decode on two streams (forked and joined in the step); "
                          "which one goes to the side stream and whether that stream has high priority")
+    ap.add_argument("--sharing", default="auto", choices=["auto", "one-level", "subgroups"],
+                    help="prefix_sharing / parallel_sampling: groups only (one level), or each prompt's samples "
+                         "as sub-groups too; auto = one level for prefix_sharing (short suffixes: the per-sample "
+                         "units win), sub-groups for parallel_sampling (long prompts: reading them once wins)")
     ap.add_argument("--separate-append", action="store_true",
                     help="decode workloads: reshape_and_cache and decode as two launches instead of one "
                          "decode-with-append launch")
@@ -283,11 +292,11 @@ def build_decode(args, torch, pa, dev, case):
                  case.num_seqs, layers=NL, pool_mb=case.k_pool.nbytes * 2 / 1e6, kernels={"decode_kernel": decode})
 
 
-def prefix_sharing_setup(pa):
-    """Tables, copy-on-write pairs and slots of the prefix-sharing workload,
-    produced by the host block manager (fork per prompt and per sample, then
-    one appended token per sample)."""
-    plan = wl.prefix_sharing_plan()
+def prefix_sharing_setup(pa, plan=None):
+    """Tables, copy-on-write pairs and slots of the prefix-sharing workload (or
+    another plan of the same shape), produced by the host block manager (fork
+    per prompt and per sample, then one appended token per sample)."""
+    plan = plan or wl.prefix_sharing_plan()
     B, R = plan.B, plan.samples_per_prompt
     bm = pa.BlockManager(plan.num_blocks, B)
     root = 10 ** 6
@@ -314,8 +323,27 @@ def prefix_sharing_setup(pa):
     return plan, bt, ctx, np.array(slots, np.int64), np.array(pairs, np.int64).reshape(-1, 2)
 
 
-def build_prefix(args, torch, pa, dev):
-    plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa)
+def prefix_sharing_subgroups(plan, bt, ctx):
+    """The second sharing level of the prefix-sharing workload: the samples of
+    one prompt (consecutive sequences) as a sub-group sharing their common
+    leading blocks (the prompt prefix and the prompt's full suffix blocks;
+    the partial block each sample copied on write is its own)."""
+    B, R = plan.B, plan.samples_per_prompt
+    S = len(ctx)
+    starts, shared = [0], []
+    for a in range(0, S, R):
+        rows = bt[a: a + R]
+        n = 0
+        while n < rows.shape[1] and rows[0, n] >= 0 and np.all(rows[:, n] == rows[0, n]):
+            n += 1
+        shared.append(min(n, int(ctx[a: a + R].min()) // B) * B)
+        starts.append(min(a + R, S))
+    return np.array(starts, np.int32), np.array(shared, np.int32)
+
+
+def build_prefix(args, torch, pa, dev, plan=None):
+    plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa, plan)
+    name = "prefix_sharing" if plan.prefix_len > 0 else "parallel_sampling"
     kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
     up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
     NL = n_layers(args, kp.nbytes * 2)
@@ -327,10 +355,23 @@ def build_prefix(args, torch, pa, dev):
     ws = pa.decode_workspace(desc, dev)
     outs = {"out": torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)}
 
-    npre = plan.prefix_len // B
-    groups = {"gs": np.array([0, S], np.int32), "gp": np.array([plan.prefix_len], np.int32),
-              "pt": np.ascontiguousarray(bt[:1, :npre])}
     shared = not args.plain_decode
+    sharing = args.sharing if args.sharing != "auto" else ("one-level" if name == "prefix_sharing" else "subgroups")
+    two = shared and sharing == "subgroups"  # the prompts' samples as sub-groups
+    ss, sh = prefix_sharing_subgroups(plan, bt, ctx)
+    if plan.prefix_len > 0:  # one group: the prefix every prompt starts with
+        npre = plan.prefix_len // B
+        groups = {"gs": np.array([0, S], np.int32), "gp": np.array([plan.prefix_len], np.int32),
+                  "pt": np.ascontiguousarray(bt[:1, :npre])}
+        gmax, gplen = S, plan.prefix_len
+    elif two:  # no group: the sub-groups alone
+        groups = {"gs": np.zeros(1, np.int32), "gp": np.zeros(0, np.int32), "pt": np.zeros((1, 1), np.int32)}
+        gmax, gplen = 0, 0
+    else:  # one level: each prompt's samples a group
+        groups = {"gs": ss, "gp": sh, "pt": np.ascontiguousarray(bt[ss[:-1], : int(sh.max()) // B])}
+        gmax, gplen = plan.samples_per_prompt, int(sh.max())
+    if two:
+        groups.update({"ss": ss, "sh": sh})
     sp_ws = torch.empty(pa._binding.load().pa_shared_prefix_workspace_bytes(pa._binding._c.byref(desc)),
                         dtype=torch.uint8, device=dev)
 
@@ -338,9 +379,11 @@ def build_prefix(args, torch, pa, dev):
         l = i % NL
         out = out if out is not None else outs["out"]
         if shared:
+            sub = dict(subgroup_starts=x["ss"], subgroup_shared_lens=x["sh"],
+                       max_subgroup_size=plan.samples_per_prompt) if two else {}
             pa.paged_attention_decode_shared_prefix(
-                x["q"], kps[l], vps[l], x["bt"], x["ctx"], x["gs"], x["gp"], x["pt"], out, max_group_size=S,
-                max_prefix_len=plan.prefix_len, max_context_len=int(ctx.max()), workspace=sp_ws)
+                x["q"], kps[l], vps[l], x["bt"], x["ctx"], x["gs"], x["gp"], x["pt"], out, max_group_size=gmax,
+                max_prefix_len=gplen, max_context_len=int(ctx.max()), workspace=sp_ws, **sub)
         else:
             pa.paged_attention_decode(x["q"], kps[l], vps[l], x["bt"], x["ctx"], out,
                                       max_context_len=int(ctx.max()), workspace=ws)
@@ -370,13 +413,23 @@ def build_prefix(args, torch, pa, dev):
     dec_unique = kv_unique + 2 * S * Hq * D * 2 + int(((ctx.astype(np.int64) + B - 1) // B).sum()) * 4 + S * 4
     dec_logical = decode_bytes(ctx, Hq, Hkv, D, B)
     copy = len(pairs) * Hkv * B * D * 2 * 2 * 2
-    mode = "shared-prefix decode (prefix attended once on the tensor cores + per-sequence suffix)" if shared \
-        else "plain decode"
+    if plan.prefix_len > 0:
+        mode = ("shared-prefix decode, two levels (prefix attended once on the tensor cores; each prompt's "
+                "suffix blocks once for its samples, each sample's own block for it alone)" if two else
+                "shared-prefix decode (prefix attended once on the tensor cores + per-sequence suffix)" if shared
+                else "plain decode")
+    else:
+        mode = ("sub-group decode (each prompt's blocks read once for its samples, each sample's own block "
+                "for it alone)" if two else
+                "shared-prefix decode, each prompt a group (prompt attended once on the tensor cores)" if shared
+                else "plain decode")
     inputs = {"q": q, "new_k": nk, "new_v": nv, "slots": slots, "pairs": pairs, "bt": bt, "ctx": ctx}
     if shared:
         inputs.update(groups)
-    return Bench("prefix_sharing", f"prefix_sharing: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
-                 f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512], {Hq}q/{Hkv}kv, D={D}, B={B}; "
+    shape = (f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512]" if plan.prefix_len > 0
+             else f"prompts of {int(plan.suffix_lens.min())}..{int(plan.suffix_lens.max())} tokens, no common prefix")
+    return Bench(name, f"{name}: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
+                 f"{shape}, {Hq}q/{Hkv}kv, D={D}, B={B}; "
                  f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + {mode}",
                  inputs, step, dec_unique + copy + cache_bytes(S, Hkv, D), 4 if shared else 3,
                  "shared_prefix_decode" if shared else "decode_kernel", "hbm", dec_unique, S,
@@ -488,6 +541,8 @@ def build_mixed(args, torch, pa, dev):
 def build(args, torch, pa, dev):
     if args.workload == "prefix_sharing":
         return build_prefix(args, torch, pa, dev)
+    if args.workload == "parallel_sampling":
+        return build_prefix(args, torch, pa, dev, wl.parallel_sampling_plan())
     if args.workload == "mixed_step":
         return build_mixed(args, torch, pa, dev)
     case = {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
@@ -773,9 +828,10 @@ def oracle_units(args):
                     return (int(cctx[r]) - 512 + i + 1) * 8 * 128 * 4
                 units.append(u)
         return units, "prefill rows (all 32 heads of one query position)"
-    if args.workload == "prefix_sharing":
+    if args.workload in ("prefix_sharing", "parallel_sampling"):
         import paged_kv_cache_262_gb300 as pa
-        plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa)
+        plan, bt, ctx, slots, pairs = prefix_sharing_setup(
+            pa, wl.parallel_sampling_plan() if args.workload == "parallel_sampling" else None)
         kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
         if len(pairs):
             ora.copy_blocks([kp], [vp], pairs)

@@ -199,6 +199,41 @@ int pa_paged_attention_decode_shared_prefix(const pa_decode_desc *desc, const vo
                                             int max_group_size, int max_prefix_len, void *out, void *workspace,
                                             size_t workspace_bytes, int32_t *err_flag, void *stream);
 
+/* Shared-prefix decode with a second level of sharing [ATT][SHARE]: the
+ * groups of pa_paged_attention_decode_shared_prefix (their prefixes attended
+ * once on the tensor cores), and a partition of all sequences into
+ * consecutive sub-groups whose members share more leading blocks -- the
+ * samples of one prompt under parallel sampling share the prompt's pages,
+ * and only the blocks written since each copy-on-write are their own.
+ * Sub-group k is sequences subgroup_starts[k] .. subgroup_starts[k+1]-1
+ * (subgroup_starts[0] = 0, subgroup_starts[num_subgroups] = num_seqs), whose
+ * block-table rows agree on keys 0 .. subgroup_shared_lens[k]-1 (a multiple
+ * of block_size, at least the prefix length of the group that holds them (0
+ * outside every group), at most each member's context).  Decode runs one unit
+ * per (sub-group, kv head): the sub-group's shared keys past the group prefix
+ * are read once for all of its members' query rows, each member's remaining
+ * keys for that member's rows only, and the group prefix's states are folded
+ * in.  Same result as pa_paged_attention_decode (within rounding).
+ *   subgroup_starts       device int32 [num_subgroups + 1]
+ *   subgroup_shared_lens  device int32 [num_subgroups]
+ *   max_subgroup_size     bound on every sub-group's size; times the GQA group
+ *                         size at most 16
+ * head_dim must be 128; the members of a sub-group must lie in one group (or
+ * in none).  A sub-group with an invalid shared length or a member with a bad
+ * context, or more than 512 blocks to read in all (shared plus every member's
+ * own), gets zero rows and PA_DEVERR_CTX.  num_subgroups == 0 is
+ * pa_paged_attention_decode_shared_prefix.  Other arguments, the workspace
+ * (pa_shared_prefix_workspace_bytes) and errors as there. */
+int pa_paged_attention_decode_shared_prefix2(const pa_decode_desc *desc, const void *q, const void *k_pool,
+                                             const void *v_pool, const int32_t *block_tables,
+                                             const int32_t *context_lens, int num_groups,
+                                             const int32_t *group_starts, const int32_t *group_prefix_lens,
+                                             const int32_t *prefix_tables, int prefix_max_blocks, int max_group_size,
+                                             int max_prefix_len, int num_subgroups, const int32_t *subgroup_starts,
+                                             const int32_t *subgroup_shared_lens, int max_subgroup_size, void *out,
+                                             void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                                             void *stream);
+
 /* Size of the fixed device scratch array of pa_paged_attention_decode_noalloc
  * (8 MiB, held on every GPU that loads the library until the process exits). */
 #define PA_NOALLOC_SCRATCH_BYTES (8u << 20)

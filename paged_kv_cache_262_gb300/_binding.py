@@ -25,7 +25,8 @@ EXPORTS = (
     "pa_version", "pa_status_string", "pa_decode_workspace_bytes", "pa_paged_attention_decode",
     "pa_paged_attention_decode_append", "pa_paged_attention_mixed",
     "pa_paged_attention_decode_noalloc", "pa_paged_attention_prefill_chunk",
-    "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix", "pa_swap_blocks",
+    "pa_shared_prefix_workspace_bytes", "pa_paged_attention_decode_shared_prefix",
+    "pa_paged_attention_decode_shared_prefix2", "pa_swap_blocks",
     "pa_bm_create_with_host", "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_host",
     "pa_bm_add_seq_tokens", "pa_bm_num_cached_blocks", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
@@ -83,6 +84,9 @@ def load(path: Optional[str] = None):
         lib.pa_paged_attention_decode_shared_prefix.restype = i
         lib.pa_paged_attention_decode_shared_prefix.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, i, _P, _P,
                                                                 _P, i, i, i, _P, _P, sz, _P, _P]
+        lib.pa_paged_attention_decode_shared_prefix2.restype = i
+        lib.pa_paged_attention_decode_shared_prefix2.argtypes = [_c.POINTER(DecodeDesc), _P, _P, _P, _P, _P, i, _P, _P,
+                                                                 _P, i, i, i, i, _P, _P, i, _P, _P, sz, _P, _P]
         lib.pa_paged_attention_prefill_chunk.restype = i
         lib.pa_paged_attention_prefill_chunk.argtypes = [_c.POINTER(DecodeDesc), _P, _P, i, i, _P, _P, _P,
                                                          _P, _P, _P, _P]
@@ -270,8 +274,11 @@ _WS_SP = {}
 def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, context_lens, group_starts,
                                          group_prefix_lens, prefix_tables, out=None, *, max_group_size,
                                          max_prefix_len, scale=None, max_context_len=None, workspace=None,
-                                         err_flag=None, stream=None):
-    """Decode with each group's shared prefix attended once (see pagedattn.h)."""
+                                         err_flag=None, stream=None, subgroup_starts=None,
+                                         subgroup_shared_lens=None, max_subgroup_size=0):
+    """Decode with each group's shared prefix attended once; with sub-groups
+    (subgroup_starts / subgroup_shared_lens), a second level of sharing read
+    once per sub-group (see pagedattn.h)."""
     import torch
     for t, n, dt, nd in ((q, "q", torch.bfloat16, 3), (k_pool, "k_pool", torch.bfloat16, 4),
                          (v_pool, "v_pool", torch.bfloat16, 4), (block_tables, "block_tables", torch.int32, 2),
@@ -291,12 +298,23 @@ def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, contex
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
             _WS_SP[key] = workspace
     ng = int(group_prefix_lens.shape[0])
-    st = load().pa_paged_attention_decode_shared_prefix(
+    if subgroup_starts is None:
+        st = load().pa_paged_attention_decode_shared_prefix(
+            _c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), ng,
+            _ptr(group_starts), _ptr(group_prefix_lens), _ptr(prefix_tables), int(prefix_tables.shape[1]),
+            int(max_group_size), int(max_prefix_len), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream_ptr(stream))
+        _check(st, "pa_paged_attention_decode_shared_prefix")
+        return out
+    _need(subgroup_starts, torch.int32, "subgroup_starts", 1)
+    _need(subgroup_shared_lens, torch.int32, "subgroup_shared_lens", 1)
+    st = load().pa_paged_attention_decode_shared_prefix2(
         _c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), ng,
         _ptr(group_starts), _ptr(group_prefix_lens), _ptr(prefix_tables), int(prefix_tables.shape[1]),
-        int(max_group_size), int(max_prefix_len), _ptr(out), _ptr(workspace),
+        int(max_group_size), int(max_prefix_len), int(subgroup_shared_lens.shape[0]), _ptr(subgroup_starts),
+        _ptr(subgroup_shared_lens), int(max_subgroup_size), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream_ptr(stream))
-    _check(st, "pa_paged_attention_decode_shared_prefix")
+    _check(st, "pa_paged_attention_decode_shared_prefix2")
     return out
 
 

@@ -30,6 +30,10 @@
 //  * When the grid fills a few waves of the resident slots, CTAs map to
 //    sequences longest context first (an in-kernel rank over the lengths).
 //  * Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+//  * Sub-group mode (shared-prefix decode, second level): one CTA per
+//    (sub-group, kv head) streams the blocks the members share once for all
+//    of their query rows (member x head as the MMA N side, up to 16), then
+//    each member's own blocks with the other members' columns masked.
 //  * Optionally (decode with append) the CTA that streams a sequence's last
 //    page also stores the step's new token (K/V at position ctx-1) into its
 //    slot of the pools and patches that row of its shared-memory copy of the
@@ -49,17 +53,17 @@
 namespace pa {
 namespace {
 
-template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP>
+template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP, bool GRP>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  decode_unit<D, B, NT, NW, NST, PRE, APP>(&tmK, &tmV, a, lin, threadIdx.x, smem, 0);
+  decode_unit<D, B, NT, NW, NST, PRE, APP, GRP>(&tmK, &tmV, a, lin, threadIdx.x, smem, 0);
 }
 
-template <int D, int B, int NT, bool PRE, bool APP>
+template <int D, int B, int NT, bool PRE, bool APP, bool GRP = false>
 int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                   cudaStream_t st) {
   // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM); 32-token pages:
@@ -69,10 +73,10 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
   // slots with 16-token pages (64 KB, 3 CTAs per SM): more CTAs in flight
   // hide the set-up of short units (prefix sharing: 72.6 -> 61.1 us).
   constexpr int NW = 4;
-  constexpr int NST = (B == 16) ? (PRE ? 2 : 3) : 1;
+  constexpr int NST = (B == 16) ? (PRE || GRP ? 2 : 3) : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
-  auto kern = decode_kernel<D, B, NT, NW, NST, PRE, APP>;
+  auto kern = decode_kernel<D, B, NT, NW, NST, PRE, APP, GRP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   kern<<<grid, NW * 32, L::kAlloc, st>>>(tk, tv, a);
@@ -83,7 +87,12 @@ template <int D, int B>
 int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                 cudaStream_t st) {
   // Separate instances keep the plain decode's registers: the shared-prefix
-  // launch (prefix states prefetched) and the decode with append.
+  // launch (prefix states prefetched), the sub-group launch and the decode
+  // with append.
+  if constexpr (D == 128)
+    if (a.nsub > 0)
+      return a.sub_rows <= 8 ? launch_decode<D, B, 1, false, false, true>(tk, tv, a, grid, st)
+                             : launch_decode<D, B, 2, false, false, true>(tk, tv, a, grid, st);
   if (a.ngroups > 0)
     return G <= 8 ? launch_decode<D, B, 1, true, false>(tk, tv, a, grid, st)
                   : launch_decode<D, B, 2, true, false>(tk, tv, a, grid, st);
@@ -131,12 +140,18 @@ int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, co
   a.pre_o = pre ? pre->pre_o : nullptr;
   a.pre_ml = pre ? pre->pre_ml : nullptr;
   a.npre = pre ? pre->npre : 0;
+  a.sub_start = pre ? pre->sub_start : nullptr;
+  a.sub_shared = pre ? pre->sub_shared : nullptr;
+  a.nsub = pre ? pre->nsub : 0;
+  a.sub_rows = pre ? pre->sub_rows : 0;
+  if (a.nsub > 0 && (d->head_dim != 128 || a.sub_rows > 16 || a.sub_rows <= 0)) return PA_ERR_UNSUPPORTED;
   a.app_k = app ? static_cast<const uint4 *>(app->new_k) : nullptr;
   a.app_v = app ? static_cast<const uint4 *>(app->new_v) : nullptr;
   a.app_slots = app ? app->slots : nullptr;
   a.kp = app ? static_cast<uint4 *>(const_cast<void *>(k_pool)) : nullptr;
   a.vp = app ? static_cast<uint4 *>(const_cast<void *>(v_pool)) : nullptr;
-  const dim3 grid(plan.max_parts, d->num_kv_heads, d->num_seqs);
+  // one CTA per (part, kv head, sequence); sub-groups: per (kv head, sub-group)
+  const dim3 grid(a.nsub > 0 ? 1 : plan.max_parts, d->num_kv_heads, a.nsub > 0 ? a.nsub : d->num_seqs);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d->head_dim == 128)
     return d->block_size == 16 ? dispatch_nt<128, 16>(a.G, tk, tv, a, grid, s)

@@ -47,6 +47,15 @@ struct DecodeArgs {
   const float *pre_o;   // [npre][S][Hq][D] o/l of the prefix's key ranges
   const float *pre_ml;  // [npre][S][Hq][2] (m, l) of the prefix's key ranges
   int npre;
+  // Sub-groups (GRP launches): sequences sub_start[k] .. sub_start[k+1]-1
+  // share keys 0 .. sub_shared[k]-1 (whole blocks; the first grp_prefix of
+  // them attended by the prefix pass).  One unit per (sub-group, kv head)
+  // attends the shared keys once for all members' query rows and each
+  // member's own keys for its rows only.
+  const int32_t *sub_start;
+  const int32_t *sub_shared;
+  int nsub;
+  int sub_rows;  // bound on a sub-group's query rows (members x G)
   // Append (optional): app_k/app_v [S][Hkv][D] hold each sequence's newest
   // token, which belongs at position ctx-1 in slot app_slots[s] (< 0: none).
   const uint4 *app_k;
@@ -86,7 +95,8 @@ struct DecodeSmem {
   static constexpr int kMiscOff = kTblOff + kMaxPartPages * 4;
   // misc: [0..3] broadcast words, [4..7] warp totals, [8..135] length histogram
   static constexpr int kStageOff = kMiscOff + 4 * 136;  // appended token's K then V row
-  static constexpr int kBytes = kStageOff + 2 * D * 2;
+  static constexpr int kMetaOff = kStageOff + 2 * D * 2;  // GRP: per page, owner + 1 << 24 | logical block
+  static constexpr int kBytes = kMetaOff + kMaxPartPages * 4;
   static constexpr int kAlloc = kBytes + 1024;  // base re-aligned to 1024 in the kernel
 };
 
@@ -165,7 +175,7 @@ __device__ int seq_of_rank(int r, const int32_t *ctx, int S, int B, int max_bloc
 // unit's shared memory at `smem` (1024-aligned, DecodeSmem<...>::kBytes) and
 // barrier `bar` for its own NW * 32 threads.  The decode kernel runs one unit
 // per CTA; the mixed-step kernel runs several side by side in one CTA.
-template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP>
+template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP, bool GRP = false>
 __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeArgs &a,
                                             int lin, int tid, uint8_t *smem, int bar) {
   using L = DecodeSmem<D, B, NW, NST>;
@@ -174,23 +184,36 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   constexpr int MT = B / 16;  // 16-token tiles per page
   constexpr int DT = D / 16;  // 16-row d tiles of O^T = V^T P^T
 
+  constexpr bool FOLD = PRE || GRP;  // shared-prefix states to fold in at the end
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kBarOff);
   int32_t *tbl = reinterpret_cast<int32_t *>(smem + L::kTblOff);
   int *misc = reinterpret_cast<int *>(smem + L::kMiscOff);
+  int32_t *meta = reinterpret_cast<int32_t *>(smem + L::kMetaOff);
 
   // Units are dispatched in linear order; map that order to (sequence rank,
-  // part, kv head), ranks longest context first when a.lpt is set.
+  // part, kv head), ranks longest context first when a.lpt is set.  GRP: to
+  // (sub-group rank, kv head), sub-groups ranked by their shared length when
+  // a.lpt is set; s is the sub-group's first member.
   const int per_seq = a.max_parts * a.Hkv;
-  const int rank = lin / per_seq;
-  const int part = (lin - rank * per_seq) / a.Hkv;
-  const int kvh = lin - rank * per_seq - part * a.Hkv;
-  const int s = (a.lpt && a.S > 1) ? seq_of_rank<NW * 32>(rank, a.ctx, a.S, B, a.max_blocks, a.max_ctx, misc, tid, bar)
-                                   : rank;
+  const int rank = GRP ? lin / a.Hkv : lin / per_seq;
+  const int part = GRP ? 0 : (lin - rank * per_seq) / a.Hkv;
+  const int kvh = GRP ? lin - rank * a.Hkv : lin - rank * per_seq - part * a.Hkv;
+  const bool rank_it = a.lpt && (GRP ? a.nsub : a.S) > 1;
+  const int sg = GRP && rank_it
+                     ? seq_of_rank<NW * 32>(rank, a.sub_shared, a.nsub, B, a.max_blocks, a.max_ctx, misc, tid, bar)
+                     : rank;  // GRP: the sub-group
+  const int s = GRP ? __ldg(a.sub_start + sg)
+                    : rank_it ? seq_of_rank<NW * 32>(rank, a.ctx, a.S, B, a.max_blocks, a.max_ctx, misc, tid, bar)
+                              : rank;
+  const int nm = GRP ? __ldg(a.sub_start + sg + 1) - s : 1;  // members (query-row groups) of the unit
   const int warp = tid >> 5, lane = tid & 31;
   const int G = a.G;
-  const int ctx = __ldg(a.ctx + s);
-  int kstart = 0;  // first key this kernel covers (end of a shared prefix; PRE launches only)
-  if (PRE && a.ngroups > 0 && s >= __ldg(a.grp_start) && s < __ldg(a.grp_start + a.ngroups)) {
+  const int ncols = nm * G;  // query rows of the unit: member g / G, head g % G
+  // GRP: a sub-group outside the batch is refused before anything is read
+  const bool in_range = !GRP || (s >= 0 && nm > 0 && s + nm <= a.S);
+  const int ctx = in_range ? __ldg(a.ctx + s) : 0;
+  int kstart = 0;  // first key this kernel covers (end of a shared prefix; PRE and GRP launches only)
+  if (FOLD && a.ngroups > 0 && s >= __ldg(a.grp_start) && s < __ldg(a.grp_start + a.ngroups)) {
     int lo = 0, hi = a.ngroups;  // grp_start[lo] <= s < grp_start[hi]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -200,25 +223,71 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     kstart = __ldg(a.grp_prefix + lo);
   }
   const bool has_pre = kstart > 0;
-  const bool bad = ctx <= 0 || ctx > a.max_blocks * B || ctx > a.max_ctx || kstart < 0 || kstart > ctx ||
-                   kstart % B != 0;
+  // query row g of the unit: (sequence, head) -> row of q / out / the prefix states
+  auto row_of = [&](int g) -> size_t {
+    return GRP ? (size_t)(s + g / G) * a.Hq + (size_t)kvh * G + g % G : (size_t)s * a.Hq + (size_t)kvh * G + g;
+  };
+  int kshared = 0;  // GRP: end of the keys every member shares
+  bool bad_grp = false;
+  int npages_grp = 0;
+  if constexpr (GRP) {
+    // members' contexts in misc[8 ..], the start of each member's own pages
+    // in the unit's page list in misc[24 ..] (the shared pages come first)
+    kshared = __ldg(a.sub_shared + sg);
+    if (in_range && tid < nm && tid < 16) misc[8 + tid] = __ldg(a.ctx + s + tid);
+    unit_sync<NW * 32>(bar);
+    if (tid == 0) {
+      int ok = in_range && ncols <= NT * 8 && kshared >= kstart && kshared % B == 0 && kstart % B == 0;
+      int at = ok ? (kshared - kstart) / B : 0;
+      for (int m = 0; ok && m < nm; ++m) {
+        const int c = misc[8 + m];
+        ok = c >= kshared && c > 0 && c <= a.max_blocks * B && c <= a.max_ctx;
+        misc[24 + m] = at;
+        at += (c + B - 1) / B - kshared / B;
+      }
+      if (ok) misc[24 + nm] = at;
+      misc[0] = ok && at <= kMaxPartPages;
+    }
+    unit_sync<NW * 32>(bar);
+    bad_grp = !misc[0];
+    npages_grp = bad_grp ? 0 : misc[24 + nm];
+  }
+  const bool bad = GRP ? bad_grp
+                       : ctx <= 0 || ctx > a.max_blocks * B || ctx > a.max_ctx || kstart < 0 || kstart > ctx ||
+                             kstart % B != 0;
+  const int npages = GRP ? npages_grp : bad ? 0 : (ctx + B - 1) / B - kstart / B;
   const int kp0 = bad ? 0 : kstart / B;  // first page of this kernel's key range
-  const int npages = bad ? 0 : (ctx + B - 1) / B - kp0;
-  const int nparts = bad ? 1 : max(1, (npages + a.part_pages - 1) / a.part_pages);
+  const int nparts = (bad || GRP) ? 1 : max(1, (npages + a.part_pages - 1) / a.part_pages);
   if (part >= nparts) return;
   __nv_bfloat16 *out_base = a.out + ((size_t)s * a.Hq + (size_t)kvh * G) * D;
   if (bad) {
-    for (int i = tid; i < G * D; i += NW * 32) out_base[i] = __float2bfloat16(0.f);
+    if (GRP) {
+      if (in_range)
+        for (int i = tid; i < ncols * D; i += NW * 32) a.out[row_of(i / D) * D + i % D] = __float2bfloat16(0.f);
+    } else
+      for (int i = tid; i < G * D; i += NW * 32) out_base[i] = __float2bfloat16(0.f);
     if (tid == 0 && a.err) atomicOr(a.err, PA_DEVERR_CTX);
     return;
   }
 
   // ---- stage this part's block-table entries; init this warp's barriers
   const int p0 = part * a.part_pages;
-  const int np = max(0, min(npages - p0, a.part_pages));
+  const int np = GRP ? npages : max(0, min(npages - p0, a.part_pages));  // GRP units are never split
   const int32_t *bt_row = a.bt + (size_t)s * a.max_blocks + kp0 + p0;
   for (int i = tid; i < np; i += NW * 32) {
-    int pg = __ldg(bt_row + i);
+    int pg;
+    if constexpr (GRP) {  // shared pages from the first member's row, then each member's own
+      int m = -1, lb = kp0 + i;
+      if (i >= misc[24]) {
+        m = 0;
+        while (m + 1 < nm && i >= misc[24 + m + 1]) ++m;
+        lb = kshared / B + (i - misc[24 + m]);
+      }
+      pg = __ldg(a.bt + (size_t)(s + max(m, 0)) * a.max_blocks + lb);
+      meta[i] = ((m + 1) << 24) | lb;
+    } else {
+      pg = __ldg(bt_row + i);
+    }
     if (pg < 0 || pg >= a.num_blocks) {
       if (a.err) atomicOr(a.err, PA_DEVERR_PAGE);
       pg = -1;
@@ -279,12 +348,13 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
     const int g = nt * 8 + (lane >> 2);
+    const __nv_bfloat16 *qg = GRP ? a.q + row_of(g) * D : qb + (size_t)g * D;
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
       const int d0 = kk * 16 + 2 * (lane & 3);
-      if (g < G) {
-        qf[nt][kk][0] = __ldg(reinterpret_cast<const uint32_t *>(qb + (size_t)g * D + d0));
-        qf[nt][kk][1] = __ldg(reinterpret_cast<const uint32_t *>(qb + (size_t)g * D + d0 + 8));
+      if (g < (GRP ? ncols : G)) {
+        qf[nt][kk][0] = __ldg(reinterpret_cast<const uint32_t *>(qg + d0));
+        qf[nt][kk][1] = __ldg(reinterpret_cast<const uint32_t *>(qg + d0 + 8));
       } else {
         qf[nt][kk][0] = qf[nt][kk][1] = 0u;
       }
@@ -309,7 +379,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   // under the streaming (thread tid: output elements tid + j NW 32, and the
   // (m, l) of head tid), when a thread's share is small enough for registers.
   constexpr int kPreElems = 4;
-  const int npre = (PRE && has_pre && nparts == 1) ? a.npre : 0;
+  const int npre = (FOLD && has_pre && nparts == 1) ? a.npre : 0;
   // (PRE: the shared-prefix launch; groups of more than 8 heads never qualify)
   const bool pre_early = PRE && NT == 1 && npre > 0 && G * D <= kPreElems * NW * 32;
   const size_t slab = (size_t)a.S * a.Hq;
@@ -355,7 +425,14 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     if (tbl[lp] >= 0) {
       const uint32_t kb = smem_u32(ring + stg * L::kSlotBytes);
       const uint32_t vb = kb + L::kPageBytes;
-      const int tok0 = (kp0 + p0 + lp) * B;
+      // the page's first token; GRP: and its owner (-1: shared by every member) with that member's context
+      int tok0 = (kp0 + p0 + lp) * B, owner = -1, octx = ctx;
+      if constexpr (GRP) {
+        const int mt_ = meta[lp];
+        tok0 = (mt_ & 0xffffff) * B;
+        owner = (mt_ >> 24) - 1;
+        octx = owner >= 0 ? misc[8 + owner] : kshared;
+      }
       if (APP && app_row >= 0 && lp == np - 1) {
         // The gather may have seen the slot before or after the store above:
         // overwrite the row with the staged copy (each lane its own chunks).
@@ -392,14 +469,17 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         float t0 = -INFINITY, t1 = -INFINITY;
+        // GRP: a member's own page counts only for its columns
+        const bool own0 = !GRP || owner < 0 || (nt * 8 + 2 * (lane & 3)) / G == owner;
+        const bool own1 = !GRP || owner < 0 || (nt * 8 + 2 * (lane & 3) + 1) / G == owner;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
           const int j = tok0 + mt * 16 + (lane >> 2);
-          const bool v0 = j < ctx, v1 = j + 8 < ctx;
-          sc[mt][nt][0] = v0 ? sc[mt][nt][0] * a.scale_log2 : -INFINITY;
-          sc[mt][nt][1] = v0 ? sc[mt][nt][1] * a.scale_log2 : -INFINITY;
-          sc[mt][nt][2] = v1 ? sc[mt][nt][2] * a.scale_log2 : -INFINITY;
-          sc[mt][nt][3] = v1 ? sc[mt][nt][3] * a.scale_log2 : -INFINITY;
+          const bool v0 = j < octx, v1 = j + 8 < octx;
+          sc[mt][nt][0] = v0 && own0 ? sc[mt][nt][0] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][1] = v0 && own1 ? sc[mt][nt][1] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][2] = v1 && own0 ? sc[mt][nt][2] * a.scale_log2 : -INFINITY;
+          sc[mt][nt][3] = v1 && own1 ? sc[mt][nt][3] * a.scale_log2 : -INFINITY;
           t0 = fmaxf(t0, fmaxf(sc[mt][nt][0], sc[mt][nt][2]));
           t1 = fmaxf(t1, fmaxf(sc[mt][nt][1], sc[mt][nt][3]));
         }
@@ -409,7 +489,10 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
           t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
         }
         const float mn0 = fmaxf(m_run[nt][0], t0), mn1 = fmaxf(m_run[nt][1], t1);
-        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        // GRP: a column may have seen only other members' pages so far (max
+        // still -inf): rescale against 0 there, so no -inf - -inf appears
+        const float su0 = GRP && mn0 == -INFINITY ? 0.f : mn0, su1 = GRP && mn1 == -INFINITY ? 0.f : mn1;
+        const float al0 = exp2f(m_run[nt][0] - su0), al1 = exp2f(m_run[nt][1] - su1);
         m_run[nt][0] = mn0;
         m_run[nt][1] = mn1;
         l_run[nt][0] *= al0;
@@ -426,9 +509,9 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
       // Value rows past the context (the tail of the last page) may hold
       // anything a slot was never written with, NaN included, and 0 * NaN
       // would reach the output: clear them before the product.
-      if (tok0 + B > ctx) {
+      if (tok0 + B > octx) {
         uint8_t *vslot = ring + stg * L::kSlotBytes + L::kPageBytes;
-        const int r0 = ctx - tok0;
+        const int r0 = octx - tok0;
         for (int idx = lane; idx < (B - r0) * L::kHalves * 8; idx += 32) {
           const int row = r0 + idx / (L::kHalves * 8), rem = idx % (L::kHalves * 8);
           *reinterpret_cast<uint4 *>(vslot + (rem >> 3) * L::kBoxBytes + row * 128 + (rem & 7) * 16) =
@@ -444,10 +527,10 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint32_t lo = pack_bf16(exp2f(sc[mt][nt][0] - m_run[nt][0]),
-                                        exp2f(sc[mt][nt][1] - m_run[nt][1]));
-          const uint32_t hi = pack_bf16(exp2f(sc[mt][nt][2] - m_run[nt][0]),
-                                        exp2f(sc[mt][nt][3] - m_run[nt][1]));
+          const float e0 = GRP && m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+          const float e1 = GRP && m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
+          const uint32_t lo = pack_bf16(exp2f(sc[mt][nt][0] - e0), exp2f(sc[mt][nt][1] - e1));
+          const uint32_t hi = pack_bf16(exp2f(sc[mt][nt][2] - e0), exp2f(sc[mt][nt][3] - e1));
           l_run[nt][0] += bf16_lo(lo) + bf16_lo(hi);
           l_run[nt][1] += bf16_hi(lo) + bf16_hi(hi);
           pb[nt][0] = movmatrix_t(lo);
@@ -517,9 +600,9 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   // output element only adds up its prefix states (loads issued together).
   float *coef = wts;  // [0..15] this CTA's sum, [16 (p + 1) + g] prefix state p
   if (npre > 0) {
-    if (tid < G) {
+    if (tid < ncols) {
       const int g = tid;
-      const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
+      const size_t row = row_of(g);
       float mx = -INFINITY, l = 0.f;
 #pragma unroll
       for (int w = 0; w < NW; ++w) mx = fmaxf(mx, red_m[w * 16 + g]);
@@ -551,7 +634,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     }
     unit_sync<NW * 32>(bar);
   }
-  for (int idx = tid, j = 0; idx < G * D; idx += NW * 32, ++j) {
+  for (int idx = tid, j = 0; idx < ncols * D; idx += NW * 32, ++j) {
     const int g = idx / D, d = idx - g * D;
     float mx = -INFINITY;
 #pragma unroll
@@ -568,7 +651,7 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     if (!split) {
       float res;
       if (npre > 0) {  // fold in the shared prefix's partial states
-        const size_t row = (size_t)s * a.Hq + (size_t)kvh * G + g;
+        const size_t row = row_of(g);
         float po[kMaxPrefixParts];
         if (pre_early) {
 #pragma unroll
@@ -586,7 +669,10 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
       } else {
         res = l > 0.f ? acc / l : 0.f;
       }
-      out_base[idx] = __float2bfloat16(res);
+      if (GRP)
+        a.out[row_of(g) * D + d] = __float2bfloat16(res);
+      else
+        out_base[idx] = __float2bfloat16(res);
     } else {
       const size_t u = (unit * a.max_parts + part) * G + g;
       a.ws_o[u * D + d] = l > 0.f ? acc / l : 0.f;

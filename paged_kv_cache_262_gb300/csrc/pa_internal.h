@@ -56,6 +56,13 @@ struct DecodePrefix {
   const float *pre_o;         // device [npre][S][Hq][D]
   const float *pre_ml;        // device [npre][S][Hq][2]
   int npre;                   // partial states per row (key ranges of the prefix)
+  // Sub-groups (optional, nsub > 0): sequences sub_start[k] .. sub_start[k+1]-1
+  // share keys 0 .. sub_shared[k]-1; one decode unit per (sub-group, kv head)
+  // covering at most sub_rows query rows (member x head).
+  const int32_t *sub_start;   // device [nsub + 1], a partition of 0 .. S-1
+  const int32_t *sub_shared;  // device [nsub], tokens, multiples of B
+  int nsub;
+  int sub_rows;
 };
 
 // The newest token of every sequence, appended by the decode launch itself

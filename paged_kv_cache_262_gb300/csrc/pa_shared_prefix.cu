@@ -12,6 +12,10 @@
 // states (m, l, o/l) exactly as split-K parts are merged.  When the groups
 // alone would not fill the GPU, the prefix is cut into up to 8 key ranges of
 // whole 128-key tiles, each attended by its own CTAs into its own state.
+// A second level (pa_paged_attention_decode_shared_prefix2): sub-groups of
+// consecutive sequences that share more leading blocks -- the samples of one
+// prompt -- are decoded as one unit per (sub-group, kv head), reading those
+// blocks once for all members (the sub-group mode of the decode unit).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -43,19 +47,36 @@ extern "C" size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc) {
   return layout(desc).total();
 }
 
-extern "C" int pa_paged_attention_decode_shared_prefix(
-    const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_tables,
-    const int32_t *context_lens, int num_groups, const int32_t *group_starts, const int32_t *group_prefix_lens,
-    const int32_t *prefix_tables, int prefix_max_blocks, int max_group_size, int max_prefix_len, void *out,
-    void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+namespace {
+
+// Both entry points: groups (one level), and optionally sub-groups (a second).
+int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
+                  const int32_t *block_tables, const int32_t *context_lens, int num_groups,
+                  const int32_t *group_starts, const int32_t *group_prefix_lens, const int32_t *prefix_tables,
+                  int prefix_max_blocks, int max_group_size, int max_prefix_len, int num_subgroups,
+                  const int32_t *subgroup_starts, const int32_t *subgroup_shared_lens, int max_subgroup_size,
+                  void *out, void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
   using namespace pa;
   int st = validate_decode_desc(d);
   if (st != PA_OK) return st;
-  if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0 || prefix_max_blocks < 0) return PA_ERR_INVALID;
+  if (num_groups < 0 || max_group_size < 0 || max_prefix_len < 0 || prefix_max_blocks < 0 || num_subgroups < 0 ||
+      max_subgroup_size < 0)
+    return PA_ERR_INVALID;
   if (d->num_seqs == 0) return PA_OK;
+  const int G = d->num_q_heads / d->num_kv_heads;
+  DecodePrefix sub{};  // the sub-group partition (the prefix states are filled in below)
+  if (num_subgroups > 0) {
+    if (!subgroup_starts || !subgroup_shared_lens || max_subgroup_size == 0) return PA_ERR_INVALID;
+    if (d->head_dim != 128 || (long long)max_subgroup_size * G > 16) return PA_ERR_UNSUPPORTED;
+    if (num_subgroups > 65535) return PA_ERR_UNSUPPORTED;
+    sub.sub_start = subgroup_starts;
+    sub.sub_shared = subgroup_shared_lens;
+    sub.nsub = num_subgroups;
+    sub.sub_rows = max_subgroup_size * G;
+  }
   if (num_groups == 0)
     return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes, err_flag,
-                         stream, nullptr);
+                         stream, num_subgroups > 0 ? &sub : nullptr);
   if (!group_starts || !group_prefix_lens || !prefix_tables || prefix_max_blocks == 0 || max_group_size == 0 ||
       max_prefix_len == 0)
     return PA_ERR_INVALID;
@@ -68,7 +89,6 @@ extern "C" int pa_paged_attention_decode_shared_prefix(
   float *pre_ml = reinterpret_cast<float *>(ws + l.decode + l.pre_o);
   // 1. each group's shared prefix, all of its rows at once, on the tensor cores;
   //    key ranges so that the pass has about one CTA per SM
-  const int G = d->num_q_heads / d->num_kv_heads;
   const long long base = (long long)num_groups * d->num_kv_heads * (((long long)max_group_size * G + 255) / 256);
   const int sms = std::max(current_sm_count(), 1);
   int kparts = (int)std::min<long long>(kMaxPrefixParts, std::max<long long>(1, (sms + base - 1) / base));
@@ -83,7 +103,37 @@ extern "C" int pa_paged_attention_decode_shared_prefix(
                       group_prefix_lens, nullptr, pre_o, pre_ml, /*causal=*/0, kparts, kparts > 1 ? kpart_len : 0,
                       err_flag, stream);
   if (st != PA_OK) return st;
-  // 2. every sequence's own keys, merged with its group's prefix states
-  const DecodePrefix pre{group_starts, group_prefix_lens, num_groups, pre_o, pre_ml, kparts};
+  // 2. every sequence's own keys (or every sub-group's), merged with its group's prefix states
+  DecodePrefix pre = sub;
+  pre.grp_start = group_starts;
+  pre.grp_prefix = group_prefix_lens;
+  pre.ngroups = num_groups;
+  pre.pre_o = pre_o;
+  pre.pre_ml = pre_ml;
+  pre.npre = kparts;
   return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, ws, l.decode, err_flag, stream, &pre);
+}
+
+}  // namespace
+
+extern "C" int pa_paged_attention_decode_shared_prefix(
+    const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_tables,
+    const int32_t *context_lens, int num_groups, const int32_t *group_starts, const int32_t *group_prefix_lens,
+    const int32_t *prefix_tables, int prefix_max_blocks, int max_group_size, int max_prefix_len, void *out,
+    void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  return shared_prefix(d, q, k_pool, v_pool, block_tables, context_lens, num_groups, group_starts, group_prefix_lens,
+                       prefix_tables, prefix_max_blocks, max_group_size, max_prefix_len, 0, nullptr, nullptr, 0, out,
+                       workspace, workspace_bytes, err_flag, stream);
+}
+
+extern "C" int pa_paged_attention_decode_shared_prefix2(
+    const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool, const int32_t *block_tables,
+    const int32_t *context_lens, int num_groups, const int32_t *group_starts, const int32_t *group_prefix_lens,
+    const int32_t *prefix_tables, int prefix_max_blocks, int max_group_size, int max_prefix_len, int num_subgroups,
+    const int32_t *subgroup_starts, const int32_t *subgroup_shared_lens, int max_subgroup_size, void *out,
+    void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream) {
+  return shared_prefix(d, q, k_pool, v_pool, block_tables, context_lens, num_groups, group_starts, group_prefix_lens,
+                       prefix_tables, prefix_max_blocks, max_group_size, max_prefix_len, num_subgroups,
+                       subgroup_starts, subgroup_shared_lens, max_subgroup_size, out, workspace, workspace_bytes,
+                       err_flag, stream);
 }

@@ -9,7 +9,7 @@ import pytest
 
 import paged_kv_cache_262_gb300 as pa
 import workloads as wl
-from gpu_util import assert_close, bf16_dev, bf16_host, need_gpu
+from gpu_util import assert_close, bf16_dev, bf16_host, need_gpu, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -167,3 +167,180 @@ def test_shared_prefix_graph_replay(torch, monkeypatch, pp):
         g.replay()
         torch.cuda.synchronize()
         assert np.array_equal(bf16_host(out), want)
+
+
+def nested_case(Hq, Hkv, D, B, spec, seed):
+    """Two levels of sharing.  spec: list of (prefix_blocks or None, subgroups)
+    where subgroups is a list of (extra_shared_blocks, [own tokens per
+    member]); prefix None = sub-groups outside every group.  Members of a
+    sub-group share the group prefix plus its extra blocks, then have their own
+    blocks.  Returns the case, the group arrays and the sub-group arrays."""
+    st = wl.Stream(seed, 41)
+    rows, ctx, gstart, gpref, ptabs, sstart, sshared = [], [], [], [], [], [0], []
+    nblk, gend = 0, 0
+    for pblocks, subs in spec:
+        prefix = list(range(nblk, nblk + (pblocks or 0)))
+        nblk += len(prefix)
+        first = len(rows)
+        for extra, owns in subs:
+            shared = prefix + list(range(nblk, nblk + extra))
+            nblk += extra
+            for own in owns:
+                n = len(shared) * B + own
+                k = (n + B - 1) // B - len(shared)
+                rows.append(shared + list(range(nblk, nblk + k)))
+                nblk += k
+                ctx.append(n)
+            sstart.append(len(rows))
+            sshared.append(len(shared) * B)
+        if pblocks:
+            gstart.append(first)
+            gpref.append(pblocks * B)
+            ptabs.append(prefix)
+            gend = len(rows)
+    if gpref:  # grouped entries come first, consecutive
+        gstart.append(gend)
+    nblk += 5
+    perm = st.permutation(nblk).astype(np.int32)
+    mb = max(len(r) for r in rows)
+    bt = np.full((len(rows), mb), -1, np.int32)
+    for i, r in enumerate(rows):
+        bt[i, : len(r)] = perm[r]
+    S = len(rows)
+    case = wl.DecodeCase("nested", S, Hq, Hkv, D, B, nblk, mb, 1.0 / math.sqrt(D), np.array(ctx, np.int32), bt,
+                         wl.normal_bf16(st, (S, Hq, D)), wl.normal_bf16(st, (nblk, Hkv, B, D)),
+                         wl.normal_bf16(st, (nblk, Hkv, B, D)))
+    if gpref:
+        pmb = max(len(p) for p in ptabs)
+        pt = np.full((len(ptabs), pmb), -1, np.int32)
+        for i, p in enumerate(ptabs):
+            pt[i, : len(p)] = perm[p]
+    else:
+        pt = np.zeros((1, 1), np.int32)
+    return (case, np.array(gstart, np.int32), np.array(gpref, np.int32), pt, np.array(sstart, np.int32),
+            np.array(sshared, np.int32))
+
+
+def nested_inputs(torch, case, gs, gp, pt, ss, sh):
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    ng = len(gp)
+    return dict(q=bf16_dev(case.q, torch), kp=bf16_dev(case.k_pool, torch), vp=bf16_dev(case.v_pool, torch),
+                bt=dev(case.block_tables), ctx=dev(case.context_lens), gs=dev(gs if ng else np.zeros(1, np.int32)),
+                gp=dev(gp if ng else np.zeros(0, np.int32)), pt=dev(pt), ss=dev(ss), sh=dev(sh),
+                kw=dict(max_group_size=int(np.diff(gs).max()) if ng else 0,
+                        max_prefix_len=int(gp.max()) if ng else 0, scale=case.scale,
+                        max_context_len=case.max_context_len, max_subgroup_size=int(np.diff(ss).max())))
+
+
+def launch_nested(x, err=None, out=None, workspace=None):
+    return pa.paged_attention_decode_shared_prefix(
+        x["q"], x["kp"], x["vp"], x["bt"], x["ctx"], x["gs"], x["gp"], x["pt"], out, err_flag=err,
+        subgroup_starts=x["ss"], subgroup_shared_lens=x["sh"], workspace=workspace, **x["kw"])
+
+
+def run_nested(torch, case, gs, gp, pt, ss, sh, err):
+    res = launch_nested(nested_inputs(torch, case, gs, gp, pt, ss, sh), err)
+    torch.cuda.synchronize()
+    return bf16_host(res)
+
+
+NESTED = {
+    # G = 4: sub-groups of up to 4 members (16 query rows); one member ends where its sub-group's sharing ends
+    (32, 8, 128, 16): [(4, [(3, [1, 9, 16, 0]), (0, [5, 30]), (2, [17])]), (10, [(1, [3, 3, 40])]),
+                       (None, [(2, [4, 7]), (0, [100])])],
+    (64, 8, 128, 32): [(3, [(2, [5, 40]), (1, [1])]), (None, [(0, [70]), (1, [2, 33])])],
+    # G = 1: sixteen members in one sub-group
+    (16, 16, 128, 16): [(2, [(1, list(range(1, 17))), (0, [20])])],
+    # G = 16: one member per sub-group
+    (32, 2, 128, 16): [(5, [(2, [9]), (0, [1]), (3, [0])])],
+}
+
+
+@pytest.mark.parametrize("shape", list(NESTED), ids=lambda s: "q%dkv%dd%db%d" % s)
+@pytest.mark.parametrize("pp", [None, 2])
+def test_subgroups_against_oracle(torch, ora, monkeypatch, shape, pp):
+    if pp is None:
+        monkeypatch.delenv("PA_PARTITION_PAGES", raising=False)
+    else:
+        monkeypatch.setenv("PA_PARTITION_PAGES", str(pp))  # the group prefix pass splits; sub-groups do not
+    Hq, Hkv, D, B = shape
+    case, gs, gp, pt, ss, sh = nested_case(Hq, Hkv, D, B, NESTED[shape], seed=sum(shape))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_nested(torch, case, gs, gp, pt, ss, sh, err)
+    assert int(err.item()) == 0
+    ref, st = ora.decode_case(case)
+    assert np.all(st == 0)
+    assert_close(got, ref, f"sub-groups {shape} pp={pp}")
+
+
+def test_subgroup_bad_shared_length_flagged(torch):
+    spec = [(4, [(2, [3, 5]), (1, [8, 9])])]
+    case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, spec, seed=3)
+    sh = sh.copy()
+    sh[0] += 5  # not a whole number of blocks
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_nested(torch, case, gs, gp, pt, ss, sh, err)
+    assert int(err.item()) & pa.DEVERR_CTX
+    assert not np.any(got[:2])  # the bad sub-group's members: zeros
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    plain = pa.paged_attention_decode(bf16_dev(case.q, torch), bf16_dev(case.k_pool, torch),
+                                      bf16_dev(case.v_pool, torch), dev(case.block_tables), dev(case.context_lens),
+                                      scale=case.scale, max_context_len=case.max_context_len)
+    torch.cuda.synchronize()
+    assert_close(got[2:], to_f64(bf16_host(plain)[2:]), "the other sub-group")
+
+
+def test_subgroups_graph_replay(torch):
+    case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, NESTED[(32, 8, 128, 16)], seed=7)
+    x = nested_inputs(torch, case, gs, gp, pt, ss, sh)
+    want = bf16_host(launch_nested(x))
+    torch.cuda.synchronize()
+    out = torch.empty_like(x["q"])
+    desc = pa.make_desc(x["q"], x["kp"], x["bt"], scale=case.scale, max_context_len=case.max_context_len)
+    import ctypes
+    ws = torch.empty(int(pa.load().pa_shared_prefix_workspace_bytes(ctypes.byref(desc))), dtype=torch.uint8,
+                     device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(2):
+            launch_nested(x, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(bf16_host(out), want)
+
+
+@pytest.mark.parametrize("which", ["prefix_sharing", "parallel_sampling"])
+def test_subgroups_prefix_sharing_workload(torch, ora, which):
+    """The prefix-sharing workload with its second level (the 4 samples of each
+    prompt share the prompt's full suffix blocks), and the parallel-sampling
+    workload (no common prefix, sub-groups only) -- bench --workload ..."""
+    import bench
+    plan, bt, ctx, slots, pairs = bench.prefix_sharing_setup(
+        pa, wl.parallel_sampling_plan() if which == "parallel_sampling" else None)
+    kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
+    if len(pairs):
+        assert ora.copy_blocks([kp], [vp], pairs) == 0
+    assert ora.reshape_and_cache(nk, nv, kp, vp, slots) == 0
+    S, B = len(ctx), plan.B
+    ss, sh = bench.prefix_sharing_subgroups(plan, bt, ctx)
+    for k in range(len(sh)):  # members agree on their shared blocks
+        a, b = ss[k], ss[k + 1]
+        assert np.all(bt[a:b, : sh[k] // B] == bt[a, : sh[k] // B])
+    case = wl.DecodeCase("prefix", S, plan.Hq, plan.Hkv, plan.D, B, plan.num_blocks, bt.shape[1],
+                         1 / math.sqrt(plan.D), ctx, bt, q, kp, vp)
+    npre = plan.prefix_len // B
+    if npre:
+        gs, gp, pt = np.array([0, S], np.int32), np.array([plan.prefix_len], np.int32), bt[:1, :npre].copy()
+    else:
+        gs, gp, pt = np.zeros(1, np.int32), np.zeros(0, np.int32), np.zeros((1, 1), np.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_nested(torch, case, gs, gp, pt, ss, sh, err)
+    assert int(err.item()) == 0
+    heads = [(s, h) for s in range(0, S, 7) for h in (0, 13, 31)]
+    ref = ora.decode_case(case, heads=heads)
+    assert_close(np.stack([got[s, h] for s, h in heads]), ref, f"{which}, sub-groups")

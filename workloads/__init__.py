@@ -303,6 +303,18 @@ def prefix_sharing_plan(seed: int = 0, num_prompts: int = 64, samples: int = 4,
                              independent_suffixes)
 
 
+def parallel_sampling_plan(seed: int = 0, num_prompts: int = 64, samples: int = 4, lo: int = 1024,
+                           hi: int = 4096) -> PrefixSharingPlan:
+    """64 prompts of U[lo, hi] tokens, 4 samples each and no prefix common to
+    all prompts: the samples of a prompt share the prompt's blocks."""
+    st = Stream(seed, 7)
+    suf = st.integers(lo, hi, num_prompts)
+    B = 16
+    pages = int(sum((int(s) + B) // B + 1 for s in suf)) + num_prompts * samples * 2
+    nblk = int(math.ceil(1.25 * pages))
+    return PrefixSharingPlan(num_prompts, samples, 0, suf, 32, 8, 128, B, nblk, seed, False)
+
+
 def prefix_sharing_values(plan: PrefixSharingPlan):
     """Pool contents, per-sequence queries and new tokens for the plan."""
     st = Stream(plan.seed, 104)
