@@ -30,6 +30,9 @@
 //  * When the grid fills a few waves of the resident slots, CTAs map to
 //    sequences longest context first (an in-kernel rank over the lengths).
 //  * Every mbarrier wait is bounded; a timeout sets PA_DEVERR_TIMEOUT.
+//  * Shared-prefix launches: a sequence in a group starts at the end of the
+//    group's prefix, whose partial softmax states a tensor-core pass wrote
+//    before; they are loaded before streaming and folded in at the end.
 //  * Sub-group mode (shared-prefix decode, second level): one CTA per
 //    (sub-group, kv head) streams the blocks the members share once for all
 //    of their query rows (member x head as the MMA N side, up to 16), then
