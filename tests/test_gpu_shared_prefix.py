@@ -344,3 +344,38 @@ def test_subgroups_prefix_sharing_workload(torch, ora, which):
     heads = [(s, h) for s in range(0, S, 7) for h in (0, 13, 31)]
     ref = ora.decode_case(case, heads=heads)
     assert_close(np.stack([got[s, h] for s, h in heads]), ref, f"{which}, sub-groups")
+
+
+def test_subgroup_guards(torch):
+    """A sub-group wider than max_subgroup_size promised (more query rows than
+    the launch's MMA width) and sub-group starts outside the batch are refused
+    in the kernel: PA_DEVERR_CTX, nothing read or written for them, the other
+    sub-groups as plain decode."""
+    spec = [(None, [(2, [3, 5]), (1, [8, 9, 4]), (0, [30])])]
+    case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, spec, seed=9)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    x = nested_inputs(torch, case, gs, gp, pt, ss, sh)
+    plain = bf16_host(pa.paged_attention_decode(x["q"], x["kp"], x["vp"], x["bt"], x["ctx"], scale=case.scale,
+                                                max_context_len=case.max_context_len))
+    # max_subgroup_size 2 promises 8 rows (one MMA n-tile); the 3-member sub-group has 12
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x["kw"] = dict(x["kw"], max_subgroup_size=2)
+    out = torch.zeros_like(x["q"])
+    launch_nested(x, err, out)
+    torch.cuda.synchronize()
+    got = bf16_host(out)
+    assert int(err.item()) & pa.DEVERR_CTX
+    assert not np.any(got[2:5])
+    assert_close(np.concatenate([got[:2], got[5:]]), to_f64(np.concatenate([plain[:2], plain[5:]])), "other sub-groups")
+    # the last sub-group reaching past the batch: refused before any read
+    bad = ss.copy()
+    bad[-1] = case.num_seqs + 3
+    x = nested_inputs(torch, case, gs, gp, pt, bad, sh)
+    err.zero_()
+    out = torch.zeros_like(x["q"])
+    launch_nested(x, err, out)
+    torch.cuda.synchronize()
+    got = bf16_host(out)
+    assert int(err.item()) & pa.DEVERR_CTX
+    assert_close(got[:5], to_f64(plain[:5]), "in-range sub-groups")
+    assert not np.any(got[5:])  # the refused sub-group's rows are left alone (zeros from the caller)
