@@ -431,7 +431,8 @@ def build_prefix(args, torch, pa, dev, plan=None):
     return Bench(name, f"{name}: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
                  f"{shape}, {Hq}q/{Hkv}kv, D={D}, B={B}; "
                  f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + {mode}",
-                 inputs, step, dec_unique + copy + cache_bytes(S, Hkv, D), 4 if shared else 3,
+                 inputs, step, dec_unique + copy + cache_bytes(S, Hkv, D),
+                 3 + (1 if shared and len(groups["gp"]) else 0),  # copy, reshape, [prefix pass,] decode
                  "shared_prefix_decode" if shared else "decode_kernel", "hbm", dec_unique, S,
                  extra={"unique_pages": int(len(unique_pages)), "logical_decode_bytes": dec_logical,
                         "unique_decode_bytes": dec_unique, "cow_pairs": int(len(pairs))},
