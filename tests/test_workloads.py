@@ -75,3 +75,27 @@ def test_mixed_step_shape():
         for i in range(m.chunk_lens[r]):
             j = c0 + i
             assert m.chunk_slots[m.cu_q[r] + i] == m.chunk_tables[r, j // 32] * 32 + j % 32
+
+
+def test_sharing_workloads_subgroups():
+    """The sub-group partition the bench forms for the two sharing workloads
+    (from the host block manager's tables): consecutive, covering every
+    sequence; members agree on their shared blocks; the shared length is whole
+    blocks, at least the common prefix and at most every member's context; one
+    block of each member's own at most (the copy made on its append)."""
+    import bench
+    import paged_kv_cache_262_gb300 as pa
+    for plan in (None, wl.parallel_sampling_plan()):
+        plan, bt, ctx, slots, pairs = bench.prefix_sharing_setup(pa, plan)
+        ss, sh = bench.prefix_sharing_subgroups(plan, bt, ctx)
+        B = plan.B
+        assert ss[0] == 0 and ss[-1] == len(ctx) and np.all(np.diff(ss) >= 1)
+        assert len(sh) == len(ss) - 1
+        for k in range(len(sh)):
+            a, b = ss[k], ss[k + 1]
+            assert sh[k] % B == 0 and plan.prefix_len <= sh[k] <= ctx[a:b].min()
+            assert np.all(bt[a:b, : sh[k] // B] == bt[a, : sh[k] // B])
+            assert np.all(ctx[a:b] - sh[k] <= B)
+        # the appended token of every sample went to a slot of its own last block
+        for s in range(len(ctx)):
+            assert slots[s] // B == bt[s, (ctx[s] - 1) // B]
