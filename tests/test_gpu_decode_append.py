@@ -177,3 +177,23 @@ def test_append_rejects_bad_arguments(torch):
         d["new_v"].data_ptr(), d["slots"].data_ptr(), d["k_pool"].data_ptr(), d["v_pool"].data_ptr(),
         d["bt"].data_ptr(), d["ctx"].data_ptr(), d["q"].data_ptr(), None, 0, None, None)
     assert st == pa.PA_ERR_INVALID
+
+
+def test_append_long_context_full_size(torch, ora):
+    """The 8 x 32768-token, GQA-8 case as the bench launches it (decode with
+    append, four 512-page split-K parts): bits equal to the two launches on
+    every output and pool byte, sampled heads against the fp64 oracle."""
+    case = wl.long_context_decode()
+    d = upload_case(case, torch)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    want = two_launches(torch, case, d)
+    got = one_launch(torch, case, d, err=err)
+    assert int(err.item()) == 0
+    for g, w, what in zip(got, want, ("out", "k_pool", "v_pool")):
+        assert np.array_equal(g, w), f"long context: {what} differs from the two launches"
+    hk, hv = case.k_pool.copy(), case.v_pool.copy()
+    assert ora.reshape_and_cache(case.new_k, case.new_v, hk, hv, case.slot_mapping) == 0
+    heads = [(s, h) for s in range(case.num_seqs) for h in (0, 9, 63)]
+    sub = case.__class__(**{**case.__dict__, "k_pool": hk, "v_pool": hv})
+    ref = ora.decode_case(sub, heads=heads)
+    assert_close(np.stack([got[0][s, h] for s, h in heads]), ref, "long context with append")

@@ -36,6 +36,14 @@ def upload(torch, m):
     return d
 
 
+def oracle_pools(ora, m):
+    """The cache as the oracle writes it: the chunks' K/V into host copies of the pools."""
+    hk, hv = m.decode.k_pool.copy(), m.decode.v_pool.copy()
+    if len(m.chunk_slots):
+        assert ora.reshape_and_cache(m.chunk_new_k, m.chunk_new_v, hk, hv, m.chunk_slots) == 0
+    return hk, hv
+
+
 def kw(m):
     return dict(max_q_len=max(1, int(m.chunk_lens.max()) if len(m.chunk_lens) else 1), scale=m.decode.scale)
 
@@ -100,7 +108,7 @@ def test_mixed_against_oracle(torch, ora):
                            seed=42, stream=9)
     d = upload(torch, m)
     po, do = fused(torch, m, d)
-    hk, hv = bf16_host(d["kp"]), bf16_host(d["vp"])
+    hk, hv = oracle_pools(ora, m)
     ref, st = ora.decode(m.decode.q, hk, hv, m.decode.block_tables, m.decode.context_lens, m.decode.scale)
     assert np.all(st == 0)
     assert_close(do, ref, "mixed launch, decode rows")
@@ -186,3 +194,28 @@ def test_mixed_graph_replay(torch, monkeypatch):
         torch.cuda.synchronize()
         assert np.array_equal(bf16_host(pout), want[0]) and np.array_equal(bf16_host(dout), want[1])
     assert math.isfinite(float(bf16_host(dout).astype(np.float32).sum()))
+
+
+def test_mixed_full_size(torch, ora):
+    """The benchmark's mixed step (16 chunks x 512 over contexts U[512,8192] +
+    240 decodes, 32-token pages) through the mixed-step launch: bits equal to
+    the separate prefill and decode calls on every row; sampled rows of both
+    against the fp64 oracle."""
+    m = wl.mixed_step()
+    d = upload(torch, m)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    want = separate(torch, m, d)
+    got = fused(torch, m, d, err)
+    assert int(err.item()) == 0
+    assert np.array_equal(got[0], want[0]) and np.array_equal(got[1], want[1])
+    hk, hv = oracle_pools(ora, m)
+    dec = m.decode
+    heads = [(s, h) for s in range(0, dec.num_seqs, 17) for h in (0, 31)]
+    sub = dec.__class__(**{**dec.__dict__, "k_pool": hk, "v_pool": hv})
+    ref = ora.decode_case(sub, heads=heads)
+    assert_close(np.stack([got[1][s, h] for s, h in heads]), ref, "mixed step, decode rows")
+    rows = [(r, i) for r in (0, 7, 15) for i in (0, 255, 511)]
+    pre = np.stack([np.stack([ora.prefill_row(m.q_chunk, m.cu_q, hk, hv, m.chunk_tables, m.chunk_ctx,
+                                              dec.scale, r, i, h)[0] for h in (0, 13, 31)]) for r, i in rows])
+    gotp = np.stack([np.stack([got[0][m.cu_q[r] + i, h] for h in (0, 13, 31)]) for r, i in rows])
+    assert_close(gotp, pre, "mixed step, prefill rows")

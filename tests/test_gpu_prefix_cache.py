@@ -55,11 +55,11 @@ def test_cached_prefix_prefill_equals_from_scratch(torch, ora, B):
     kp = torch.zeros((nblk, Hkv, B, D), dtype=torch.bfloat16, device="cuda")
     vp = torch.zeros_like(kp)
     assert bm.add_seq_tokens(0, tok_a) == 0
-    prefill(torch, bm, 0, tok_a, kv_a[0], kv_a[1], q_a, 0, kp, vp, Hq, B, nblk)
+    _, _, slots_a = prefill(torch, bm, 0, tok_a, kv_a[0], kv_a[1], q_a, 0, kp, vp, Hq, B, nblk)
     cached = bm.add_seq_tokens(1, tok_b)
     assert cached == (shared // B) * B and cached > 0
     assert bm.block_table(1)[: cached // B] == bm.block_table(0)[: cached // B]
-    got, bt_b, _ = prefill(torch, bm, 1, tok_b, kv_b[0], kv_b[1], q_b, cached, kp, vp, Hq, B, nblk)
+    got, bt_b, slots_b = prefill(torch, bm, 1, tok_b, kv_b[0], kv_b[1], q_b, cached, kp, vp, Hq, B, nblk)
     # the same prompt from scratch in its own pool and manager
     bm2 = pa.BlockManager(nblk, B)
     kp2 = torch.zeros_like(kp)
@@ -67,9 +67,11 @@ def test_cached_prefix_prefill_equals_from_scratch(torch, ora, B):
     bm2.add_seq(0, nb)
     full, _, _ = prefill(torch, bm2, 0, tok_b, kv_b[0], kv_b[1], q_b, 0, kp2, vp2, Hq, B, nblk)
     assert_close(got, to_f64(full[cached:]), f"cached vs scratch B={B}")
-    # and the oracle, on the cache state the GPU holds
-    hk = bf16_host(kp)
-    hv = bf16_host(vp)
+    # and the oracle, on the cache it writes itself: A's tokens, then B's own ones
+    hk = np.zeros((nblk, Hkv, B, D), np.uint16)
+    hv = np.zeros_like(hk)
+    assert ora.reshape_and_cache(kv_a[0], kv_a[1], hk, hv, slots_a) == 0
+    assert ora.reshape_and_cache(kv_b[0][cached:], kv_b[1][cached:], hk, hv, slots_b) == 0
     cu = np.array([0, nb - cached], np.int32)
     rows = [0, 1, 57, nb - cached - 1]
     ref = np.stack([np.stack([ora.prefill_row(q_b[cached:], cu, hk, hv, bt_b, np.array([nb], np.int32),
