@@ -15,6 +15,11 @@ seeded generator in ``workloads``:
   prefix common to all: each prompt's blocks shared by its samples
   (sub-groups; ``--sharing one-level``: each prompt a group;
   ``--plain-decode``);
+* ``swap``: preemption -- 16 sequences x 2048 tokens (8 kv heads, D=128,
+  B=16, 4 layers; blocks scattered over the pool) to a pinned host pool and
+  back to new device blocks, pairs from the block manager (swap_blocks; the
+  link's reference rate is a copy-engine copy of the same bytes, measured in
+  the same run);
 * ``mixed_step``: one reshape_and_cache of every new token, then chunked
   prefill of 16 x 512 query tokens (tensor cores) and decode of 240 sequences
   (B=32) in one mixed-step launch whose CTAs run the two side by side
@@ -64,7 +69,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s"
 L2_BYTES = 129e6
 WORKLOADS = ["llama8b_decode", "long_context_decode", "tiny_decode", "prefix_sharing", "parallel_sampling",
-             "mixed_step"]
+             "mixed_step", "swap"]
 
 
 def parse():
@@ -539,11 +544,65 @@ def build_mixed(args, torch, pa, dev):
                  kernels=({"mixed_kernel": mixed} if fused else {}) | {"prefill_kernel": prefill, "decode_kernel": decode})
 
 
+def build_swap(args, torch, pa, dev):
+    B, Hkv, D, L = 16, 8, 128, 4
+    nseq, ntok = 16, 2048
+    per = ntok // B
+    ndev, nhost = int(1.25 * nseq * per), nseq * per
+    bm = pa.BlockManager(ndev, B, num_host_blocks=nhost)
+    for s in range(nseq):
+        bm.add_seq(s, 0)
+    for _ in range(ntok):  # round-robin appends: every sequence's blocks scattered over the pool
+        for s in range(nseq):
+            bm.append(s)
+    out_pairs = np.array([p for s in range(nseq) for p in bm.swap_out(s)], np.int64)
+    in_pairs = np.array([p for s in range(nseq) for p in bm.swap_in(s)], np.int64)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    dk = [torch.randn((ndev, Hkv, B, D), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    dv = [torch.randn((ndev, Hkv, B, D), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    hk = [torch.empty((nhost, Hkv, B, D), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    hv = [torch.empty_like(h).pin_memory() for h in hk]
+    blk = Hkv * B * D * 2
+    moved = 2 * len(out_pairs) * L * blk  # K and V of every block and layer, one way
+
+    def swap(i, x):
+        pa.swap_blocks(dk, dv, hk, hv, x["out_pairs"])  # preempt: device -> host
+        pa.swap_blocks(hk, hv, dk, dv, x["in_pairs"])   # resume: host -> new device blocks
+
+    def step(i, x, ev, o=None):
+        ev and ev[0].record()
+        swap(i, x)
+        ev and ev[1].record()
+        return []
+
+    # the link's reference: one contiguous copy-engine copy of the same bytes each way
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for r in range(4):
+        if r == 1:
+            e0.record()
+        hbuf.copy_(dbuf, non_blocking=True)
+        dbuf.copy_(hbuf, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    link_gbs = 3 * 2 * moved / (e0.elapsed_time(e1) / 1e3) / 1e9
+    return Bench("swap", f"swap: {nseq} sequences x {ntok} tokens, {Hkv} kv heads, D={D}, B={B}, {L} layers "
+                 f"({len(out_pairs)} scattered blocks) to pinned host memory and back to new device blocks",
+                 {"out_pairs": out_pairs, "in_pairs": in_pairs}, step, 2 * moved, 2, "swap_blocks", "link",
+                 2 * moved, nseq, extra={"link_gbs": round(link_gbs, 1), "blocks": int(len(out_pairs)),
+                                         "bytes_each_way": moved},
+                 layers=L, pool_mb=2 * L * ndev * blk / 1e6, kernels={"swap_blocks": swap})
+
+
 def build(args, torch, pa, dev):
     if args.workload == "prefix_sharing":
         return build_prefix(args, torch, pa, dev)
     if args.workload == "parallel_sampling":
         return build_prefix(args, torch, pa, dev, wl.parallel_sampling_plan())
+    if args.workload == "swap":
+        return build_swap(args, torch, pa, dev)
     if args.workload == "mixed_step":
         return build_mixed(args, torch, pa, dev)
     case = {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
@@ -669,6 +728,11 @@ def run_ours(args, rank, world, local_rank):
         achieved = b.kernel_work / (k_mean / 1e3) / 1e9
         peak, unit = peaks["hbm"], "GB/s"
         peak_note = f"{peaks['source']} hbm_gbs (copy, read+write bytes)"
+    elif b.bound == "link":
+        achieved = b.kernel_work / (k_mean / 1e3) / 1e9
+        peak, unit = b.extra["link_gbs"], "GB/s"
+        peak_note = ("chip-to-chip link: contiguous copy-engine copies (cudaMemcpyAsync, pinned host <-> device) "
+                     "of the same bytes each way, measured in this run")
     else:
         achieved = b.kernel_work / (k_mean / 1e3) / 1e12
         peak, unit = peaks["bf16_sustained"], "TFLOP/s"
@@ -702,7 +766,7 @@ def run_ours(args, rank, world, local_rank):
         res["workload_extra"] = b.extra
     if e2e:
         res["e2e"] = e2e
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.workload != "swap":  # (no attention arithmetic to time there)
         res["cpu_baseline"] = cpu_baseline(args, args.cpu_seconds)
     return res
 
