@@ -20,6 +20,11 @@ seeded generator in ``workloads``:
   back to new device blocks, pairs from the block manager (swap_blocks; the
   link's reference rate is a copy-engine copy of the same bytes, measured in
   the same run);
+* ``block_manager``: the host block manager alone (no GPU): 64 prompts x 4
+  samples admitted with prefix-cache lookups (a 2048-token system prompt
+  common to all, then each prompt's U[1,512] tokens), forked per sample, one
+  append each (copy-on-write); 64 unshared sequences swapped out and in;
+  everything freed; operations per second of host time;
 * ``mixed_step``: one reshape_and_cache of every new token, then chunked
   prefill of 16 x 512 query tokens (tensor cores) and decode of 240 sequences
   (B=32) in one mixed-step launch whose CTAs run the two side by side
@@ -69,7 +74,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 METRIC = "paged decode attention: KV HBM GB/s (% of GB300 peak), decode tokens/s"
 L2_BYTES = 129e6
 WORKLOADS = ["llama8b_decode", "long_context_decode", "tiny_decode", "prefix_sharing", "parallel_sampling",
-             "mixed_step", "swap"]
+             "mixed_step", "swap", "block_manager"]
 
 
 def parse():
@@ -996,8 +1001,83 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_block_manager(args):
+    """Host throughput of the block manager's operations (prefix caching,
+    fork, copy-on-write append, swap, free) over the prefix-sharing plan."""
+    import paged_kv_cache_262_gb300 as pa
+    plan = wl.prefix_sharing_plan()
+    st = wl.Stream(0, 8)
+    system = [int(t) for t in st.integers(0, 32000, plan.prefix_len)]
+    prompts = [system + [int(t) for t in st.integers(0, 32000, int(n))] for n in plan.suffix_lens]
+    R, B = plan.samples_per_prompt, plan.B
+    nblk = 4 * plan.num_blocks
+    times = {k: 0.0 for k in ("admit", "fork", "append", "swap", "free")}
+    counts = {"tokens": 0, "cached_tokens": 0, "forks": 0, "appends": 0, "cow": 0, "swapped_blocks": 0, "frees": 0}
+
+    def one_pass():
+        bm = pa.BlockManager(nblk, B, num_host_blocks=nblk)
+        t0 = time.perf_counter()
+        for p, toks in enumerate(prompts):
+            counts["cached_tokens"] += bm.add_seq_tokens(p * R, toks)
+            counts["tokens"] += len(toks)
+        t1 = time.perf_counter()
+        for p in range(len(prompts)):
+            for i in range(1, R):
+                bm.fork(p * R, p * R + i)
+                counts["forks"] += 1
+        t2 = time.perf_counter()
+        for s_ in range(len(prompts) * R):
+            _, pair = bm.append(s_)
+            counts["appends"] += 1
+            counts["cow"] += pair is not None
+        base = len(prompts) * R  # swapping needs unshared blocks: 64 separate 1024-token sequences
+        for j in range(64):
+            bm.add_seq(base + j, 1024)
+        t3 = time.perf_counter()
+        for j in range(64):
+            counts["swapped_blocks"] += len(bm.swap_out(base + j))
+            bm.swap_in(base + j)
+        t4 = time.perf_counter()
+        for s_ in range(base + 64):
+            bm.free_seq(s_)
+            counts["frees"] += 1
+        t5 = time.perf_counter()
+        for k, a, b in (("admit", t0, t1), ("fork", t1, t2), ("append", t2, t3), ("swap", t3, t4), ("free", t4, t5)):
+            times[k] += b - a
+
+    for _ in range(args.warmup):
+        one_pass()
+    for k in times:
+        times[k] = 0.0
+    for k in counts:
+        counts[k] = 0
+    w0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_pass()
+    wall = time.perf_counter() - w0
+    rate = lambda n, t: round(n / t, 1) if t > 0 else None  # noqa: E731
+    return {"metric": "host block manager: prompt tokens admitted per second (prefix-cache lookups)",
+            "value": rate(counts["tokens"], times["admit"]), "unit": "tokens/s", "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "none", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": f"block_manager: {len(prompts)} prompts x {R} samples, {plan.prefix_len}-token "
+                                   f"system prompt + U[1,512] tokens, B={B}; admit, fork, append; 64 unshared "
+                                   f"1024-token sequences swapped out and in; free all; per step (host only, "
+                                   f"through the C ABI from Python)"},
+            "cached_fraction": round(counts["cached_tokens"] / max(counts["tokens"], 1), 4),
+            "ops_per_s": {"fork": rate(counts["forks"], times["fork"]),
+                          "append": rate(counts["appends"], times["append"]),
+                          "copy_on_write_share": round(counts["cow"] / max(counts["appends"], 1), 4),
+                          "swap_blocks_out_and_in": rate(counts["swapped_blocks"], times["swap"]),
+                          "free": rate(counts["frees"], times["free"])},
+            "gpu_launches": 0}
+
+
 def main():
     args = parse()
+    if args.workload == "block_manager":  # host only
+        print(json.dumps(run_block_manager(args)), flush=True)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -391,3 +391,16 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
     for s in list(model):
         bm.free_seq(s)
     assert bm.num_free() == N and bm.num_free_host() == H
+
+
+def test_block_manager_benchmark_runs():
+    """bench.py --workload block_manager (host only): one pass of admission with
+    prefix-cache hits, forks, copy-on-write appends, swaps and frees."""
+    import types
+
+    import bench
+    res = bench.run_block_manager(types.SimpleNamespace(steps=1, warmup=0))
+    assert res["value"] > 0 and res["gpu_launches"] == 0
+    # every prompt after the first finds the 2048-token system prompt cached (whole blocks)
+    assert 0.5 < res["cached_fraction"] < 1.0
+    assert 0.0 < res["ops_per_s"]["copy_on_write_share"] <= 1.0
