@@ -91,3 +91,33 @@ def test_cache_call_validation(lib):
     assert g(P(16), P(16), 0, 16, 1, 10, 4096, None, None) == pa.PA_ERR_INVALID
     assert g(P(16), P(16), 1, 16, 1, 10, 4095, None, None) == pa.PA_ERR_INVALID
     assert g(P(None), P(16), 1, 16, 1, 10, 4096, None, None) == pa.PA_ERR_INVALID
+
+
+def test_new_entry_points_validate_before_any_gpu_work(lib):
+    """Decode with append, the mixed-step launch and the sub-group decode reject
+    bad arguments on the host, before touching the GPU."""
+    d = _desc()
+    app = lib.pa_paged_attention_decode_append
+    # q, new_k, new_v, slots, k_pool, v_pool, tables, ctx, out, workspace, ws_bytes, err, stream
+    assert app(ctypes.byref(d), 16, None, 16, 16, 16, 16, 16, 16, 16, None, 0, None, None) == pa.PA_ERR_INVALID
+    assert app(ctypes.byref(d), 16, 18, 16, 16, 16, 16, 16, 16, 16, None, 0, None, None) == pa.PA_ERR_INVALID
+    assert app(ctypes.byref(_desc(head_dim=96)), 16, 16, 16, 16, 16, 16, 16, 16, 16, None, 0, None,
+               None) == pa.PA_ERR_UNSUPPORTED
+    mixed = lib.pa_paged_attention_mixed
+
+    def call_mixed(pd, dd):
+        return mixed(pd, 16, 16, 8, 8, 16, 16, 16, dd, 16, 16, 16, 16, None, 0, 16, 16, None, None)
+    assert call_mixed(None, ctypes.byref(d)) == pa.PA_ERR_INVALID
+    assert call_mixed(ctypes.byref(_desc(block_size=32)), ctypes.byref(d)) == pa.PA_ERR_INVALID  # other pools
+    g3 = _desc(num_q_heads=6, num_kv_heads=2)  # a GQA group the tensor-core prefill does not build
+    assert call_mixed(ctypes.byref(g3), ctypes.byref(g3)) == pa.PA_ERR_UNSUPPORTED
+    sp2 = lib.pa_paged_attention_decode_shared_prefix2
+
+    def call_sp2(desc, nsub, starts, shared, max_size):
+        return sp2(ctypes.byref(desc), 16, 16, 16, 16, 16, 0, None, None, None, 0, 0, 0, nsub, starts, shared,
+                   max_size, 16, 16, 1 << 20, None, None)
+    assert call_sp2(d, -1, 16, 16, 4) == pa.PA_ERR_INVALID
+    assert call_sp2(d, 2, None, 16, 4) == pa.PA_ERR_INVALID
+    assert call_sp2(d, 2, 16, 16, 5) == pa.PA_ERR_UNSUPPORTED   # 5 members x 4 heads > 16 query rows
+    assert call_sp2(_desc(head_dim=64), 2, 16, 16, 2) == pa.PA_ERR_UNSUPPORTED
+    assert call_sp2(_desc(num_seqs=0), 2, 16, 16, 4) == pa.PA_OK  # nothing to decode
