@@ -358,6 +358,9 @@ int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *con
  * write when a sharer appends into a block with ref_count > 1, and returned to
  * the free list when the last reference is dropped.  The free list is LIFO;
  * initially blocks are handed out in increasing id order.  Not thread safe.
+ * No C++ exception leaves these calls: a failed host allocation returns
+ * PA_ERR_OOM (NULL from the create calls, -1 from pa_bm_wasted_slots) and
+ * leaves the manager as it was before the call.
  * ------------------------------------------------------------------------ */
 typedef struct pa_bm pa_bm;
 
@@ -396,14 +399,18 @@ int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n
  * exactly), and a new prompt reuses the longest chain of registered full
  * blocks from its start (ref_count + 1 each; a registered block keeps its
  * content after its last user frees it, until the block is handed out
- * again).  *cached_tokens (may be NULL) gets the number of leading tokens
+ * again; then every registered block that continued it -- its K/V were
+ * computed after the old content -- leaves the cache with it).  The first
+ * call allocates num_blocks * block_size token ids of host memory for the
+ * cache's keys.  *cached_tokens (may be NULL) gets the number of leading tokens
  * whose K/V are already in the cache: the caller writes and prefills only
  * tokens cached_tokens .. num_tokens-1.  A block registered here holds valid
  * K/V once this sequence's prefill of it has run.  PA_ERR_OOM leaves no
  * trace. */
 int pa_bm_add_seq_tokens(pa_bm *bm, int seq_id, const int32_t *tokens, int num_tokens, int *cached_tokens);
 
-/* Number of blocks currently registered in the prefix cache. */
+/* Number of blocks currently registered in the prefix cache (free ones
+ * included). */
 int pa_bm_num_cached_blocks(const pa_bm *bm);
 
 /* Moves seq_id to host blocks (preemption): every block must be unshared

@@ -11,6 +11,7 @@
 // the preemptive-swapping answer: a paused request's pages move to host RAM
 // and come back when device blocks free up).
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <new>
 #include <unordered_map>
@@ -27,6 +28,21 @@ struct Seq {
   bool swapped = false;
 };
 
+// No C++ exception leaves an entry point: a failed allocation (the only
+// exception these containers throw) becomes PA_ERR_OOM.  Each entry point
+// makes its allocations before it changes any state, or undoes its changes,
+// so that a failure leaves the manager as it was.
+template <class F>
+int guarded(F &&f) noexcept {
+  try {
+    return f();
+  } catch (const std::bad_alloc &) {
+    return PA_ERR_OOM;
+  } catch (...) {
+    return PA_ERR_INVALID;
+  }
+}
+
 }  // namespace
 
 struct pa_bm {
@@ -40,10 +56,20 @@ struct pa_bm {
   // parent (the block before it in the sequence, -1 for the first) and its B
   // token ids; lookups compare both exactly, the hash only picks the bucket.
   // A cached block keeps its content after its last user frees it, until the
-  // block is handed out again.
-  std::unordered_map<uint64_t, std::vector<int32_t>> cache;
-  std::vector<int32_t> c_parent;             // per block, -2 = not cached
-  std::vector<std::vector<int32_t>> c_tokens;
+  // block is handed out again; then every cached block that continues it (its
+  // children, their children, ...) leaves the cache with it, since their K/V
+  // were computed after the old content.  A block in use never loses a cached
+  // ancestor: whoever holds a block holds the blocks before it.
+  // All of it lives in arrays sized up front (the token copies on first use),
+  // so registering, finding and dropping entries never allocates.
+  std::vector<int32_t> c_parent;  // per block, -2 = not cached
+  std::vector<uint64_t> c_hash;
+  std::vector<int32_t> c_next, c_prev;    // hash-bucket chain
+  std::vector<int32_t> c_kid;             // first cached child
+  std::vector<int32_t> c_snext, c_sprev;  // chain of the parent's cached children
+  std::vector<int32_t> bucket;            // head of each hash bucket, -1 = empty
+  uint64_t bucket_mask = 0;
+  std::vector<int32_t> c_tok;  // [num_blocks][block_size] token ids of cached blocks
   int ncached = 0;
   std::vector<int32_t> host_free;  // free host blocks (LIFO), for swapped-out sequences
   int num_host_blocks = 0;
@@ -57,21 +83,35 @@ struct pa_bm {
     }
     return h ^ (h >> 29);
   }
-  void uncache(int32_t b) {
-    if (c_parent[b] == -2) return;
-    auto it = cache.find(key_hash(c_parent[b], c_tokens[b].data(), block_size));
-    if (it != cache.end()) {
-      auto &v = it->second;
-      for (size_t i = 0; i < v.size(); ++i)
-        if (v[i] == b) {
-          v.erase(v.begin() + i);
-          break;
-        }
-      if (v.empty()) cache.erase(it);
+  void unlink(int32_t b) {  // b is cached and has no cached children
+    const int32_t pv = c_prev[b], nx = c_next[b];
+    if (pv >= 0)
+      c_next[pv] = nx;
+    else
+      bucket[c_hash[b] & bucket_mask] = nx;
+    if (nx >= 0) c_prev[nx] = pv;
+    const int32_t p = c_parent[b];
+    if (p >= 0) {
+      const int32_t sp = c_sprev[b], sn = c_snext[b];
+      if (sp >= 0)
+        c_snext[sp] = sn;
+      else
+        c_kid[p] = sn;
+      if (sn >= 0) c_sprev[sn] = sp;
     }
     c_parent[b] = -2;
-    c_tokens[b].clear();
     --ncached;
+  }
+  void uncache(int32_t root) {  // root and all its cached descendants, leaves first
+    if (c_parent[root] == -2) return;
+    int32_t b = root;
+    for (;;) {
+      while (c_kid[b] >= 0) b = c_kid[b];
+      const int32_t p = c_parent[b];
+      unlink(b);
+      if (b == root) return;
+      b = p;
+    }
   }
   int32_t take() {  // caller checked nfree > 0
     for (;;) {
@@ -85,7 +125,7 @@ struct pa_bm {
       return b;
     }
   }
-  void drop(int32_t b) {
+  void drop(int32_t b) {  // never allocates: free_list has room for every block
     if (--ref[b] == 0) {
       if (!in_free[b]) {  // a revived block still has its old entry: reuse it
         free_list.push_back(b);
@@ -95,16 +135,30 @@ struct pa_bm {
     }
   }
   int32_t lookup(int32_t parent, const int32_t *tok) const {
-    auto it = cache.find(key_hash(parent, tok, block_size));
-    if (it == cache.end()) return -1;
-    for (int32_t b : it->second)
-      if (c_parent[b] == parent && std::equal(c_tokens[b].begin(), c_tokens[b].end(), tok)) return b;
+    if (c_tok.empty()) return -1;
+    const uint64_t h = key_hash(parent, tok, block_size);
+    for (int32_t b = bucket[h & bucket_mask]; b >= 0; b = c_next[b])
+      if (c_hash[b] == h && c_parent[b] == parent && std::equal(tok, tok + block_size, &c_tok[(size_t)b * block_size]))
+        return b;
     return -1;
   }
-  void register_block(int32_t b, int32_t parent, const int32_t *tok) {
+  void register_block(int32_t b, int32_t parent, const int32_t *tok) {  // b not cached; c_tok allocated
+    std::copy(tok, tok + block_size, &c_tok[(size_t)b * block_size]);
+    const uint64_t h = key_hash(parent, tok, block_size);
+    c_hash[b] = h;
     c_parent[b] = parent;
-    c_tokens[b].assign(tok, tok + block_size);
-    cache[key_hash(parent, tok, block_size)].push_back(b);
+    c_kid[b] = -1;
+    int32_t &head = bucket[h & bucket_mask];
+    c_prev[b] = -1;
+    c_next[b] = head;
+    if (head >= 0) c_prev[head] = b;
+    head = b;
+    if (parent >= 0) {
+      c_sprev[b] = -1;
+      c_snext[b] = c_kid[parent];
+      if (c_kid[parent] >= 0) c_sprev[c_kid[parent]] = b;
+      c_kid[parent] = b;
+    }
     ++ncached;
   }
 };
@@ -115,18 +169,32 @@ pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_siz
   if (num_blocks <= 0 || num_host_blocks < 0 || block_size <= 0) return nullptr;
   pa_bm *bm = new (std::nothrow) pa_bm();
   if (!bm) return nullptr;
-  bm->num_blocks = num_blocks;
-  bm->block_size = block_size;
-  bm->ref.assign(num_blocks, 0);
-  bm->free_list.reserve(num_blocks);
-  for (int b = num_blocks - 1; b >= 0; --b) bm->free_list.push_back(b);
-  bm->nfree = num_blocks;
-  bm->in_free.assign(num_blocks, 1);
-  bm->c_parent.assign(num_blocks, -2);
-  bm->c_tokens.resize(num_blocks);
-  bm->num_host_blocks = num_host_blocks;
-  bm->host_free.reserve(num_host_blocks);
-  for (int b = num_host_blocks - 1; b >= 0; --b) bm->host_free.push_back(b);
+  try {
+    bm->num_blocks = num_blocks;
+    bm->block_size = block_size;
+    bm->ref.assign(num_blocks, 0);
+    bm->free_list.reserve(num_blocks);
+    for (int b = num_blocks - 1; b >= 0; --b) bm->free_list.push_back(b);
+    bm->nfree = num_blocks;
+    bm->in_free.assign(num_blocks, 1);
+    bm->c_parent.assign(num_blocks, -2);
+    bm->c_hash.assign(num_blocks, 0);
+    bm->c_next.assign(num_blocks, -1);
+    bm->c_prev.assign(num_blocks, -1);
+    bm->c_kid.assign(num_blocks, -1);
+    bm->c_snext.assign(num_blocks, -1);
+    bm->c_sprev.assign(num_blocks, -1);
+    size_t nb = 1;
+    while (nb < (size_t)num_blocks) nb <<= 1;
+    bm->bucket.assign(nb, -1);
+    bm->bucket_mask = nb - 1;
+    bm->num_host_blocks = num_host_blocks;
+    bm->host_free.reserve(num_host_blocks);
+    for (int b = num_host_blocks - 1; b >= 0; --b) bm->host_free.push_back(b);
+  } catch (...) {
+    delete bm;
+    return nullptr;
+  }
   return bm;
 }
 
@@ -136,25 +204,29 @@ void pa_bm_destroy(pa_bm *bm) { delete bm; }
 
 int pa_bm_add_seq(pa_bm *bm, int seq_id, int num_tokens) {
   if (!bm || seq_id < 0 || num_tokens < 0) return PA_ERR_INVALID;
-  if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
-  const int64_t need = ((int64_t)num_tokens + bm->block_size - 1) / bm->block_size;
-  if (need > (int64_t)bm->nfree) return PA_ERR_OOM;
-  Seq s;
-  s.len = num_tokens;
-  s.blocks.reserve(need);
-  for (int64_t i = 0; i < need; ++i) s.blocks.push_back(bm->take());
-  bm->seqs.emplace(seq_id, std::move(s));
-  return PA_OK;
+  return guarded([&]() -> int {
+    if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
+    const int64_t need = ((int64_t)num_tokens + bm->block_size - 1) / bm->block_size;
+    if (need > (int64_t)bm->nfree) return PA_ERR_OOM;
+    Seq s;
+    s.len = num_tokens;
+    s.blocks.reserve(need);
+    // the last allocation; the blocks then go into the reserved room
+    Seq &q = bm->seqs.emplace(seq_id, std::move(s)).first->second;
+    for (int64_t i = 0; i < need; ++i) q.blocks.push_back(bm->take());
+    return PA_OK;
+  });
 }
 
 int pa_bm_fork(pa_bm *bm, int parent_id, int child_id) {
   if (!bm || child_id < 0) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(parent_id);
-  if (it == bm->seqs.end() || bm->seqs.count(child_id) || it->second.swapped) return PA_ERR_STATE;
-  Seq c = it->second;
-  for (int32_t b : c.blocks) ++bm->ref[b];
-  bm->seqs.emplace(child_id, std::move(c));
-  return PA_OK;
+  return guarded([&]() -> int {
+    auto it = bm->seqs.find(parent_id);
+    if (it == bm->seqs.end() || bm->seqs.count(child_id) || it->second.swapped) return PA_ERR_STATE;
+    const Seq &c = bm->seqs.emplace(child_id, it->second).first->second;  // copies; then no allocation
+    for (int32_t b : c.blocks) ++bm->ref[b];
+    return PA_OK;
+  });
 }
 
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]) {
@@ -164,9 +236,17 @@ int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[
   Seq &s = it->second;
   const int B = bm->block_size;
   const int j = s.len;
+  if (j == INT_MAX) return PA_ERR_INVALID;
   cow_pair_out[0] = cow_pair_out[1] = -1;
   if (j % B == 0) {  // the token opens a new block
     if (bm->nfree == 0) return PA_ERR_OOM;
+    if (s.blocks.size() == s.blocks.capacity()) {  // grow before the block is taken
+      const int st = guarded([&]() -> int {
+        s.blocks.reserve(std::max<size_t>(8, 2 * s.blocks.size()));
+        return PA_OK;
+      });
+      if (st != PA_OK) return st;
+    }
     s.blocks.push_back(bm->take());
   } else {
     int32_t &last = s.blocks[j / B];
@@ -230,40 +310,45 @@ int pa_bm_num_free(const pa_bm *bm) { return bm ? bm->nfree : -1; }
 
 int pa_bm_add_seq_tokens(pa_bm *bm, int seq_id, const int32_t *tokens, int num_tokens, int *cached_tokens) {
   if (!bm || seq_id < 0 || num_tokens < 0 || (num_tokens > 0 && !tokens)) return PA_ERR_INVALID;
-  if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
-  const int B = bm->block_size;
-  const int nfull = num_tokens / B;
-  const int need = (num_tokens + B - 1) / B;
-  // longest chain of cached full blocks from the start
-  std::vector<int32_t> hit;
-  int32_t parent = -1;
-  for (int i = 0; i < nfull; ++i) {
-    const int32_t b = bm->lookup(parent, tokens + (size_t)i * B);
-    if (b < 0) break;
-    hit.push_back(b);
-    parent = b;
-  }
-  int revive = 0;  // hits that sit in the free pool
-  for (int32_t b : hit) revive += bm->ref[b] == 0;
-  if ((int64_t)(need - (int)hit.size()) > (int64_t)bm->nfree - revive) return PA_ERR_OOM;
-  Seq s;
-  s.len = num_tokens;
-  for (int32_t b : hit) {
-    if (bm->ref[b]++ == 0) --bm->nfree;  // revived: its stale free-list entry is skipped later
-    s.blocks.push_back(b);
-  }
-  parent = hit.empty() ? -1 : hit.back();
-  for (int i = (int)hit.size(); i < need; ++i) {
-    const int32_t b = bm->take();
-    if (i < nfull) {  // a full block of the prompt: findable by later prompts
-      bm->register_block(b, parent, tokens + (size_t)i * B);
+  return guarded([&]() -> int {
+    if (bm->seqs.count(seq_id)) return PA_ERR_STATE;
+    const int B = bm->block_size;
+    const int64_t nfull = num_tokens / B;
+    const int64_t need = ((int64_t)num_tokens + B - 1) / B;
+    // longest chain of cached full blocks from the start
+    std::vector<int32_t> hit;
+    int32_t parent = -1;
+    for (int64_t i = 0; i < nfull; ++i) {
+      const int32_t b = bm->lookup(parent, tokens + (size_t)i * B);
+      if (b < 0) break;
+      hit.push_back(b);
       parent = b;
     }
-    s.blocks.push_back(b);
-  }
-  if (cached_tokens) *cached_tokens = (int)hit.size() * B;
-  bm->seqs.emplace(seq_id, std::move(s));
-  return PA_OK;
+    int64_t revive = 0;  // hits that sit in the free pool
+    for (int32_t b : hit) revive += bm->ref[b] == 0;
+    if (need - (int64_t)hit.size() > (int64_t)bm->nfree - revive) return PA_ERR_OOM;
+    Seq s;
+    s.len = num_tokens;
+    s.blocks.reserve(need);
+    // the last allocations; nothing below allocates
+    if (nfull > (int64_t)hit.size() && bm->c_tok.empty()) bm->c_tok.assign((size_t)bm->num_blocks * B, 0);
+    Seq &q = bm->seqs.emplace(seq_id, std::move(s)).first->second;
+    for (int32_t b : hit) {
+      if (bm->ref[b]++ == 0) --bm->nfree;  // revived: its stale free-list entry is skipped later
+      q.blocks.push_back(b);
+    }
+    parent = hit.empty() ? -1 : hit.back();
+    for (int64_t i = (int64_t)hit.size(); i < need; ++i) {
+      const int32_t b = bm->take();
+      q.blocks.push_back(b);
+      if (i < nfull) {  // a full block of the prompt: findable by later prompts
+        bm->register_block(b, parent, tokens + (size_t)i * B);
+        parent = b;
+      }
+    }
+    if (cached_tokens) *cached_tokens = (int)hit.size() * B;
+    return PA_OK;
+  });
 }
 
 int pa_bm_num_cached_blocks(const pa_bm *bm) { return bm ? bm->ncached : -1; }
@@ -313,8 +398,11 @@ int pa_bm_swap_in(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n) {
 
 int pa_bm_num_free_host(const pa_bm *bm) { return bm ? (int)bm->host_free.size() : -1; }
 
-int64_t pa_bm_wasted_slots(const pa_bm *bm) {
-  if (!bm) return -1;
+}  // extern "C"
+
+namespace {
+
+int64_t wasted_slots(const pa_bm *bm) {
   // Only a sequence's last block can be partly filled.  A block shared by
   // several sequences is counted once, with the largest fill among them.
   std::unordered_map<int32_t, int> fill;
@@ -331,6 +419,19 @@ int64_t pa_bm_wasted_slots(const pa_bm *bm) {
   int64_t w = 0;
   for (const auto &kv : fill) w += bm->block_size - kv.second;
   return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t pa_bm_wasted_slots(const pa_bm *bm) {
+  if (!bm) return -1;
+  try {
+    return wasted_slots(bm);
+  } catch (...) {
+    return -1;
+  }
 }
 
 }  // extern "C"

@@ -282,7 +282,67 @@ def test_prefix_cache_never_hands_out_a_block_twice():
         bm.add_seq(2, 1)
 
 
-def test_model_based_contents_through_cow_swap_and_prefix_cache():
+def test_prefix_cache_drops_continuations_of_a_reused_block():
+    """A cached block's K/V were computed after its whole prefix.  When a block
+    is handed out again for new content, the cached blocks that continued it
+    must leave the cache with it, or a prompt that matches the new content
+    would be given a continuation computed after the old one."""
+    bm = pa.BlockManager(2, 1)
+    A, C, X = 100, 200, 300
+    assert bm.add_seq_tokens(0, [A, C]) == 0               # blocks 0 (A), 1 (C after A)
+    bm.free_seq(0)                                          # both free, both still cached
+    assert bm.num_cached_blocks() == 2
+    assert bm.add_seq_tokens(1, [X]) == 0                   # block 0 now holds X
+    assert bm.num_cached_blocks() == 1                      # C-after-A went with A
+    assert bm.add_seq_tokens(2, [X, C]) == 1                # only X is found
+
+
+def test_prefix_cache_drops_whole_subtrees_and_keeps_live_chains():
+    """Three prompts share a first block and branch after it.  Once they are
+    freed, handing that first block out again for new content drops every
+    cached continuation of it at once; a chain still in use is not touched."""
+    B = 2
+    bm = pa.BlockManager(8, B)
+    a, b, c, d, x = [1, 2], [3, 4], [5, 6], [7, 8], [9, 10]
+    assert bm.add_seq_tokens(0, a + b + c) == 0
+    assert bm.add_seq_tokens(1, a + b + d) == 4             # a, b found; d's block is new
+    assert bm.add_seq_tokens(2, a + c) == 2
+    assert bm.num_cached_blocks() == 5                      # a; b, c under a; c, d under b
+    assert bm.add_seq_tokens(3, d + d) == 0                 # an unrelated chain, kept in use
+    t0 = bm.block_table(0)
+    for s in (1, 2, 0):                                     # seq 0 last: its first block is reused first
+        bm.free_seq(s)
+    assert bm.num_free() == 6 and bm.num_cached_blocks() == 7
+    assert bm.add_seq_tokens(4, x) == 0
+    assert bm.block_table(4) == t0[:1]                      # a's block now holds x
+    assert bm.num_cached_blocks() == 3                      # x and the live d d; a's subtree is gone
+    assert bm.add_seq_tokens(5, x + b + c) == 2             # b after x was never computed
+    assert bm.add_seq_tokens(6, d + d + a) == 4             # the live chain is still found
+
+
+def test_failed_allocations_leave_no_trace(tmp_path):
+    """Every host allocation inside every block-manager call made to fail in
+    turn (a replaced operator new, in a C++ driver built with the block
+    manager's source): each failure comes back as an error status, never as a
+    C++ exception through the C ABI, and leaves the manager as it was."""
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    exe = str(tmp_path / "bm_alloc_fail")
+    subprocess.run([cxx, "-std=c++17", "-O1", "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "bm_alloc_fail.cpp"),
+                    os.path.join(root, "paged_kv_cache_262_gb300", "csrc", "pa_block_manager.cpp"),
+                    "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("ok ") and int(r.stdout.split()[1]) >= 20, r.stdout
+
+
+@pytest.mark.parametrize("N", [24, 64])
+def test_model_based_contents_through_cow_swap_and_prefix_cache(N):
     """Random prompts (some repeating earlier prompts' leading blocks), forks,
     appends, frees, swap-outs and swap-ins against simulated device and host
     page pools.  The test plays the caller: it writes each new token into the
@@ -290,8 +350,11 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
     pair to the simulated pools, and after each operation reads every resident
     sequence back through its block table: the tokens must be exactly the
     sequence's own, and each block's reference count must equal the number of
-    resident tables holding it."""
-    B, N, H = 8, 64, 24
+    resident tables holding it.  A slot holds what a key or value depends on:
+    the token and every token before it (a fingerprint of the prefix), so a
+    prefix-cache hit on a block whose content was computed after another
+    prefix fails the read-back."""
+    B, H = 8, 24
     bm = pa.BlockManager(N, B, num_host_blocks=H)
     dev = np.full((N, B), -1, np.int64)
     host = np.full((H, B), -1, np.int64)
@@ -299,13 +362,22 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
     st = wl.Stream(77, 3)
     u = st.uniform(3000)
     fresh = iter(range(10 ** 6, 10 ** 7))
+    chunks = [[next(fresh) for _ in range(B)] for _ in range(4)]
     prompts = []
     nxt = 0
 
+    def fp(toks):  # per position: a fingerprint of toks[:j + 1]
+        out, h = [], 0
+        for x in toks:
+            h = (h * 1000003 + x + 1) % (1 << 61)
+            out.append(h)
+        return out
+
     def write(s, start):
         t = bm.block_table(s)
+        f = fp(model[s])
         for j in range(start, len(model[s])):
-            dev[t[j // B], j % B] = model[s][j]
+            dev[t[j // B], j % B] = f[j]
 
     def check_all():
         refs = np.zeros(N, int)
@@ -314,7 +386,7 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
                 continue
             t = bm.block_table(s)
             assert len(t) == (len(toks) + B - 1) // B and bm.seq_len(s) == len(toks)
-            assert [int(dev[t[j // B], j % B]) for j in range(len(toks))] == toks, f"seq {s}"
+            assert [int(dev[t[j // B], j % B]) for j in range(len(toks))] == fp(toks), f"seq {s}"
             for b in t:
                 refs[b] += 1
         assert all(bm.ref_count(b) == refs[b] for b in range(N))
@@ -327,10 +399,14 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
         op = u[(k * 7919) % 3000]
         try:
             if op < 0.2 or not model:
-                if prompts and op < 0.12:  # repeat some full blocks of an earlier prompt
+                if prompts and op < 0.08:  # repeat some full blocks of an earlier prompt
                     base = prompts[int(u[k] * 1e6) % len(prompts)]
                     keep = (int(u[k] * 1e8) % (len(base) // B + 1)) * B
                     toks = base[:keep] + [next(fresh) for _ in range(int(u[k] * 1e5) % 20)]
+                elif op < 0.16:  # blocks from a small set in any order: equal blocks after other prefixes
+                    n = 1 + int(u[k] * 1e3) % 5
+                    toks = [x for i in range(n) for x in chunks[int(u[k] * 10 ** (4 + i)) % len(chunks)]]
+                    toks += [next(fresh) for _ in range(int(u[k] * 1e5) % 4 == 3)]
                 else:
                     toks = [next(fresh) for _ in range(1 + int(u[k] * 1e5) % 40)]
                 if not toks:
@@ -339,7 +415,7 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
                 assert c % B == 0 and 0 <= c <= len(toks)
                 model[nxt] = list(toks)
                 t = bm.block_table(nxt)
-                assert [int(dev[t[j // B], j % B]) for j in range(c)] == toks[:c]  # cached blocks hold the prompt
+                assert [int(dev[t[j // B], j % B]) for j in range(c)] == fp(toks)[:c]  # cached blocks hold the prompt
                 write(nxt, c)
                 prompts.append(list(toks))
                 nxt += 1
@@ -356,8 +432,8 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache():
                     slot, cow = bm.append(s)
                     if cow is not None:
                         dev[cow[1]] = dev[cow[0]]
-                    dev[slot // B, slot % B] = tok
                     model[s].append(tok)
+                    dev[slot // B, slot % B] = fp(model[s])[-1]
             elif op < 0.78:
                 s = pick()
                 if s is not None:
