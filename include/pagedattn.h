@@ -75,7 +75,7 @@ typedef enum pa_status {
   PA_ERR_INVALID = -1,     /* bad argument (null pointer, size, alignment) */
   PA_ERR_UNSUPPORTED = -2, /* valid but not built (head_dim, block_size, GQA group) */
   PA_ERR_CUDA = -3,        /* CUDA runtime / launch error */
-  PA_ERR_OOM = -4,         /* block manager: no free block */
+  PA_ERR_OOM = -4,         /* block manager: no free block, or no host memory */
   PA_ERR_WORKSPACE = -5,   /* workspace missing or smaller than required */
   PA_ERR_STATE = -6        /* block manager: unknown / duplicate sequence id,
                               reference count underflow */

@@ -88,6 +88,16 @@ int validate_decode_desc(const pa_decode_desc *d) {
   return PA_OK;
 }
 
+// A new nonzero tag for the split-K arrival counters of one decode launch.
+unsigned int next_decode_epoch() {
+  static std::atomic<unsigned int> counter{0};
+  unsigned int e;
+  do {
+    e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (e == 0);
+  return e;
+}
+
 // Split policy.  Each CTA streams one part (part_pages pages of one
 // (sequence, kv head)); two CTAs (16-token pages) or three (32-token pages)
 // are resident per SM.  The host knows only the longest-context bound, so it
@@ -102,15 +112,6 @@ int validate_decode_desc(const pa_decode_desc *d) {
 // longest context first).  Parts never go below kMinPartPages pages unless
 // the context is shorter.  PA_PARTITION_PAGES in the environment overrides
 // the part length (tuning).
-unsigned int next_decode_epoch() {
-  static std::atomic<unsigned int> counter{0};
-  unsigned int e;
-  do {
-    e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
-  } while (e == 0);
-  return e;
-}
-
 DecodePlan make_decode_plan(const pa_decode_desc *d, int sm_count) {
   const int kCtasPerSm = d->block_size == 16 ? 2 : 3;  // resident decode CTAs per SM (shared memory)
   constexpr int kMinPartPages = 32;
@@ -163,7 +164,7 @@ const char *pa_status_string(int s) {
     case PA_ERR_INVALID: return "invalid argument";
     case PA_ERR_UNSUPPORTED: return "unsupported shape";
     case PA_ERR_CUDA: return "CUDA error";
-    case PA_ERR_OOM: return "out of blocks";
+    case PA_ERR_OOM: return "out of blocks or host memory";
     case PA_ERR_WORKSPACE: return "workspace missing or too small";
     case PA_ERR_STATE: return "bad block-manager state";
     default: return "unknown status";
