@@ -1007,8 +1007,9 @@ def run_block_manager(args):
     import paged_kv_cache_262_gb300 as pa
     plan = wl.prefix_sharing_plan()
     st = wl.Stream(0, 8)
-    system = [int(t) for t in st.integers(0, 32000, plan.prefix_len)]
-    prompts = [system + [int(t) for t in st.integers(0, 32000, int(n))] for n in plan.suffix_lens]
+    system = np.asarray(st.integers(0, 32000, plan.prefix_len), np.int32)
+    prompts = [np.concatenate([system, np.asarray(st.integers(0, 32000, int(n)), np.int32)])
+               for n in plan.suffix_lens]
     R, B = plan.samples_per_prompt, plan.B
     nblk = 4 * plan.num_blocks
     times = {k: 0.0 for k in ("admit", "fork", "append", "swap", "free")}
@@ -1063,7 +1064,7 @@ def run_block_manager(args):
             "config": {"workload": f"block_manager: {len(prompts)} prompts x {R} samples, {plan.prefix_len}-token "
                                    f"system prompt + U[1,512] tokens, B={B}; admit, fork, append; 64 unshared "
                                    f"1024-token sequences swapped out and in; free all; per step (host only, "
-                                   f"through the C ABI from Python)"},
+                                   f"through the C ABI from Python; prompts held as int32 arrays)"},
             "cached_fraction": round(counts["cached_tokens"] / max(counts["tokens"], 1), 4),
             "ops_per_s": {"fork": rate(counts["forks"], times["fork"]),
                           "append": rate(counts["appends"], times["append"]),

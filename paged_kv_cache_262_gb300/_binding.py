@@ -525,11 +525,16 @@ class BlockManager:
         return self._swap(self._lib.pa_bm_swap_in, seq_id)
 
     def add_seq_tokens(self, seq_id: int, tokens) -> int:
-        """New sequence holding the prompt `tokens` (ints); returns how many
-        leading tokens were found in the prefix cache."""
-        arr = (_c.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+        """New sequence holding the prompt `tokens` (a 1-D sequence of int32
+        token ids; a contiguous int32 numpy array is passed without a copy);
+        returns how many leading tokens were found in the prefix cache."""
+        import numpy as np
+        arr = np.ascontiguousarray(tokens, dtype=np.int32)
+        if arr.ndim != 1:
+            raise ValueError("tokens must be 1-D")
         cached = _c.c_int()
-        _check(self._lib.pa_bm_add_seq_tokens(self._h, int(seq_id), arr, len(tokens), _c.byref(cached)),
+        ptr = arr.ctypes.data_as(_c.POINTER(_c.c_int32)) if arr.size else None
+        _check(self._lib.pa_bm_add_seq_tokens(self._h, int(seq_id), ptr, int(arr.size), _c.byref(cached)),
                "pa_bm_add_seq_tokens")
         return cached.value
 
