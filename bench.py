@@ -1012,8 +1012,12 @@ def run_block_manager(args):
                for n in plan.suffix_lens]
     R, B = plan.samples_per_prompt, plan.B
     nblk = 4 * plan.num_blocks
-    times = {k: 0.0 for k in ("admit", "fork", "append", "swap", "free")}
-    counts = {"tokens": 0, "cached_tokens": 0, "forks": 0, "appends": 0, "cow": 0, "swapped_blocks": 0, "frees": 0}
+    times = {k: 0.0 for k in ("admit", "fork", "append", "steady", "swap", "free")}
+    counts = {"tokens": 0, "cached_tokens": 0, "forks": 0, "appends": 0, "cow": 0, "swapped_blocks": 0, "frees": 0,
+              "steps": 0}
+    ids = np.arange(len(prompts) * R, dtype=np.int32)
+    DECODE_STEPS = 8
+    max_blocks = (max(len(p) for p in prompts) + DECODE_STEPS + B - 1) // B
 
     def one_pass():
         bm = pa.BlockManager(nblk, B, num_host_blocks=nblk)
@@ -1026,15 +1030,25 @@ def run_block_manager(args):
             for i in range(1, R):
                 bm.fork(p * R, p * R + i)
                 counts["forks"] += 1
+        def decode_step():
+            # one decode step's host work: a token onto every sequence, then the
+            # padded block-table matrix and context lengths the attention call takes
+            _, cows = bm.append_batch(ids)
+            bm.block_tables(ids, max_blocks)
+            return int((cows[:, 0] >= 0).sum())
+
         t2 = time.perf_counter()
-        for s_ in range(len(prompts) * R):
-            _, pair = bm.append(s_)
-            counts["appends"] += 1
-            counts["cow"] += pair is not None
+        counts["cow"] += decode_step()  # the first step after the forks: copy-on-write of the shared blocks
+        counts["appends"] += len(ids)
+        t3 = time.perf_counter()
+        for _ in range(DECODE_STEPS - 1):
+            decode_step()
+        times["steady"] += time.perf_counter() - t3
+        counts["steps"] += DECODE_STEPS - 1
         base = len(prompts) * R  # swapping needs unshared blocks: 64 separate 1024-token sequences
         for j in range(64):
             bm.add_seq(base + j, 1024)
-        t3 = time.perf_counter()
+        t3s = time.perf_counter()  # the swap phase starts after that set-up
         for j in range(64):
             counts["swapped_blocks"] += len(bm.swap_out(base + j))
             bm.swap_in(base + j)
@@ -1043,7 +1057,7 @@ def run_block_manager(args):
             bm.free_seq(s_)
             counts["frees"] += 1
         t5 = time.perf_counter()
-        for k, a, b in (("admit", t0, t1), ("fork", t1, t2), ("append", t2, t3), ("swap", t3, t4), ("free", t4, t5)):
+        for k, a, b in (("admit", t0, t1), ("fork", t1, t2), ("append", t2, t3), ("swap", t3s, t4), ("free", t4, t5)):
             times[k] += b - a
 
     for _ in range(args.warmup):
@@ -1062,7 +1076,8 @@ def run_block_manager(args):
             "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
             "scaling": "none", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "config": {"workload": f"block_manager: {len(prompts)} prompts x {R} samples, {plan.prefix_len}-token "
-                                   f"system prompt + U[1,512] tokens, B={B}; admit, fork, append; 64 unshared "
+                                   f"system prompt + U[1,512] tokens, B={B}; admit, fork, {DECODE_STEPS} decode steps (each one "
+                                   f"append_batch + block_tables call over all {len(ids)} sequences); 64 unshared "
                                    f"1024-token sequences swapped out and in; free all; per step (host only, "
                                    f"through the C ABI from Python; prompts held as int32 arrays)"},
             "cached_fraction": round(counts["cached_tokens"] / max(counts["tokens"], 1), 4),
@@ -1071,6 +1086,8 @@ def run_block_manager(args):
                           "copy_on_write_share": round(counts["cow"] / max(counts["appends"], 1), 4),
                           "swap_blocks_out_and_in": rate(counts["swapped_blocks"], times["swap"]),
                           "free": rate(counts["frees"], times["free"])},
+            "decode_step_host_us": {"first_after_fork": round(times["append"] / args.steps * 1e6, 2),
+                                    "steady": round(times["steady"] / max(counts["steps"], 1) * 1e6, 2)},
             "gpu_launches": 0}
 
 

@@ -385,6 +385,16 @@ int pa_bm_fork(pa_bm *bm, int parent_id, int child_id);
  * cow_pair_out = {-1, -1}.  PA_ERR_OOM leaves the sequence unchanged. */
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]);
 
+/* One decode step's appends in one call: one token onto each of
+ * seq_ids[0..n-1] (distinct, resident sequences), in that order, exactly as
+ * n calls of pa_bm_append would do them.  slots_out[n] gets each token's
+ * slot and cow_pairs_out[n][2] each copy-on-write pair ({-1, -1} for none).
+ * Everything is checked before anything changes: PA_ERR_STATE (an unknown or
+ * swapped-out id), PA_ERR_INVALID (a repeated id, null pointers, n < 0) and
+ * PA_ERR_OOM (the step needs more free blocks than there are) leave the
+ * manager and the output arrays untouched.  n == 0 does nothing. */
+int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots_out, int64_t *cow_pairs_out);
+
 /* Drops seq_id: every block's ref_count - 1, blocks reaching 0 go back to the
  * free list (the <eos> path of [CHUNK]). */
 int pa_bm_free_seq(pa_bm *bm, int seq_id);
@@ -392,6 +402,16 @@ int pa_bm_free_seq(pa_bm *bm, int seq_id);
 /* Copies seq_id's block table into out[0..cap-1]; *n = its length.  Returns
  * PA_ERR_INVALID if cap < *n (nothing copied beyond cap). */
 int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n);
+
+/* The block tables of seq_ids[0..n-1] as one row-major int32 matrix
+ * out[n][max_blocks], the layout the attention calls take: row i holds
+ * sequence i's blocks, then pad up to max_blocks (the kernels never read
+ * past ceil(context_len / B) entries of a row).  context_lens_out[n] (may
+ * be NULL) gets each sequence's length in tokens.  PA_ERR_STATE (an unknown
+ * or swapped-out id) and PA_ERR_INVALID (a table longer than max_blocks,
+ * null pointers) are returned before anything is written. */
+int pa_bm_block_tables(const pa_bm *bm, const int32_t *seq_ids, int n, int32_t *out, int max_blocks, int32_t pad,
+                       int32_t *context_lens_out);
 
 /* Automatic prefix caching [SHARE]: like pa_bm_add_seq for a prompt of
  * num_tokens token ids, but every full block of the prompt is registered by

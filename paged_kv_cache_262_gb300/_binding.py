@@ -31,6 +31,7 @@ EXPORTS = (
     "pa_bm_add_seq_tokens", "pa_bm_num_cached_blocks", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
+    "pa_bm_append_batch", "pa_bm_block_tables",
 )
 
 
@@ -123,6 +124,10 @@ def load(path: Optional[str] = None):
         lib.pa_bm_free_seq.argtypes = [_P, i]
         lib.pa_bm_block_table.restype = i
         lib.pa_bm_block_table.argtypes = [_P, i, _c.POINTER(_c.c_int32), i, _c.POINTER(i)]
+        lib.pa_bm_append_batch.restype = i
+        lib.pa_bm_append_batch.argtypes = [_P, _P, i, _P, _P]
+        lib.pa_bm_block_tables.restype = i
+        lib.pa_bm_block_tables.argtypes = [_P, _P, i, _P, i, _c.c_int32, _P]
         lib.pa_bm_seq_len.restype = i
         lib.pa_bm_seq_len.argtypes = [_P, i]
         lib.pa_bm_ref_count.restype = i
@@ -490,6 +495,29 @@ class BlockManager:
         pair = (_c.c_int64 * 2)()
         _check(self._lib.pa_bm_append(self._h, int(seq_id), _c.byref(slot), pair), "pa_bm_append")
         return slot.value, (None if pair[0] < 0 else (pair[0], pair[1]))
+
+    def append_batch(self, seq_ids):
+        """One token onto each of `seq_ids` (distinct), in order, in one call.
+        Returns (slots int64 [n], cow_pairs int64 [n, 2]; -1 rows: no copy);
+        on an error nothing has changed."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32).reshape(-1)
+        slots = np.empty(ids.size, np.int64)
+        cows = np.empty((ids.size, 2), np.int64)
+        _check(self._lib.pa_bm_append_batch(self._h, ids.ctypes.data, int(ids.size), slots.ctypes.data,
+                                            cows.ctypes.data), "pa_bm_append_batch")
+        return slots, cows
+
+    def block_tables(self, seq_ids, max_blocks: int, pad: int = 0):
+        """Padded block-table matrix int32 [n, max_blocks] and context lengths
+        int32 [n] of `seq_ids`, as the attention calls take them."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32).reshape(-1)
+        out = np.empty((ids.size, int(max_blocks)), np.int32)
+        lens = np.empty(ids.size, np.int32)
+        _check(self._lib.pa_bm_block_tables(self._h, ids.ctypes.data, int(ids.size), out.ctypes.data,
+                                            int(max_blocks), int(pad), lens.ctypes.data), "pa_bm_block_tables")
+        return out, lens
 
     def free_seq(self, seq_id: int):
         _check(self._lib.pa_bm_free_seq(self._h, int(seq_id)), "pa_bm_free_seq")

@@ -15,7 +15,6 @@
 #include <cstdint>
 #include <new>
 #include <unordered_map>
-#include <unordered_set>
 #include <vector>
 
 #include "pagedattn.h"
@@ -26,6 +25,7 @@ struct Seq {
   std::vector<int32_t> blocks;  // device block ids, or host block ids while swapped out
   int len = 0;
   bool swapped = false;
+  uint64_t stamp = 0;  // last batch call that listed this sequence
 };
 
 // No C++ exception leaves an entry point: a failed allocation (the only
@@ -74,6 +74,13 @@ struct pa_bm {
   std::vector<int32_t> host_free;  // free host blocks (LIFO), for swapped-out sequences
   int num_host_blocks = 0;
   std::unordered_map<int, Seq> seqs;
+  // Scratch of the batch calls: a call number, per block the call that last
+  // counted it and how many of that call's sequences append into it.
+  uint64_t batch_no = 0;
+  std::vector<uint64_t> blk_stamp;
+  std::vector<int32_t> blk_count;
+  std::vector<Seq *> batch_seqs;
+  std::vector<const Seq *> batch_cseqs;
 
   static uint64_t key_hash(int32_t parent, const int32_t *tok, int n) {
     uint64_t h = 0x9E3779B97F4A7C15ull ^ (uint64_t)(uint32_t)parent;
@@ -134,6 +141,31 @@ struct pa_bm {
       ++nfree;
     }
   }
+  bool needs_block(const Seq &s) const {  // appending to s takes a free block
+    return s.len % block_size == 0 || ref[s.blocks[s.len / block_size]] > 1;
+  }
+  void grow(Seq &s) { s.blocks.reserve(std::max<size_t>(8, 2 * s.blocks.size())); }
+  // One token onto s; the caller checked that a block is free if one is
+  // needed and that s.blocks has room for a new one.  Never allocates.
+  void append_one(Seq &s, int64_t *slot_out, int64_t *cow_pair_out) {
+    const int B = block_size;
+    const int j = s.len;
+    cow_pair_out[0] = cow_pair_out[1] = -1;
+    if (j % B == 0) {  // the token opens a new block
+      s.blocks.push_back(take());
+    } else {
+      int32_t &last = s.blocks[j / B];
+      if (ref[last] > 1) {  // shared partial block: copy on write
+        const int32_t fresh = take();
+        cow_pair_out[0] = last;
+        cow_pair_out[1] = fresh;
+        drop(last);
+        last = fresh;
+      }
+    }
+    *slot_out = (int64_t)s.blocks[j / B] * B + (j % B);
+    s.len = j + 1;
+  }
   int32_t lookup(int32_t parent, const int32_t *tok) const {
     if (c_tok.empty()) return -1;
     const uint64_t h = key_hash(parent, tok, block_size);
@@ -188,6 +220,8 @@ pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_siz
     while (nb < (size_t)num_blocks) nb <<= 1;
     bm->bucket.assign(nb, -1);
     bm->bucket_mask = nb - 1;
+    bm->blk_stamp.assign(num_blocks, 0);
+    bm->blk_count.assign(num_blocks, 0);
     bm->num_host_blocks = num_host_blocks;
     bm->host_free.reserve(num_host_blocks);
     for (int b = num_host_blocks - 1; b >= 0; --b) bm->host_free.push_back(b);
@@ -234,34 +268,59 @@ int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[
   auto it = bm->seqs.find(seq_id);
   if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
   Seq &s = it->second;
-  const int B = bm->block_size;
-  const int j = s.len;
-  if (j == INT_MAX) return PA_ERR_INVALID;
-  cow_pair_out[0] = cow_pair_out[1] = -1;
-  if (j % B == 0) {  // the token opens a new block
-    if (bm->nfree == 0) return PA_ERR_OOM;
-    if (s.blocks.size() == s.blocks.capacity()) {  // grow before the block is taken
-      const int st = guarded([&]() -> int {
-        s.blocks.reserve(std::max<size_t>(8, 2 * s.blocks.size()));
-        return PA_OK;
-      });
-      if (st != PA_OK) return st;
-    }
-    s.blocks.push_back(bm->take());
-  } else {
-    int32_t &last = s.blocks[j / B];
-    if (bm->ref[last] > 1) {  // shared partial block: copy on write
-      if (bm->nfree == 0) return PA_ERR_OOM;
-      int32_t fresh = bm->take();
-      cow_pair_out[0] = last;
-      cow_pair_out[1] = fresh;
-      bm->drop(last);
-      last = fresh;
-    }
+  if (s.len == INT_MAX) return PA_ERR_INVALID;
+  if (bm->needs_block(s) && bm->nfree == 0) return PA_ERR_OOM;
+  if (s.len % bm->block_size == 0 && s.blocks.size() == s.blocks.capacity()) {
+    const int st = guarded([&]() -> int {
+      bm->grow(s);
+      return PA_OK;
+    });
+    if (st != PA_OK) return st;
   }
-  *slot_out = (int64_t)s.blocks[j / B] * B + (j % B);
-  s.len = j + 1;
+  bm->append_one(s, slot_out, cow_pair_out);
   return PA_OK;
+}
+
+int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots_out, int64_t *cow_pairs_out) {
+  if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out))) return PA_ERR_INVALID;
+  if (n == 0) return PA_OK;
+  return guarded([&]() -> int {
+    // every check and allocation first: a failure leaves no trace
+    bm->batch_seqs.resize(n);
+    Seq **sq = bm->batch_seqs.data();
+    const uint64_t call = ++bm->batch_no;
+    const int B = bm->block_size;
+    for (int i = 0; i < n; ++i) {
+      auto it = bm->seqs.find(seq_ids[i]);
+      if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
+      Seq &s = it->second;
+      if (s.stamp == call || s.len == INT_MAX) return PA_ERR_INVALID;  // listed twice
+      s.stamp = call;
+      sq[i] = &s;
+    }
+    // k of the batch appending into a partial block of ref_count r copy it
+    // min(k, r - 1) times: after r - 1 copies the last holder owns it alone
+    int64_t need = 0;
+    for (int i = 0; i < n; ++i) {
+      const Seq &s = *sq[i];
+      if (s.len % B == 0) {
+        ++need;
+        continue;
+      }
+      const int32_t x = s.blocks[s.len / B];
+      if (bm->ref[x] < 2) continue;
+      if (bm->blk_stamp[x] != call) {
+        bm->blk_stamp[x] = call;
+        bm->blk_count[x] = 0;
+      }
+      if (bm->blk_count[x]++ < bm->ref[x] - 1) ++need;
+    }
+    if (need > (int64_t)bm->nfree) return PA_ERR_OOM;
+    for (int i = 0; i < n; ++i)
+      if (sq[i]->len % B == 0 && sq[i]->blocks.size() == sq[i]->blocks.capacity()) bm->grow(*sq[i]);
+    for (int i = 0; i < n; ++i) bm->append_one(*sq[i], slots_out + i, cow_pairs_out + 2 * i);
+    return PA_OK;
+  });
 }
 
 int pa_bm_free_seq(pa_bm *bm, int seq_id) {
@@ -293,6 +352,30 @@ int pa_bm_block_table(const pa_bm *bm, int seq_id, int32_t *out, int cap, int *n
   if (cap < *n || (!out && *n > 0)) return PA_ERR_INVALID;
   std::copy(bl.begin(), bl.end(), out);
   return PA_OK;
+}
+
+int pa_bm_block_tables(const pa_bm *bm, const int32_t *seq_ids, int n, int32_t *out, int max_blocks, int32_t pad,
+                       int32_t *context_lens_out) {
+  if (!bm || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || (!out && max_blocks > 0)))) return PA_ERR_INVALID;
+  if (n == 0) return PA_OK;
+  pa_bm *m = const_cast<pa_bm *>(bm);  // only the scratch list of sequences changes
+  return guarded([&]() -> int {
+    m->batch_cseqs.resize(n);
+    const Seq **sq = m->batch_cseqs.data();
+    for (int i = 0; i < n; ++i) {  // check every id first: nothing is written on error
+      auto it = bm->seqs.find(seq_ids[i]);
+      if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
+      if ((int64_t)it->second.blocks.size() > max_blocks) return PA_ERR_INVALID;
+      sq[i] = &it->second;
+    }
+    for (int i = 0; i < n; ++i) {
+      int32_t *row = out + (size_t)i * max_blocks;
+      std::copy(sq[i]->blocks.begin(), sq[i]->blocks.end(), row);
+      std::fill(row + sq[i]->blocks.size(), row + max_blocks, pad);
+      if (context_lens_out) context_lens_out[i] = sq[i]->len;
+    }
+    return PA_OK;
+  });
 }
 
 int pa_bm_seq_len(const pa_bm *bm, int seq_id) {

@@ -138,6 +138,11 @@ int main() {
   ok = ok && inject("add_seq", bm, [&] { return (long long)pa_bm_add_seq(bm, 3, 9); }, OOM);
   for (int i = 0; i < 40 && ok; ++i)
     ok = inject("append (growing table)", bm, [&] { return (long long)pa_bm_append(bm, 3, &slot, cow); }, OOM);
+  ok = ok && pa_bm_fork(bm, 2, 5) == PA_OK;
+  const int32_t ids[4] = {5, 0, 2, 3};
+  int64_t bslots[4], bcows[8];
+  for (int i = 0; i < 6 && ok; ++i)
+    ok = inject("append_batch", bm, [&] { return (long long)pa_bm_append_batch(bm, ids, 4, bslots, bcows); }, OOM);
   ok = ok && inject("swap_out", bm, [&] { return (long long)pa_bm_swap_out(bm, 3, pairs, 64, &n); }, OOM);
   ok = ok && inject("wasted_slots", bm, [&] { return (long long)pa_bm_wasted_slots(bm); }, -1);
   ok = ok && inject("swap_in", bm, [&] { return (long long)pa_bm_swap_in(bm, 3, pairs, 64, &n); }, OOM);
@@ -148,7 +153,7 @@ int main() {
     std::printf("revived prompt found %d cached tokens, want 20\n", cached);
     ok = false;
   }
-  for (int q : {1, 3, 4})
+  for (int q : {1, 3, 4, 5})
     if (ok) ok = pa_bm_free_seq(bm, q) == PA_OK;
   if (ok && (pa_bm_num_free(bm) != kBlocks || pa_bm_num_free_host(bm) != kHost)) {
     std::printf("blocks lost: %d free of %d, %d host of %d\n", pa_bm_num_free(bm), kBlocks, pa_bm_num_free_host(bm),

@@ -320,6 +320,122 @@ def test_prefix_cache_drops_whole_subtrees_and_keeps_live_chains():
     assert bm.add_seq_tokens(6, d + d + a) == 4             # the live chain is still found
 
 
+def _state(bm, ids, N):
+    return ([bm.ref_count(b) for b in range(N)], bm.num_free(), bm.num_cached_blocks(),
+            {s: (bm.seq_len(s), bm.block_table(s)) for s in ids})
+
+
+def test_append_batch_equals_single_appends():
+    """A decode step's appends in one call give the same slots, copy-on-write
+    pairs, tables and reference counts as one call per sequence, through
+    forks whose samples share a partial block (some of the sharers appending,
+    or all of them) and sequences that open a new block."""
+    B, N = 4, 256
+    one, bat = pa.BlockManager(N, B), pa.BlockManager(N, B)
+    st = wl.Stream(91, 1)
+    u = st.uniform(4000)
+    k = 0
+    live = []
+    for p in range(12):
+        toks = [int(x) for x in st.integers(0, 1000, 1 + int(u[k] * 30))]
+        k += 1
+        for m in (one, bat):
+            m.add_seq_tokens(100 * p, toks)
+        live.append(100 * p)
+        for i in range(1, 1 + p % 4):           # 0..3 samples per prompt
+            for m in (one, bat):
+                m.fork(100 * p, 100 * p + i)
+            live.append(100 * p + i)
+    for step in range(12):
+        batch = [s for s in live if u[k + live.index(s)] < 0.8]  # most, not all, sequences this step
+        k += len(live)
+        sl, cw = bat.append_batch(batch)
+        for i, s in enumerate(batch):
+            slot, pair = one.append(s)
+            assert sl[i] == slot, (step, s)
+            assert (None if cw[i, 0] < 0 else (cw[i, 0], cw[i, 1])) == pair, (step, s)
+        assert _state(one, live, N) == _state(bat, live, N)
+    sl, cw = bat.append_batch([])
+    assert sl.shape == (0,) and cw.shape == (0, 2)
+
+
+def test_append_batch_checks_everything_first():
+    B = 4
+    bm = pa.BlockManager(8, B, num_host_blocks=4)
+    bm.add_seq(0, 6)                          # 2 blocks, the last half full
+    bm.fork(0, 1)
+    bm.fork(0, 2)                             # the partial block: ref_count 3
+    bm.add_seq(3, 4)                          # full: its next token opens a block
+    bm.add_seq(4, 1)
+    bm.swap_out(4)
+    before = _state(bm, [0, 1, 2, 3], 8)
+    assert bm.num_free() == 5
+    for ids, status in (([0, 9], pa.PA_ERR_STATE), ([0, 4], pa.PA_ERR_STATE), ([0, 1, 0], pa.PA_ERR_INVALID)):
+        with pytest.raises(pa.PaError) as e:
+            bm.append_batch(ids)
+        assert e.value.status == status and _state(bm, [0, 1, 2, 3], 8) == before
+    # all three sharers append: 2 copies (the last keeps the block) + 1 new block = 3 blocks
+    bm.add_seq(5, 2 * B)                      # leaves exactly 3 free
+    before = _state(bm, [0, 1, 2, 3, 5], 8)
+    bm.add_seq(6, 1)                          # leaves 2: one short
+    with pytest.raises(pa.PaError) as e:
+        bm.append_batch([0, 1, 2, 3])
+    assert e.value.status == pa.PA_ERR_OOM
+    bm.free_seq(6)
+    assert _state(bm, [0, 1, 2, 3, 5], 8) == before
+    sl, cw = bm.append_batch([0, 1, 2, 3])
+    assert bm.num_free() == 0
+    assert (cw[:, 0] >= 0).tolist() == [True, True, False, False]
+    assert len({int(x) // B for x in sl[:3]}) == 3          # three different blocks now
+
+
+def test_block_tables_matrix():
+    B = 16
+    bm = pa.BlockManager(64, B, num_host_blocks=8)
+    lens = [1, 16, 17, 100, 0]
+    for s, n in enumerate(lens):
+        bm.add_seq(s, n)
+    t, l = bm.block_tables([3, 0, 4, 2], 8, pad=-7)
+    assert l.tolist() == [100, 1, 0, 17]
+    for row, s in zip(t, [3, 0, 4, 2]):
+        bt = bm.block_table(s)
+        assert row[: len(bt)].tolist() == bt and (row[len(bt):] == -7).all()
+    with pytest.raises(pa.PaError) as e:
+        bm.block_tables([3], 6)                  # 100 tokens need 7 blocks
+    assert e.value.status == pa.PA_ERR_INVALID
+    bm.swap_out(1)
+    for ids in ([1], [99]):
+        with pytest.raises(pa.PaError) as e:
+            bm.block_tables(ids, 8)
+        assert e.value.status == pa.PA_ERR_STATE
+    t, l = bm.block_tables([], 8)
+    assert t.shape == (0, 8) and l.shape == (0,)
+
+
+def test_batch_calls_reject_bad_arguments_through_the_c_abi():
+    import ctypes
+    bm = pa.BlockManager(8, 4)
+    bm.add_seq(0, 3)
+    lib, h = bm._lib, bm._h
+    ids = np.array([0], np.int32)
+    slots, cows = np.zeros(1, np.int64), np.zeros((1, 2), np.int64)
+    out, lens = np.zeros((1, 4), np.int32), np.zeros(1, np.int32)
+    P = lambda a: a.ctypes.data  # noqa: E731
+    assert lib.pa_bm_append_batch(None, P(ids), 1, P(slots), P(cows)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_append_batch(h, P(ids), -1, P(slots), P(cows)) == pa.PA_ERR_INVALID
+    for args in ((None, P(slots), P(cows)), (P(ids), None, P(cows)), (P(ids), P(slots), None)):
+        assert lib.pa_bm_append_batch(h, args[0], 1, args[1], args[2]) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_append_batch(h, None, 0, None, None) == pa.PA_OK
+    assert lib.pa_bm_block_tables(None, P(ids), 1, P(out), 4, 0, P(lens)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_block_tables(h, P(ids), -1, P(out), 4, 0, P(lens)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_block_tables(h, P(ids), 1, P(out), -1, 0, P(lens)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_block_tables(h, None, 1, P(out), 4, 0, P(lens)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_block_tables(h, P(ids), 1, None, 4, 0, P(lens)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_block_tables(h, P(ids), 1, P(out), 4, 9, None) == pa.PA_OK  # lengths optional
+    assert out[0].tolist() == [bm.block_table(0)[0], 9, 9, 9]
+    assert bm.seq_len(0) == 3 and bm.num_free() == 7                              # nothing appended
+
+
 def test_failed_allocations_leave_no_trace(tmp_path):
     """Every host allocation inside every block-manager call made to fail in
     turn (a replaced operator new, in a C++ driver built with the block
@@ -341,8 +457,8 @@ def test_failed_allocations_leave_no_trace(tmp_path):
     assert r.stdout.startswith("ok ") and int(r.stdout.split()[1]) >= 20, r.stdout
 
 
-@pytest.mark.parametrize("N", [24, 64])
-def test_model_based_contents_through_cow_swap_and_prefix_cache(N):
+@pytest.mark.parametrize("N,batch", [(24, False), (64, False), (24, True), (64, True)])
+def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
     """Random prompts (some repeating earlier prompts' leading blocks), forks,
     appends, frees, swap-outs and swap-ins against simulated device and host
     page pools.  The test plays the caller: it writes each new token into the
@@ -353,7 +469,9 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N):
     resident tables holding it.  A slot holds what a key or value depends on:
     the token and every token before it (a fingerprint of the prefix), so a
     prefix-cache hit on a block whose content was computed after another
-    prefix fails the read-back."""
+    prefix fails the read-back.  With `batch`, appends go to a random subset
+    of the resident sequences in one append_batch call, and the step's copies
+    and writes are applied in the batch's order."""
     B, H = 8, 24
     bm = pa.BlockManager(N, B, num_host_blocks=H)
     dev = np.full((N, B), -1, np.int64)
@@ -425,6 +543,16 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N):
                     bm.fork(p, nxt)
                     model[nxt] = list(model[p])
                     nxt += 1
+            elif op < 0.6 and batch:
+                res = [s for s in model if s not in swapped]
+                sub = [s for i, s in enumerate(res) if u[(k * 31 + i) % 3000] < 0.5]
+                if sub:
+                    sl, cw = bm.append_batch(sub)
+                    for i, s in enumerate(sub):
+                        if cw[i, 0] >= 0:
+                            dev[cw[i, 1]] = dev[cw[i, 0]]
+                        model[s].append(next(fresh))
+                        dev[sl[i] // B, sl[i] % B] = fp(model[s])[-1]
             elif op < 0.6:
                 s = pick(lambda s: s not in swapped)
                 if s is not None:

@@ -28,7 +28,10 @@ def torch():
     return need_gpu()
 
 
-def test_serving_loop_matches_the_oracle(torch, ora):
+@pytest.mark.parametrize("batch", [False, True])
+def test_serving_loop_matches_the_oracle(torch, ora, batch):
+    """batch: each decode step's appends are one append_batch call and the
+    attention call's table matrix and context lengths come from block_tables."""
     st = wl.Stream(91, 4)
     bm = pa.BlockManager(N_DEV, B, num_host_blocks=N_HOST)
     kp = wl.normal_bf16(st, (N_DEV, HKV, B, D))   # never-used slots hold noise
@@ -108,7 +111,15 @@ def test_serving_loop_matches_the_oracle(torch, ora):
             swapped.discard(2)
         live = [s for s in sorted(toks) if s not in swapped]
         cow = []
-        for s in live:
+        if batch:
+            for s in live:
+                toks[s].append(int(st.integers(0, 30000, 1)[0]))
+            sl, cw = bm.append_batch(live)
+            for i, s in enumerate(live):
+                assert sl[i] == bm.block_table(s)[(len(toks[s]) - 1) // B] * B + (len(toks[s]) - 1) % B
+                if cw[i, 0] >= 0:
+                    cow.append((int(cw[i, 0]), int(cw[i, 1])))
+        for s in live if not batch else ():
             toks[s].append(int(st.integers(0, 30000, 1)[0]))
             slot, pair = bm.append(s)
             assert slot == bm.block_table(s)[(len(toks[s]) - 1) // B] * B + (len(toks[s]) - 1) % B
@@ -122,6 +133,10 @@ def test_serving_loop_matches_the_oracle(torch, ora):
             write(toks[s], bm.block_table(s), len(toks[s]) - 1)
         bt = tables(live)
         ctx = np.array([len(toks[s]) for s in live], np.int32)
+        if batch:
+            bt2, lens = bm.block_tables(live, bt.shape[1], pad=-1)
+            assert np.array_equal(bt2, bt) and np.array_equal(lens, ctx)
+            bt = bt2
         q = wl.normal_bf16(st, (len(live), HQ, D))
         out = pa.paged_attention_decode(bf16_dev(q, torch), dk, dv, torch.from_numpy(bt).cuda(),
                                         torch.from_numpy(ctx).cuda(), scale=SCALE, max_context_len=int(ctx.max()),
