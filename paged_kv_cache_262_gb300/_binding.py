@@ -162,6 +162,26 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+def _flag(err_flag) -> Optional[int]:
+    """The device error word the kernels OR their PA_DEVERR_* bits into."""
+    if err_flag is None:
+        return None
+    import torch
+    _need(err_flag, torch.int32, "err_flag")
+    if err_flag.numel() < 1:
+        raise ValueError("err_flag needs one int32")
+    return err_flag.data_ptr()
+
+
+def _ws(workspace) -> Optional[int]:
+    if workspace is None:
+        return None
+    import torch
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda or not workspace.is_contiguous():
+        raise TypeError("workspace must be a contiguous CUDA tensor")
+    return workspace.data_ptr()
+
+
 def _stream_ptr(stream) -> Optional[int]:
     import torch
     if stream is None:
@@ -179,6 +199,37 @@ def _need(t, dtype, name, ndim=None):
         raise ValueError(f"{name} must be contiguous")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def _shapes(*, rows=None, **named):
+    """Host-side checks a plain-pointer C ABI cannot make: every tensor on one
+    device, K and V pools alike, per-sequence arrays with a row for every
+    sequence, head_dim as in the pools.  `rows` is (name, count) pairs that
+    must have at least count rows."""
+    import torch
+    ts = [(n, t) for n, t in named.items() if t is not None]
+    dev = ts[0][1].device
+    if dev.type == "cuda" and dev.index != torch.cuda.current_device():
+        raise ValueError(f"{ts[0][0]} is on {dev}, the current device is cuda:{torch.cuda.current_device()}")
+    for n, t in ts:
+        if t.device != dev:
+            raise ValueError(f"{n} is on {t.device}, {ts[0][0]} on {dev}")
+    kp, vp = named.get("k_pool"), named.get("v_pool")
+    if kp is not None and vp is not None and tuple(kp.shape) != tuple(vp.shape):
+        raise ValueError(f"k_pool {tuple(kp.shape)} and v_pool {tuple(vp.shape)} differ")
+    for n, need in rows or ():
+        if named[n].shape[0] < need:
+            raise ValueError(f"{n} has {named[n].shape[0]} rows, needs {need}")
+
+
+def _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, num_seqs, qname="q", oname="out",
+                 tname="block_tables", cname="context_lens"):
+    _shapes(**{qname: q, "k_pool": k_pool, "v_pool": v_pool, tname: block_tables, cname: context_lens,
+               oname: out}, rows=((tname, num_seqs), (cname, num_seqs)))
+    if q.shape[2] != k_pool.shape[3]:
+        raise ValueError(f"{qname} head_dim {q.shape[2]} != the pools' {k_pool.shape[3]}")
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError(f"{oname} must have {qname}'s shape {tuple(q.shape)}")
 
 
 def make_desc(q, k_pool, block_tables, *, num_seqs=None, scale=None, max_context_len=None) -> DecodeDesc:
@@ -225,13 +276,14 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=No
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out", 3)
+    _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, q.shape[0])
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
         workspace = decode_workspace(desc, q.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pa_paged_attention_decode(_c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                           _ptr(block_tables), _ptr(context_lens), _ptr(out),
-                                          _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
+                                          _ws(workspace), ws_bytes, _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode")
     return out
 
@@ -259,6 +311,8 @@ def paged_attention_decode_append(q, new_k, new_v, slot_mapping, k_pool, v_pool,
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out", 3)
+    _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, S)
+    _shapes(q=q, new_k=new_k, new_v=new_v, slot_mapping=slot_mapping)
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
         workspace = decode_workspace(desc, q.device)
@@ -266,7 +320,7 @@ def paged_attention_decode_append(q, new_k, new_v, slot_mapping, k_pool, v_pool,
     st = load().pa_paged_attention_decode_append(_c.byref(desc), _ptr(q), _ptr(new_k), _ptr(new_v),
                                                  _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool),
                                                  _ptr(block_tables), _ptr(context_lens), _ptr(out),
-                                                 _ptr(workspace), ws_bytes, _ptr(err_flag), _stream_ptr(stream))
+                                                 _ws(workspace), ws_bytes, _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode_append")
     return out
 
@@ -294,6 +348,14 @@ def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, contex
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out", 3)
+    _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, q.shape[0])
+    ng0 = int(group_prefix_lens.shape[0])
+    _shapes(q=q, group_starts=group_starts, group_prefix_lens=group_prefix_lens, prefix_tables=prefix_tables,
+            subgroup_starts=subgroup_starts, subgroup_shared_lens=subgroup_shared_lens,
+            rows=(("group_starts", ng0 + 1 if ng0 else 0), ("prefix_tables", ng0)))
+    if subgroup_shared_lens is not None and subgroup_starts is not None and \
+            subgroup_starts.shape[0] < subgroup_shared_lens.shape[0] + 1:
+        raise ValueError("subgroup_starts needs num_subgroups + 1 entries")
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
         need = int(load().pa_shared_prefix_workspace_bytes(_c.byref(desc)))
@@ -307,8 +369,8 @@ def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, contex
         st = load().pa_paged_attention_decode_shared_prefix(
             _c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), ng,
             _ptr(group_starts), _ptr(group_prefix_lens), _ptr(prefix_tables), int(prefix_tables.shape[1]),
-            int(max_group_size), int(max_prefix_len), _ptr(out), _ptr(workspace),
-            workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream_ptr(stream))
+            int(max_group_size), int(max_prefix_len), _ptr(out), _ws(workspace),
+            workspace.numel() * workspace.element_size(), _flag(err_flag), _stream_ptr(stream))
         _check(st, "pa_paged_attention_decode_shared_prefix")
         return out
     _need(subgroup_starts, torch.int32, "subgroup_starts", 1)
@@ -317,8 +379,8 @@ def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, contex
         _c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), ng,
         _ptr(group_starts), _ptr(group_prefix_lens), _ptr(prefix_tables), int(prefix_tables.shape[1]),
         int(max_group_size), int(max_prefix_len), int(subgroup_shared_lens.shape[0]), _ptr(subgroup_starts),
-        _ptr(subgroup_shared_lens), int(max_subgroup_size), _ptr(out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(err_flag), _stream_ptr(stream))
+        _ptr(subgroup_shared_lens), int(max_subgroup_size), _ptr(out), _ws(workspace),
+        workspace.numel() * workspace.element_size(), _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode_shared_prefix2")
     return out
 
@@ -336,10 +398,11 @@ def paged_attention_decode_noalloc(q, k_pool, v_pool, block_tables, context_lens
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out", 3)
+    _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, q.shape[0])
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     st = load().pa_paged_attention_decode_noalloc(_c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                                   _ptr(block_tables), _ptr(context_lens), _ptr(out),
-                                                  _ptr(err_flag), _stream_ptr(stream))
+                                                  _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_decode_noalloc")
     return out
 
@@ -357,11 +420,14 @@ def paged_attention_prefill_chunk(q, cu_q, k_pool, v_pool, block_tables, context
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out", 3)
+    R = context_lens.shape[0]
+    _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, R)
+    _shapes(q=q, cu_q=cu_q, rows=(("cu_q", R + 1),))
     desc = make_desc(q, k_pool, block_tables, num_seqs=context_lens.shape[0], scale=scale,
                      max_context_len=max_context_len)
     st = load().pa_paged_attention_prefill_chunk(_c.byref(desc), _ptr(q), _ptr(cu_q), int(max_q_len),
                                                  int(q.shape[0]), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
-                                                 _ptr(context_lens), _ptr(out), _ptr(err_flag),
+                                                 _ptr(context_lens), _ptr(out), _flag(err_flag),
                                                  _stream_ptr(stream))
     _check(st, "pa_paged_attention_prefill_chunk")
     return out
@@ -389,6 +455,13 @@ def paged_attention_mixed(prefill_q, cu_q, prefill_tables, prefill_context_lens,
         decode_out = torch.empty_like(decode_q)
     _need(prefill_out, torch.bfloat16, "prefill_out", 3)
     _need(decode_out, torch.bfloat16, "decode_out", 3)
+    R = prefill_context_lens.shape[0]
+    _attn_shapes(prefill_q, k_pool, v_pool, prefill_tables, prefill_context_lens, prefill_out, R, "prefill_q",
+                 "prefill_out", "prefill_tables", "prefill_context_lens")
+    _shapes(prefill_q=prefill_q, cu_q=cu_q, rows=(("cu_q", R + 1),))
+    _attn_shapes(decode_q, k_pool, v_pool, decode_tables, decode_context_lens, decode_out, decode_q.shape[0],
+                 "decode_q", "decode_out", "decode_tables", "decode_context_lens")
+    _shapes(prefill_q=prefill_q, decode_q=decode_q)
     pdesc = make_desc(prefill_q, k_pool, prefill_tables, num_seqs=prefill_context_lens.shape[0], scale=scale,
                       max_context_len=prefill_max_context_len)
     ddesc = make_desc(decode_q, k_pool, decode_tables, scale=scale, max_context_len=decode_max_context_len)
@@ -398,8 +471,8 @@ def paged_attention_mixed(prefill_q, cu_q, prefill_tables, prefill_context_lens,
     st = load().pa_paged_attention_mixed(_c.byref(pdesc), _ptr(prefill_q), _ptr(cu_q), int(max_q_len),
                                          int(prefill_q.shape[0]), _ptr(prefill_tables), _ptr(prefill_context_lens),
                                          _ptr(prefill_out), _c.byref(ddesc), _ptr(decode_q), _ptr(decode_tables),
-                                         _ptr(decode_context_lens), _ptr(decode_out), _ptr(workspace), ws_bytes,
-                                         _ptr(k_pool), _ptr(v_pool), _ptr(err_flag), _stream_ptr(stream))
+                                         _ptr(decode_context_lens), _ptr(decode_out), _ws(workspace), ws_bytes,
+                                         _ptr(k_pool), _ptr(v_pool), _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_paged_attention_mixed")
     return prefill_out, decode_out
 
@@ -413,9 +486,13 @@ def reshape_and_cache(k, v, k_pool, v_pool, slot_mapping, *, err_flag=None, stre
     _need(v_pool, torch.bfloat16, "v_pool", 4)
     _need(slot_mapping, torch.int64, "slot_mapping", 1)
     nblk, hkv, bs, d = k_pool.shape
+    _shapes(k=k, v=v, k_pool=k_pool, v_pool=v_pool, slot_mapping=slot_mapping)
+    T = slot_mapping.shape[0]
+    if tuple(k.shape) != (T, hkv, d) or tuple(v.shape) != (T, hkv, d):
+        raise ValueError(f"k and v must be [{T}][{hkv}][{d}] (a row per slot_mapping entry)")
     st = load().pa_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_pool), _ptr(v_pool), _ptr(slot_mapping),
                                      int(slot_mapping.shape[0]), int(hkv), int(d), int(bs), int(nblk),
-                                     _ptr(err_flag), _stream_ptr(stream))
+                                     _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_reshape_and_cache")
 
 
@@ -428,12 +505,17 @@ def copy_blocks(k_pools: Sequence, v_pools: Sequence, block_pairs, *, err_flag=N
     for t in list(k_pools) + list(v_pools):
         _need(t, torch.bfloat16, "pool", 4)
     _need(block_pairs, torch.int64, "block_pairs", 2)
+    for t in list(k_pools) + list(v_pools):
+        if tuple(t.shape) != tuple(k_pools[0].shape) or t.device != block_pairs.device:
+            raise ValueError("every pool must have the first pool's shape, on block_pairs' device")
+    if block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be [num_pairs][2]")
     nblk = k_pools[0].shape[0]
     blk_bytes = k_pools[0][0].numel() * 2
     kp = (_P * L)(*[t.data_ptr() for t in k_pools])
     vp = (_P * L)(*[t.data_ptr() for t in v_pools])
     st = load().pa_copy_blocks(kp, vp, L, _ptr(block_pairs), int(block_pairs.shape[0]), int(nblk),
-                               int(blk_bytes), _ptr(err_flag), _stream_ptr(stream))
+                               int(blk_bytes), _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_copy_blocks")
 
 
@@ -453,10 +535,17 @@ def swap_blocks(src_k_pools: Sequence, src_v_pools: Sequence, dst_k_pools: Seque
             if not t.is_cuda and not t.is_pinned():
                 raise ValueError("host pools must be pinned")
     _need(block_pairs, torch.int64, "block_pairs", 2)
+    if block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be [num_pairs][2]")
+    for p in pools:
+        if any(tuple(t.shape) != tuple(p[0].shape) for t in p):
+            raise ValueError("the pools of one side must all have the same shape")
+    if tuple(src_k_pools[0].shape[1:]) != tuple(dst_k_pools[0].shape[1:]):
+        raise ValueError("source and destination blocks must have the same shape")
     arr = [(_P * L)(*[t.data_ptr() for t in p]) for p in pools]
     st = load().pa_swap_blocks(arr[0], arr[1], arr[2], arr[3], L, _ptr(block_pairs), int(block_pairs.shape[0]),
                                int(src_k_pools[0].shape[0]), int(dst_k_pools[0].shape[0]),
-                               int(src_k_pools[0][0].numel() * 2), _ptr(err_flag), _stream_ptr(stream))
+                               int(src_k_pools[0][0].numel() * 2), _flag(err_flag), _stream_ptr(stream))
     _check(st, "pa_swap_blocks")
 
 

@@ -121,3 +121,37 @@ def test_new_entry_points_validate_before_any_gpu_work(lib):
     assert call_sp2(d, 2, 16, 16, 5) == pa.PA_ERR_UNSUPPORTED   # 5 members x 4 heads > 16 query rows
     assert call_sp2(_desc(head_dim=64), 2, 16, 16, 2) == pa.PA_ERR_UNSUPPORTED
     assert call_sp2(_desc(num_seqs=0), 2, 16, 16, 4) == pa.PA_OK  # nothing to decode
+
+
+def test_binding_checks_shapes_and_devices_before_any_call():
+    """The plain-pointer C ABI cannot see buffer sizes, so the binding refuses
+    arguments that would make a kernel read or write past a tensor: K and V
+    pools of different shapes, per-sequence arrays shorter than the batch, a
+    head_dim unlike the pools', an output of another shape, tensors on
+    different devices."""
+    import torch
+    from paged_kv_cache_262_gb300 import _binding as b
+    kp = torch.zeros(8, 2, 16, 64, dtype=torch.bfloat16)
+    q = torch.zeros(3, 4, 64, dtype=torch.bfloat16)
+    bt = torch.zeros(3, 5, dtype=torch.int32)
+    ctx = torch.zeros(3, dtype=torch.int32)
+    b._attn_shapes(q, kp, kp.clone(), bt, ctx, q.clone(), 3)            # consistent: no error
+    bad = [
+        (q, kp, torch.zeros(7, 2, 16, 64, dtype=torch.bfloat16), bt, ctx, q, 3),   # v_pool smaller
+        (q, kp, kp, bt[:2], ctx, q, 3),                                            # a table row short
+        (q, kp, kp, bt, ctx[:2], q, 3),                                            # a context length short
+        (torch.zeros(3, 4, 128, dtype=torch.bfloat16), kp, kp, bt, ctx,
+         torch.zeros(3, 4, 128, dtype=torch.bfloat16), 3),                         # head_dim 128 vs 64
+        (q, kp, kp, bt, ctx, q[:2], 3),                                            # out of another shape
+        (q, kp, kp, bt.to("meta"), ctx, q, 3),                                     # another device
+    ]
+    for args in bad:
+        with pytest.raises(ValueError):
+            b._attn_shapes(*args)
+    with pytest.raises(ValueError):
+        b._shapes(group_starts=torch.zeros(2, dtype=torch.int32), rows=(("group_starts", 3),))
+    with pytest.raises(TypeError):
+        b._flag(torch.zeros(1, dtype=torch.int32))                         # a host error word
+    with pytest.raises(TypeError):
+        b._ws(torch.zeros(16, dtype=torch.uint8))                          # a host workspace
+    assert b._flag(None) is None and b._ws(None) is None
