@@ -246,21 +246,38 @@ def decode_workspace_bytes(desc: DecodeDesc) -> int:
 
 
 _WS = {}
+_WS_SP = {}
 
 
-def decode_workspace(desc: DecodeDesc, device):
-    """A workspace of the size the call needs, cached per device and reused
-    (its contents need no clearing between calls)."""
+def _cached_ws(cache, need, device, stream):
+    """A workspace of at least `need` bytes for launches on `stream` (None:
+    the device's current stream), cached per (device, stream) and reused by
+    later calls on that stream, which run after the earlier ones; its
+    contents need no clearing between calls.  Calls on different streams
+    get different workspaces, so they may run at the same time.  It is
+    allocated on its stream, so replacing it with a larger one never hands
+    its memory to other work while a launch on that stream may still use
+    it."""
     import torch
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    s = stream if stream is not None else torch.cuda.current_stream(idx)
+    key = (idx, s.cuda_stream)
+    ws = cache.get(key)
+    if ws is None or ws.numel() < need:
+        with torch.cuda.stream(s):
+            ws = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda", idx))
+        cache[key] = ws
+    return ws
+
+
+def decode_workspace(desc: DecodeDesc, device, stream=None):
+    """The workspace a decode call of `desc` needs on `stream` (None: the
+    current stream), or None when it needs none; see _cached_ws."""
     need = decode_workspace_bytes(desc)
     if need == 0:
         return None
-    key = torch.device(device).index
-    ws = _WS.get(key)
-    if ws is None or ws.numel() < need:
-        ws = torch.empty(need, dtype=torch.uint8, device=device)
-        _WS[key] = ws
-    return ws
+    return _cached_ws(_WS, need, device, stream)
 
 
 # --------------------------------------------------------------- the four calls
@@ -279,7 +296,7 @@ def paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, out=No
     _attn_shapes(q, k_pool, v_pool, block_tables, context_lens, out, q.shape[0])
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
-        workspace = decode_workspace(desc, q.device)
+        workspace = decode_workspace(desc, q.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pa_paged_attention_decode(_c.byref(desc), _ptr(q), _ptr(k_pool), _ptr(v_pool),
                                           _ptr(block_tables), _ptr(context_lens), _ptr(out),
@@ -315,7 +332,7 @@ def paged_attention_decode_append(q, new_k, new_v, slot_mapping, k_pool, v_pool,
     _shapes(q=q, new_k=new_k, new_v=new_v, slot_mapping=slot_mapping)
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
-        workspace = decode_workspace(desc, q.device)
+        workspace = decode_workspace(desc, q.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pa_paged_attention_decode_append(_c.byref(desc), _ptr(q), _ptr(new_k), _ptr(new_v),
                                                  _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool),
@@ -326,8 +343,6 @@ def paged_attention_decode_append(q, new_k, new_v, slot_mapping, k_pool, v_pool,
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
-
-_WS_SP = {}
 
 
 def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, context_lens, group_starts,
@@ -359,11 +374,7 @@ def paged_attention_decode_shared_prefix(q, k_pool, v_pool, block_tables, contex
     desc = make_desc(q, k_pool, block_tables, scale=scale, max_context_len=max_context_len)
     if workspace is None:
         need = int(load().pa_shared_prefix_workspace_bytes(_c.byref(desc)))
-        key = q.device.index
-        workspace = _WS_SP.get(key)
-        if workspace is None or workspace.numel() < need:
-            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-            _WS_SP[key] = workspace
+        workspace = _cached_ws(_WS_SP, need, q.device, stream)
     ng = int(group_prefix_lens.shape[0])
     if subgroup_starts is None:
         st = load().pa_paged_attention_decode_shared_prefix(
@@ -466,7 +477,7 @@ def paged_attention_mixed(prefill_q, cu_q, prefill_tables, prefill_context_lens,
                       max_context_len=prefill_max_context_len)
     ddesc = make_desc(decode_q, k_pool, decode_tables, scale=scale, max_context_len=decode_max_context_len)
     if workspace is None:
-        workspace = decode_workspace(ddesc, decode_q.device)
+        workspace = decode_workspace(ddesc, decode_q.device, stream)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().pa_paged_attention_mixed(_c.byref(pdesc), _ptr(prefill_q), _ptr(cu_q), int(max_q_len),
                                          int(prefill_q.shape[0]), _ptr(prefill_tables), _ptr(prefill_context_lens),

@@ -155,3 +155,127 @@ def test_binding_checks_shapes_and_devices_before_any_call():
     with pytest.raises(TypeError):
         b._ws(torch.zeros(16, dtype=torch.uint8))                          # a host workspace
     assert b._flag(None) is None and b._ws(None) is None
+
+
+def test_default_workspaces_are_per_stream(monkeypatch):
+    """Calls that pass no workspace share one per (device, stream): calls on
+    one stream reuse it (they run in order), a call on another stream gets
+    its own (the two may run at once), and each is allocated on its stream.
+    torch.cuda's stream calls are faked, so this runs without a GPU."""
+    import contextlib
+    import torch
+    from paged_kv_cache_262_gb300 import _binding as b
+
+    class S:
+        def __init__(self, h):
+            self.cuda_stream = h
+
+    cur, active, made = S(7), [], []
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: cur)
+
+    @contextlib.contextmanager
+    def on(s):
+        active.append(s)
+        yield
+        active.pop()
+
+    monkeypatch.setattr(torch.cuda, "stream", on)
+    real_empty = torch.empty
+
+    def fake_empty(n, dtype=None, device=None):
+        made.append((n, active[-1].cuda_stream if active else None, device))
+        return real_empty(n, dtype=dtype)
+
+    monkeypatch.setattr(torch, "empty", fake_empty)
+    cache = {}
+    a = b._cached_ws(cache, 100, "cuda", None)                     # the current stream (7)
+    assert b._cached_ws(cache, 80, "cuda", None) is a               # same stream: reused
+    other = S(9)
+    c = b._cached_ws(cache, 100, "cuda", other)
+    assert c is not a                                               # another stream: its own
+    d = b._cached_ws(cache, 200, torch.device("cuda", 0), None)     # grown, on stream 7
+    assert d is not a and d.numel() == 200
+    assert b._cached_ws(cache, 100, "cuda", other) is c
+    assert [m[:2] for m in made] == [(100, 7), (100, 9), (200, 7)]
+    assert all(m[2] == torch.device("cuda", 0) for m in made)
+
+
+def test_every_wrapper_marshals_its_call_without_a_gpu(monkeypatch):
+    """Each attention and cache wrapper runs end to end on CPU tensors against
+    a recording stand-in for the library (the CUDA checks and torch.cuda's
+    stream calls faked): every argument check passes on consistent shapes,
+    the call reaches the library with the sizes it should, and a default
+    workspace is taken from the per-stream cache."""
+    import contextlib
+    import torch
+    import paged_kv_cache_262_gb300 as pa
+    from paged_kv_cache_262_gb300 import _binding as b
+
+    calls = []
+
+    class Lib:
+        def __getattr__(self, name):
+            def f(*args):
+                calls.append((name, args))
+                return 4096 if name.endswith("workspace_bytes") else 0
+            return f
+
+    class S:
+        cuda_stream = 7
+
+    def need(t, dtype, name, ndim=None):  # _need without the device check
+        assert isinstance(t, torch.Tensor) and t.dtype == dtype and t.is_contiguous(), name
+        assert ndim is None or t.dim() == ndim, name
+
+    monkeypatch.setattr(b, "load", lambda path=None: Lib())
+    monkeypatch.setattr(b, "_need", need)
+    monkeypatch.setattr(b, "_ws", lambda w: None if w is None else w.data_ptr())
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: S())
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
+    real_empty = torch.empty
+    monkeypatch.setattr(torch, "empty", lambda *a, **k: real_empty(*a, **{x: y for x, y in k.items() if x != "device"}))
+    monkeypatch.setattr(b, "_WS", {})
+    monkeypatch.setattr(b, "_WS_SP", {})
+
+    bf, i32, i64 = torch.bfloat16, torch.int32, torch.int64
+    S_, HQ, HKV, D, B, NB, MB = 4, 8, 2, 128, 16, 32, 6
+    kp, vp = torch.zeros(NB, HKV, B, D, dtype=bf), torch.zeros(NB, HKV, B, D, dtype=bf)
+    q = torch.zeros(S_, HQ, D, dtype=bf)
+    bt, ctx = torch.zeros(S_, MB, dtype=i32), torch.full((S_,), 40, dtype=i32)
+    err = torch.zeros(1, dtype=i32)
+    nk, nv, slots = torch.zeros(S_, HKV, D, dtype=bf), torch.zeros(S_, HKV, D, dtype=bf), torch.zeros(S_, dtype=i64)
+
+    pa.paged_attention_decode(q, kp, vp, bt, ctx, err_flag=err)
+    pa.paged_attention_decode_append(q, nk, nv, slots, kp, vp, bt, ctx, err_flag=err)
+    pa.paged_attention_decode_noalloc(q, kp, vp, bt, ctx, err_flag=err)
+    gs, gp, pt = torch.tensor([0, 2], dtype=i32), torch.tensor([32], dtype=i32), torch.zeros(1, 2, dtype=i32)
+    pa.paged_attention_decode_shared_prefix(q, kp, vp, bt, ctx, gs, gp, pt, max_group_size=2, max_prefix_len=32,
+                                            err_flag=err)
+    pa.paged_attention_decode_shared_prefix(q, kp, vp, bt, ctx, gs, gp, pt, max_group_size=2, max_prefix_len=32,
+                                            subgroup_starts=torch.tensor([0, 2, 4], dtype=i32),
+                                            subgroup_shared_lens=torch.tensor([16, 0], dtype=i32),
+                                            max_subgroup_size=2, err_flag=err)
+    cu = torch.tensor([0, 5, 9], dtype=i32)
+    pq = torch.zeros(9, HQ, D, dtype=bf)
+    pa.paged_attention_prefill_chunk(pq, cu, kp, vp, bt[:2], ctx[:2], max_q_len=5, err_flag=err)
+    pa.paged_attention_mixed(pq, cu, bt[:2], ctx[:2], q, bt, ctx, kp, vp, max_q_len=5, err_flag=err)
+    pa.reshape_and_cache(nk, nv, kp, vp, slots, err_flag=err)
+    pa.copy_blocks([kp], [vp], torch.tensor([[1, 2]], dtype=i64), err_flag=err)
+
+    names = [n for n, _ in calls if not n.endswith("workspace_bytes")]
+    assert names == ["pa_paged_attention_decode", "pa_paged_attention_decode_append",
+                     "pa_paged_attention_decode_noalloc", "pa_paged_attention_decode_shared_prefix",
+                     "pa_paged_attention_decode_shared_prefix2", "pa_paged_attention_prefill_chunk",
+                     "pa_paged_attention_mixed", "pa_reshape_and_cache", "pa_copy_blocks"]
+    args = dict(calls)
+    assert args["pa_reshape_and_cache"][5:10] == (S_, HKV, D, B, NB)
+    assert args["pa_paged_attention_prefill_chunk"][3:5] == (5, 9)
+    assert args["pa_paged_attention_decode_shared_prefix2"][13] == 2            # sub-groups
+    assert len(b._WS) == 1 and len(b._WS_SP) == 1                              # one per (device, stream)
+    # and a mismatched pool is refused before the library is reached
+    n = len(calls)
+    with pytest.raises(ValueError):
+        pa.paged_attention_decode(q, kp, vp[:-1].contiguous(), bt, ctx)
+    assert len(calls) == n
