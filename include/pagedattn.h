@@ -356,8 +356,10 @@ int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *con
  * tables, per-block reference counts.  Blocks are allocated on demand (a
  * sequence of n tokens holds ceil(n / B) blocks), shared by fork, copied on
  * write when a sharer appends into a block with ref_count > 1, and returned to
- * the free list when the last reference is dropped.  The free list is LIFO;
- * initially blocks are handed out in increasing id order.  Not thread safe.
+ * the free pool when the last reference is dropped.  Free blocks that hold no
+ * prefix-cache content are handed out first, most recently freed first
+ * (initially in increasing id order); free blocks still in the prefix cache
+ * only after them, least recently freed first.  Not thread safe.
  * No C++ exception leaves these calls: a failed host allocation returns
  * PA_ERR_OOM (NULL from the create calls, -1 from pa_bm_wasted_slots) and
  * leaves the manager as it was before the call.
@@ -385,15 +387,29 @@ int pa_bm_fork(pa_bm *bm, int parent_id, int child_id);
  * cow_pair_out = {-1, -1}.  PA_ERR_OOM leaves the sequence unchanged. */
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]);
 
+/* pa_bm_append with the token's id.  While every token id of seq_id is known
+ * (it was admitted by pa_bm_add_seq_tokens, or forked from such a sequence,
+ * and every append since gave its id), a block this token fills is
+ * registered in the prefix cache like a prompt's full block -- when the
+ * blocks before it are registered, so that a lookup from the start can
+ * reach it -- and a later prompt that repeats the sequence (the next turn of
+ * a conversation: earlier prompt, generated answer, new message) finds it.
+ * Its K/V are valid once this step's cache write of the token has run.
+ * pa_bm_append (no id) ends the tracking: none of the sequence's later
+ * blocks is registered. */
+int pa_bm_append_token(pa_bm *bm, int seq_id, int32_t token, int64_t *slot_out, int64_t cow_pair_out[2]);
+
 /* One decode step's appends in one call: one token onto each of
  * seq_ids[0..n-1] (distinct, resident sequences), in that order, exactly as
- * n calls of pa_bm_append would do them.  slots_out[n] gets each token's
- * slot and cow_pairs_out[n][2] each copy-on-write pair ({-1, -1} for none).
+ * n calls of pa_bm_append_token (tokens[n] given) or pa_bm_append (tokens
+ * NULL) would do them.  slots_out[n] gets each token's slot and
+ * cow_pairs_out[n][2] each copy-on-write pair ({-1, -1} for none).
  * Everything is checked before anything changes: PA_ERR_STATE (an unknown or
  * swapped-out id), PA_ERR_INVALID (a repeated id, null pointers, n < 0) and
  * PA_ERR_OOM (the step needs more free blocks than there are) leave the
  * manager and the output arrays untouched.  n == 0 does nothing. */
-int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots_out, int64_t *cow_pairs_out);
+int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, const int32_t *tokens, int n, int64_t *slots_out,
+                       int64_t *cow_pairs_out);
 
 /* Drops seq_id: every block's ref_count - 1, blocks reaching 0 go back to the
  * free list (the <eos> path of [CHUNK]). */

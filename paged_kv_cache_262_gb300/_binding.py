@@ -31,7 +31,7 @@ EXPORTS = (
     "pa_bm_add_seq_tokens", "pa_bm_num_cached_blocks", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
-    "pa_bm_append_batch", "pa_bm_block_tables",
+    "pa_bm_append_batch", "pa_bm_block_tables", "pa_bm_append_token",
 )
 
 
@@ -125,7 +125,9 @@ def load(path: Optional[str] = None):
         lib.pa_bm_block_table.restype = i
         lib.pa_bm_block_table.argtypes = [_P, i, _c.POINTER(_c.c_int32), i, _c.POINTER(i)]
         lib.pa_bm_append_batch.restype = i
-        lib.pa_bm_append_batch.argtypes = [_P, _P, i, _P, _P]
+        lib.pa_bm_append_batch.argtypes = [_P, _P, _P, i, _P, _P]
+        lib.pa_bm_append_token.restype = i
+        lib.pa_bm_append_token.argtypes = [_P, i, _c.c_int32, _c.POINTER(i64), _c.POINTER(i64)]
         lib.pa_bm_block_tables.restype = i
         lib.pa_bm_block_tables.argtypes = [_P, _P, i, _P, i, _c.c_int32, _P]
         lib.pa_bm_seq_len.restype = i
@@ -589,23 +591,35 @@ class BlockManager:
     def fork(self, parent: int, child: int):
         _check(self._lib.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")
 
-    def append(self, seq_id: int):
-        """Returns (slot, cow_pair or None)."""
+    def append(self, seq_id: int, token: Optional[int] = None):
+        """Returns (slot, cow_pair or None).  With the token's id, a block it
+        fills is registered in the prefix cache (pa_bm_append_token)."""
         slot = _c.c_int64()
         pair = (_c.c_int64 * 2)()
-        _check(self._lib.pa_bm_append(self._h, int(seq_id), _c.byref(slot), pair), "pa_bm_append")
+        if token is None:
+            _check(self._lib.pa_bm_append(self._h, int(seq_id), _c.byref(slot), pair), "pa_bm_append")
+        else:
+            _check(self._lib.pa_bm_append_token(self._h, int(seq_id), int(token), _c.byref(slot), pair),
+                   "pa_bm_append_token")
         return slot.value, (None if pair[0] < 0 else (pair[0], pair[1]))
 
-    def append_batch(self, seq_ids):
-        """One token onto each of `seq_ids` (distinct), in order, in one call.
-        Returns (slots int64 [n], cow_pairs int64 [n, 2]; -1 rows: no copy);
-        on an error nothing has changed."""
+    def append_batch(self, seq_ids, tokens=None):
+        """One token onto each of `seq_ids` (distinct), in order, in one call;
+        `tokens` (optional, one id per sequence) as in append.  Returns
+        (slots int64 [n], cow_pairs int64 [n, 2]; -1 rows: no copy); on an
+        error nothing has changed."""
         import numpy as np
         ids = np.ascontiguousarray(seq_ids, dtype=np.int32).reshape(-1)
+        tok = None
+        if tokens is not None:
+            tok = np.ascontiguousarray(tokens, dtype=np.int32).reshape(-1)
+            if tok.size != ids.size:
+                raise ValueError("tokens needs one id per sequence")
         slots = np.empty(ids.size, np.int64)
         cows = np.empty((ids.size, 2), np.int64)
-        _check(self._lib.pa_bm_append_batch(self._h, ids.ctypes.data, int(ids.size), slots.ctypes.data,
-                                            cows.ctypes.data), "pa_bm_append_batch")
+        _check(self._lib.pa_bm_append_batch(self._h, ids.ctypes.data, None if tok is None else tok.ctypes.data,
+                                            int(ids.size), slots.ctypes.data, cows.ctypes.data),
+               "pa_bm_append_batch")
         return slots, cows
 
     def block_tables(self, seq_ids, max_blocks: int, pad: int = 0):

@@ -26,6 +26,12 @@ struct Seq {
   int len = 0;
   bool swapped = false;
   uint64_t stamp = 0;  // last batch call that listed this sequence
+  // Token ids are known for every token so far (admitted with its prompt's
+  // ids, every append given its id): then `tail` holds the ids of the partly
+  // filled last block (room for a whole block is reserved), and a block that
+  // an append fills is registered in the prefix cache.
+  bool tracked = false;
+  std::vector<int32_t> tail;
 };
 
 // No C++ exception leaves an entry point: a failed allocation (the only
@@ -48,10 +54,19 @@ int guarded(F &&f) noexcept {
 struct pa_bm {
   int num_blocks = 0;
   int block_size = 0;
-  std::vector<int32_t> ref;        // per block, 0 = free
-  std::vector<int32_t> free_list;  // LIFO stack; back() is handed out next (may hold revived entries)
-  std::vector<uint8_t> in_free;    // per block: has an entry in free_list (at most one)
-  int nfree = 0;                   // blocks with ref 0
+  std::vector<int32_t> ref;  // per block, 0 = free
+  // Free blocks in two tiers.  Blocks holding no cached content are handed
+  // out first, most recently freed first (a stack; initially in increasing
+  // id order).  Free blocks still in the prefix cache are handed out only
+  // when no other is left, least recently freed first (a list, oldest at its
+  // head), so the content most likely to be asked for again stays longest.
+  // A block is freed no earlier than the blocks that continue it (whoever
+  // holds a block holds the ones before it), so leaves leave the cache first.
+  std::vector<int32_t> stack;                 // free, not cached
+  std::vector<int32_t> lru_prev, lru_next;    // free and cached
+  int32_t lru_head = -1, lru_tail = -1;
+  std::vector<uint8_t> where;                 // per block: 0 in use, 1 on the stack, 2 in the list
+  int nfree = 0;                              // blocks with ref 0
   // Prefix cache: full blocks registered by content.  A block's key is its
   // parent (the block before it in the sequence, -1 for the first) and its B
   // token ids; lookups compare both exactly, the hash only picks the bucket.
@@ -108,6 +123,33 @@ struct pa_bm {
     }
     c_parent[b] = -2;
     --ncached;
+    if (where[b] == 2) {  // free, and now nothing to keep: first in line again
+      lru_remove(b);
+      stack.push_back(b);
+      where[b] = 1;
+    }
+  }
+  void lru_remove(int32_t b) {
+    const int32_t pv = lru_prev[b], nx = lru_next[b];
+    if (pv >= 0)
+      lru_next[pv] = nx;
+    else
+      lru_head = nx;
+    if (nx >= 0)
+      lru_prev[nx] = pv;
+    else
+      lru_tail = pv;
+    where[b] = 0;
+  }
+  void lru_push(int32_t b) {  // as the most recently freed
+    lru_prev[b] = lru_tail;
+    lru_next[b] = -1;
+    if (lru_tail >= 0)
+      lru_next[lru_tail] = b;
+    else
+      lru_head = b;
+    lru_tail = b;
+    where[b] = 2;
   }
   void uncache(int32_t root) {  // root and all its cached descendants, leaves first
     if (c_parent[root] == -2) return;
@@ -121,22 +163,33 @@ struct pa_bm {
     }
   }
   int32_t take() {  // caller checked nfree > 0
-    for (;;) {
-      int32_t b = free_list.back();
-      free_list.pop_back();
-      in_free[b] = 0;
-      if (ref[b] != 0) continue;  // revived by a cache hit after it was freed
-      uncache(b);                 // its old content is about to be overwritten
-      ref[b] = 1;
+    int32_t b;
+    if (!stack.empty()) {
+      b = stack.back();
+      stack.pop_back();
+      where[b] = 0;
+    } else {  // evict the least recently freed cached block
+      b = lru_head;
+      lru_remove(b);
+      uncache(b);  // its old content is about to be overwritten
+    }
+    ref[b] = 1;
+    --nfree;
+    return b;
+  }
+  void revive(int32_t b) {  // a prefix-cache hit on b
+    if (ref[b]++ == 0) {
+      lru_remove(b);
       --nfree;
-      return b;
     }
   }
-  void drop(int32_t b) {  // never allocates: free_list has room for every block
+  void drop(int32_t b) {  // never allocates: the stack has room for every block
     if (--ref[b] == 0) {
-      if (!in_free[b]) {  // a revived block still has its old entry: reuse it
-        free_list.push_back(b);
-        in_free[b] = 1;
+      if (c_parent[b] != -2) {
+        lru_push(b);
+      } else {
+        stack.push_back(b);
+        where[b] = 1;
       }
       ++nfree;
     }
@@ -145,9 +198,18 @@ struct pa_bm {
     return s.len % block_size == 0 || ref[s.blocks[s.len / block_size]] > 1;
   }
   void grow(Seq &s) { s.blocks.reserve(std::max<size_t>(8, 2 * s.blocks.size())); }
+  // Appending `token` (nullptr: an id not given) to s fills a block that is
+  // then registered, so the cache's key store must exist first.
+  bool fills_tracked(const Seq &s, const int32_t *token) const {
+    return token && s.tracked && (s.len + 1) % block_size == 0;
+  }
+  void ensure_keys() {  // allocates once
+    if (c_tok.empty()) c_tok.assign((size_t)num_blocks * block_size, 0);
+  }
   // One token onto s; the caller checked that a block is free if one is
-  // needed and that s.blocks has room for a new one.  Never allocates.
-  void append_one(Seq &s, int64_t *slot_out, int64_t *cow_pair_out) {
+  // needed, that s.blocks has room for a new one and, when the token fills a
+  // tracked block, that the key store exists.  Never allocates.
+  void append_one(Seq &s, int64_t *slot_out, int64_t *cow_pair_out, const int32_t *token) {
     const int B = block_size;
     const int j = s.len;
     cow_pair_out[0] = cow_pair_out[1] = -1;
@@ -165,6 +227,21 @@ struct pa_bm {
     }
     *slot_out = (int64_t)s.blocks[j / B] * B + (j % B);
     s.len = j + 1;
+    if (!token) {  // an id not given: from here on nothing of s is registered
+      s.tracked = false;
+      s.tail.clear();
+      return;
+    }
+    if (!s.tracked) return;
+    s.tail.push_back(*token);  // within the reserved block's room
+    if (s.len % B == 0) {      // the token filled its block: findable by later prompts
+      const size_t nb = s.blocks.size();
+      const int32_t b = s.blocks[nb - 1], parent = nb >= 2 ? s.blocks[nb - 2] : -1;
+      // only reachable when the chain before it is cached; its K/V are valid
+      // once this step's cache write of the token has run
+      if ((parent < 0 || c_parent[parent] != -2) && c_parent[b] == -2) register_block(b, parent, s.tail.data());
+      s.tail.clear();
+    }
   }
   int32_t lookup(int32_t parent, const int32_t *tok) const {
     if (c_tok.empty()) return -1;
@@ -195,6 +272,27 @@ struct pa_bm {
   }
 };
 
+namespace {
+
+int append_single(pa_bm *bm, int seq_id, const int32_t *token, int64_t *slot_out, int64_t cow_pair_out[2]) {
+  if (!bm || !slot_out || !cow_pair_out) return PA_ERR_INVALID;
+  auto it = bm->seqs.find(seq_id);
+  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
+  Seq &s = it->second;
+  if (s.len == INT_MAX) return PA_ERR_INVALID;
+  if (bm->needs_block(s) && bm->nfree == 0) return PA_ERR_OOM;
+  const int st = guarded([&]() -> int {  // allocations first
+    if (s.len % bm->block_size == 0 && s.blocks.size() == s.blocks.capacity()) bm->grow(s);
+    if (bm->fills_tracked(s, token)) bm->ensure_keys();
+    return PA_OK;
+  });
+  if (st != PA_OK) return st;
+  bm->append_one(s, slot_out, cow_pair_out, token);
+  return PA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_size) {
@@ -205,10 +303,12 @@ pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_siz
     bm->num_blocks = num_blocks;
     bm->block_size = block_size;
     bm->ref.assign(num_blocks, 0);
-    bm->free_list.reserve(num_blocks);
-    for (int b = num_blocks - 1; b >= 0; --b) bm->free_list.push_back(b);
+    bm->stack.reserve(num_blocks);
+    for (int b = num_blocks - 1; b >= 0; --b) bm->stack.push_back(b);
     bm->nfree = num_blocks;
-    bm->in_free.assign(num_blocks, 1);
+    bm->where.assign(num_blocks, 1);
+    bm->lru_prev.assign(num_blocks, -1);
+    bm->lru_next.assign(num_blocks, -1);
     bm->c_parent.assign(num_blocks, -2);
     bm->c_hash.assign(num_blocks, 0);
     bm->c_next.assign(num_blocks, -1);
@@ -257,31 +357,30 @@ int pa_bm_fork(pa_bm *bm, int parent_id, int child_id) {
   return guarded([&]() -> int {
     auto it = bm->seqs.find(parent_id);
     if (it == bm->seqs.end() || bm->seqs.count(child_id) || it->second.swapped) return PA_ERR_STATE;
-    const Seq &c = bm->seqs.emplace(child_id, it->second).first->second;  // copies; then no allocation
-    for (int32_t b : c.blocks) ++bm->ref[b];
+    auto c = bm->seqs.emplace(child_id, it->second).first;  // copies
+    if (c->second.tracked) {
+      try {
+        c->second.tail.reserve(bm->block_size);  // a copy keeps only the ids' own room
+      } catch (...) {
+        bm->seqs.erase(c);
+        throw;
+      }
+    }
+    for (int32_t b : c->second.blocks) ++bm->ref[b];  // no allocation from here
     return PA_OK;
   });
 }
 
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]) {
-  if (!bm || !slot_out || !cow_pair_out) return PA_ERR_INVALID;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end() || it->second.swapped) return PA_ERR_STATE;
-  Seq &s = it->second;
-  if (s.len == INT_MAX) return PA_ERR_INVALID;
-  if (bm->needs_block(s) && bm->nfree == 0) return PA_ERR_OOM;
-  if (s.len % bm->block_size == 0 && s.blocks.size() == s.blocks.capacity()) {
-    const int st = guarded([&]() -> int {
-      bm->grow(s);
-      return PA_OK;
-    });
-    if (st != PA_OK) return st;
-  }
-  bm->append_one(s, slot_out, cow_pair_out);
-  return PA_OK;
+  return append_single(bm, seq_id, nullptr, slot_out, cow_pair_out);
 }
 
-int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots_out, int64_t *cow_pairs_out) {
+int pa_bm_append_token(pa_bm *bm, int seq_id, int32_t token, int64_t *slot_out, int64_t cow_pair_out[2]) {
+  return append_single(bm, seq_id, &token, slot_out, cow_pair_out);
+}
+
+int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, const int32_t *tokens, int n, int64_t *slots_out,
+                       int64_t *cow_pairs_out) {
   if (!bm || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out))) return PA_ERR_INVALID;
   if (n == 0) return PA_OK;
   return guarded([&]() -> int {
@@ -316,9 +415,11 @@ int pa_bm_append_batch(pa_bm *bm, const int32_t *seq_ids, int n, int64_t *slots_
       if (bm->blk_count[x]++ < bm->ref[x] - 1) ++need;
     }
     if (need > (int64_t)bm->nfree) return PA_ERR_OOM;
-    for (int i = 0; i < n; ++i)
+    for (int i = 0; i < n; ++i) {
       if (sq[i]->len % B == 0 && sq[i]->blocks.size() == sq[i]->blocks.capacity()) bm->grow(*sq[i]);
-    for (int i = 0; i < n; ++i) bm->append_one(*sq[i], slots_out + i, cow_pairs_out + 2 * i);
+      if (bm->fills_tracked(*sq[i], tokens ? tokens + i : nullptr)) bm->ensure_keys();
+    }
+    for (int i = 0; i < n; ++i) bm->append_one(*sq[i], slots_out + i, cow_pairs_out + 2 * i, tokens ? tokens + i : nullptr);
     return PA_OK;
   });
 }
@@ -413,11 +514,14 @@ int pa_bm_add_seq_tokens(pa_bm *bm, int seq_id, const int32_t *tokens, int num_t
     Seq s;
     s.len = num_tokens;
     s.blocks.reserve(need);
+    s.tracked = true;
+    s.tail.reserve(B);
+    s.tail.assign(tokens + (size_t)nfull * B, tokens + num_tokens);
     // the last allocations; nothing below allocates
-    if (nfull > (int64_t)hit.size() && bm->c_tok.empty()) bm->c_tok.assign((size_t)bm->num_blocks * B, 0);
+    if (nfull > (int64_t)hit.size()) bm->ensure_keys();
     Seq &q = bm->seqs.emplace(seq_id, std::move(s)).first->second;
     for (int32_t b : hit) {
-      if (bm->ref[b]++ == 0) --bm->nfree;  // revived: its stale free-list entry is skipped later
+      bm->revive(b);
       q.blocks.push_back(b);
     }
     parent = hit.empty() ? -1 : hit.back();

@@ -138,11 +138,18 @@ int main() {
   ok = ok && inject("add_seq", bm, [&] { return (long long)pa_bm_add_seq(bm, 3, 9); }, OOM);
   for (int i = 0; i < 40 && ok; ++i)
     ok = inject("append (growing table)", bm, [&] { return (long long)pa_bm_append(bm, 3, &slot, cow); }, OOM);
+  for (int i = 0; i < 7 && ok; ++i) {  // seq 1 keeps its ids: fills and registers its block
+    const int32_t tok = 500 + i;
+    ok = inject("append_token", bm, [&] { return (long long)pa_bm_append_token(bm, 1, tok, &slot, cow); }, OOM);
+  }
   ok = ok && pa_bm_fork(bm, 2, 5) == PA_OK;
   const int32_t ids[4] = {5, 0, 2, 3};
   int64_t bslots[4], bcows[8];
   for (int i = 0; i < 6 && ok; ++i)
-    ok = inject("append_batch", bm, [&] { return (long long)pa_bm_append_batch(bm, ids, 4, bslots, bcows); }, OOM);
+    ok = inject("append_batch", bm, [&] { return (long long)pa_bm_append_batch(bm, ids, nullptr, 4, bslots, bcows); }, OOM);
+  const int32_t tids[2] = {1, 0}, toks[2] = {900, 901};
+  for (int i = 0; i < 5 && ok; ++i)
+    ok = inject("append_batch (ids)", bm, [&] { return (long long)pa_bm_append_batch(bm, tids, toks, 2, bslots, bcows); }, OOM);
   ok = ok && inject("swap_out", bm, [&] { return (long long)pa_bm_swap_out(bm, 3, pairs, 64, &n); }, OOM);
   ok = ok && inject("wasted_slots", bm, [&] { return (long long)pa_bm_wasted_slots(bm); }, -1);
   ok = ok && inject("swap_in", bm, [&] { return (long long)pa_bm_swap_in(bm, 3, pairs, 64, &n); }, OOM);

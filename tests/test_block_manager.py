@@ -282,42 +282,46 @@ def test_prefix_cache_never_hands_out_a_block_twice():
         bm.add_seq(2, 1)
 
 
-def test_prefix_cache_drops_continuations_of_a_reused_block():
-    """A cached block's K/V were computed after its whole prefix.  When a block
-    is handed out again for new content, the cached blocks that continued it
-    must leave the cache with it, or a prompt that matches the new content
-    would be given a continuation computed after the old one."""
+def test_prefix_cache_never_serves_a_continuation_of_other_content():
+    """A cached block's K/V were computed after its whole prefix.  Once the
+    block before it holds other content, a prompt that matches the new
+    content must not be given the old continuation."""
     bm = pa.BlockManager(2, 1)
     A, C, X = 100, 200, 300
-    assert bm.add_seq_tokens(0, [A, C]) == 0               # blocks 0 (A), 1 (C after A)
+    assert bm.add_seq_tokens(0, [A, C]) == 0               # A, then C after A
     bm.free_seq(0)                                          # both free, both still cached
     assert bm.num_cached_blocks() == 2
-    assert bm.add_seq_tokens(1, [X]) == 0                   # block 0 now holds X
-    assert bm.num_cached_blocks() == 1                      # C-after-A went with A
+    assert bm.add_seq_tokens(1, [X]) == 0                   # evicts C-after-A, freed first
+    assert bm.num_cached_blocks() == 2                      # A and X
     assert bm.add_seq_tokens(2, [X, C]) == 1                # only X is found
+    assert bm.num_cached_blocks() == 2                      # X and C-after-X (A evicted for it)
 
 
-def test_prefix_cache_drops_whole_subtrees_and_keeps_live_chains():
-    """Three prompts share a first block and branch after it.  Once they are
-    freed, handing that first block out again for new content drops every
-    cached continuation of it at once; a chain still in use is not touched."""
+def test_prefix_cache_eviction_order():
+    """Free blocks holding no cached content are handed out before any cached
+    one; cached free blocks go least recently freed first, which puts a
+    prompt's later blocks before its earlier ones; a chain in use is never
+    touched; hits stay exact throughout."""
     B = 2
-    bm = pa.BlockManager(8, B)
-    a, b, c, d, x = [1, 2], [3, 4], [5, 6], [7, 8], [9, 10]
-    assert bm.add_seq_tokens(0, a + b + c) == 0
-    assert bm.add_seq_tokens(1, a + b + d) == 4             # a, b found; d's block is new
-    assert bm.add_seq_tokens(2, a + c) == 2
-    assert bm.num_cached_blocks() == 5                      # a; b, c under a; c, d under b
-    assert bm.add_seq_tokens(3, d + d) == 0                 # an unrelated chain, kept in use
-    t0 = bm.block_table(0)
-    for s in (1, 2, 0):                                     # seq 0 last: its first block is reused first
+    bm = pa.BlockManager(12, B)
+    a, b, c, d = [1, 2], [3, 4], [5, 6], [7, 8]
+    assert bm.add_seq_tokens(0, a + b + c) == 0             # blocks 0, 1, 2
+    assert bm.add_seq_tokens(1, a + b + d) == 4             # d after b: block 3
+    assert bm.add_seq_tokens(2, a + c) == 2                 # c after a: block 4
+    assert bm.add_seq_tokens(3, d + d) == 0                 # blocks 5, 6, kept in use
+    for s in (1, 2, 0):                                     # freed in this order: 3, 4, then 2, 1, 0
         bm.free_seq(s)
-    assert bm.num_free() == 6 and bm.num_cached_blocks() == 7
-    assert bm.add_seq_tokens(4, x) == 0
-    assert bm.block_table(4) == t0[:1]                      # a's block now holds x
-    assert bm.num_cached_blocks() == 3                      # x and the live d d; a's subtree is gone
-    assert bm.add_seq_tokens(5, x + b + c) == 2             # b after x was never computed
-    assert bm.add_seq_tokens(6, d + d + a) == 4             # the live chain is still found
+    assert bm.num_free() == 10 and bm.num_cached_blocks() == 7
+    bm.add_seq(4, 5 * B)                                    # the 5 never-used blocks go first
+    assert sorted(bm.block_table(4)) == [7, 8, 9, 10, 11] and bm.num_cached_blocks() == 7
+    bm.add_seq(5, B)                                        # then the least recently freed: d after b
+    assert bm.block_table(5) == [3] and bm.num_cached_blocks() == 6
+    assert bm.add_seq_tokens(6, a + b + d) == 4             # d after b is gone; c after a is evicted for it
+    assert bm.block_table(6)[2] == 4
+    assert bm.add_seq_tokens(7, a + b + c) == 6             # the first prompt's chain is whole
+    bm.free_seq(6)
+    assert bm.add_seq_tokens(8, a + c) == 2                 # c after a was evicted
+    assert bm.add_seq_tokens(9, d + d) == 4                 # the live chain, untouched
 
 
 def _state(bm, ids, N):
@@ -421,11 +425,11 @@ def test_batch_calls_reject_bad_arguments_through_the_c_abi():
     slots, cows = np.zeros(1, np.int64), np.zeros((1, 2), np.int64)
     out, lens = np.zeros((1, 4), np.int32), np.zeros(1, np.int32)
     P = lambda a: a.ctypes.data  # noqa: E731
-    assert lib.pa_bm_append_batch(None, P(ids), 1, P(slots), P(cows)) == pa.PA_ERR_INVALID
-    assert lib.pa_bm_append_batch(h, P(ids), -1, P(slots), P(cows)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_append_batch(None, P(ids), None, 1, P(slots), P(cows)) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_append_batch(h, P(ids), None, -1, P(slots), P(cows)) == pa.PA_ERR_INVALID
     for args in ((None, P(slots), P(cows)), (P(ids), None, P(cows)), (P(ids), P(slots), None)):
-        assert lib.pa_bm_append_batch(h, args[0], 1, args[1], args[2]) == pa.PA_ERR_INVALID
-    assert lib.pa_bm_append_batch(h, None, 0, None, None) == pa.PA_OK
+        assert lib.pa_bm_append_batch(h, args[0], None, 1, args[1], args[2]) == pa.PA_ERR_INVALID
+    assert lib.pa_bm_append_batch(h, None, None, 0, None, None) == pa.PA_OK
     assert lib.pa_bm_block_tables(None, P(ids), 1, P(out), 4, 0, P(lens)) == pa.PA_ERR_INVALID
     assert lib.pa_bm_block_tables(h, P(ids), -1, P(out), 4, 0, P(lens)) == pa.PA_ERR_INVALID
     assert lib.pa_bm_block_tables(h, P(ids), 1, P(out), -1, 0, P(lens)) == pa.PA_ERR_INVALID
@@ -434,6 +438,108 @@ def test_batch_calls_reject_bad_arguments_through_the_c_abi():
     assert lib.pa_bm_block_tables(h, P(ids), 1, P(out), 4, 9, None) == pa.PA_OK  # lengths optional
     assert out[0].tolist() == [bm.block_table(0)[0], 9, 9, 9]
     assert bm.seq_len(0) == 3 and bm.num_free() == 7                              # nothing appended
+
+
+def test_generated_blocks_serve_the_next_turn():
+    """A conversation's second turn repeats the first turn's prompt and the
+    answer generated for it.  Appends that give the token ids register every
+    block they fill, so the second turn finds the answer's full blocks too;
+    without the ids only the first prompt's full blocks are found."""
+    B = 8
+    st = wl.Stream(61, 1)
+    p1 = [int(x) for x in st.integers(0, 1000, 37)]          # 4 full blocks + 5 tokens
+    ans = [int(x) for x in st.integers(0, 1000, 20)]         # fills blocks 4, 5, 6; 1 token into block 7
+    msg = [int(x) for x in st.integers(0, 1000, 10)]
+    for with_ids, want in ((True, 56), (False, 32)):
+        bm = pa.BlockManager(64, B)
+        assert bm.add_seq_tokens(0, p1) == 0
+        for t in ans:
+            bm.append(0, t if with_ids else None)
+        t0 = bm.block_table(0)
+        assert bm.num_cached_blocks() == (7 if with_ids else 4)
+        bm.free_seq(0)
+        assert bm.add_seq_tokens(1, p1 + ans + msg) == want
+        assert bm.block_table(1)[: want // B] == t0[: want // B]
+    # an append without its id ends the registering: block 4, filled by the
+    # third append, is registered; blocks 5 and 6 are not
+    bm = pa.BlockManager(64, B)
+    bm.add_seq_tokens(0, p1)
+    for i, t in enumerate(ans):
+        bm.append(0, None if i == 5 else t)
+    assert bm.num_cached_blocks() == 5
+    bm.free_seq(0)
+    assert bm.add_seq_tokens(1, p1 + ans + msg) == 40
+
+
+def test_conversations_find_every_full_block_of_their_history():
+    """Six conversations over five turns, each turn's answer sampled twice
+    (a fork; the first sample is kept) with token ids given to every
+    append.  With a pool large enough that nothing is evicted, each turn's
+    prompt -- the history so far plus a new message -- finds exactly the
+    history's full blocks: the earlier prompts' blocks, the blocks the kept
+    answers filled, and the block where an answer continued its prompt."""
+    B = 16
+    bm = pa.BlockManager(4096, B)
+    st = wl.Stream(63, 1)
+    ints = lambda n: [int(x) for x in st.integers(0, 30000, n)]  # noqa: E731
+    hist = {c: [] for c in range(6)}
+    sid = 0
+    for turn in range(5):
+        for c in hist:
+            toks = hist[c] + ints(5 + int(st.integers(0, 36, 1)[0]))
+            assert bm.add_seq_tokens(sid, toks) == len(hist[c]) // B * B, (turn, c)
+            bm.fork(sid, sid + 1)
+            n = 1 + int(st.integers(0, 50, 1)[0])
+            kept, other = ints(n), ints(n)
+            bm.append_batch([sid, sid + 1], [kept[0], other[0]])
+            for x, y in zip(kept[1:], other[1:]):
+                bm.append(sid, x)
+                bm.append(sid + 1, y)
+            hist[c] = toks + kept
+            bm.free_seq(sid)
+            bm.free_seq(sid + 1)
+            sid += 2
+    assert bm.num_free() == 4096
+
+
+def test_forked_samples_register_their_own_continuations():
+    B = 4
+    bm = pa.BlockManager(64, B)
+    prompt = list(range(100, 110))                             # 2 full blocks + 2 tokens
+    bm.add_seq_tokens(0, prompt)
+    bm.fork(0, 1)
+    a, b = [1, 2, 3, 4, 5, 6], [7, 8, 9, 10, 11, 12]
+    for x, y in zip(a, b):
+        bm.append(0, x)                                        # the first copies the shared partial block
+        bm.append(1, y)
+    assert bm.num_cached_blocks() == 2 + 2 * 2                 # each sample filled blocks 2 and 3
+    bm.free_seq(0)
+    bm.free_seq(1)
+    assert bm.add_seq_tokens(2, prompt + a + [0]) == 16
+    assert bm.add_seq_tokens(3, prompt + b + [0]) == 16
+    assert bm.add_seq_tokens(4, prompt + a[:2] + b[2:] + [0]) == 12  # the samples' blocks 2 differ
+
+
+def test_append_batch_with_ids_equals_single_appends_with_ids():
+    B, N = 4, 128
+    one, bat = pa.BlockManager(N, B), pa.BlockManager(N, B)
+    st = wl.Stream(62, 1)
+    for m in (one, bat):
+        m.add_seq_tokens(0, list(range(9)))
+        m.fork(0, 1)
+        m.add_seq_tokens(2, list(range(50, 53)))
+        m.add_seq(3, 5)                                        # ids unknown: never registered
+    ids = [0, 1, 2, 3]
+    for step in range(11):
+        tok = [int(x) for x in st.integers(0, 1000, 4)]
+        sl, cw = bat.append_batch(ids, tok)
+        for i, s in enumerate(ids):
+            slot, pair = one.append(s, tok[i])
+            assert sl[i] == slot and (None if cw[i, 0] < 0 else (cw[i, 0], cw[i, 1])) == pair
+        assert _state(one, ids, N) == _state(bat, ids, N)
+    assert bat.num_cached_blocks() == 2 + 3 + 3 + 3            # prompt 0; 3 more each for 0, 1 and 2
+    with pytest.raises(ValueError):
+        bat.append_batch(ids, tok[:3])
 
 
 def test_failed_allocations_leave_no_trace(tmp_path):
@@ -457,8 +563,9 @@ def test_failed_allocations_leave_no_trace(tmp_path):
     assert r.stdout.startswith("ok ") and int(r.stdout.split()[1]) >= 20, r.stdout
 
 
-@pytest.mark.parametrize("N,batch", [(24, False), (64, False), (24, True), (64, True)])
-def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
+@pytest.mark.parametrize("N,batch,ids", [(24, False, False), (64, False, False), (24, True, False), (64, True, False),
+                                         (24, False, True), (64, False, True), (24, True, True), (64, True, True)])
+def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch, ids):
     """Random prompts (some repeating earlier prompts' leading blocks), forks,
     appends, frees, swap-outs and swap-ins against simulated device and host
     page pools.  The test plays the caller: it writes each new token into the
@@ -471,7 +578,10 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
     prefix-cache hit on a block whose content was computed after another
     prefix fails the read-back.  With `batch`, appends go to a random subset
     of the resident sequences in one append_batch call, and the step's copies
-    and writes are applied in the batch's order."""
+    and writes are applied in the batch's order.  With `ids`, most appends
+    give their token id (so the blocks they fill enter the prefix cache) and
+    some prompts continue a live or freed sequence's whole history, as a
+    conversation's next turn does."""
     B, H = 8, 24
     bm = pa.BlockManager(N, B, num_host_blocks=H)
     dev = np.full((N, B), -1, np.int64)
@@ -481,6 +591,7 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
     u = st.uniform(3000)
     fresh = iter(range(10 ** 6, 10 ** 7))
     chunks = [[next(fresh) for _ in range(B)] for _ in range(4)]
+    history = []  # the token lists of freed sequences
     prompts = []
     nxt = 0
 
@@ -521,6 +632,11 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
                     base = prompts[int(u[k] * 1e6) % len(prompts)]
                     keep = (int(u[k] * 1e8) % (len(base) // B + 1)) * B
                     toks = base[:keep] + [next(fresh) for _ in range(int(u[k] * 1e5) % 20)]
+                elif ids and 0.16 <= op < 0.19:  # the next turn of a conversation
+                    cands = history + [model[x] for x in sorted(model)]
+                    base = cands[int(u[k] * 1e6) % len(cands)]
+                    keep = int(u[k] * 1e8) % (len(base) + 1)
+                    toks = base[:keep] + [next(fresh) for _ in range(int(u[k] * 1e5) % 12)]
                 elif op < 0.16:  # blocks from a small set in any order: equal blocks after other prefixes
                     n = 1 + int(u[k] * 1e3) % 5
                     toks = [x for i in range(n) for x in chunks[int(u[k] * 10 ** (4 + i)) % len(chunks)]]
@@ -547,17 +663,18 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
                 res = [s for s in model if s not in swapped]
                 sub = [s for i, s in enumerate(res) if u[(k * 31 + i) % 3000] < 0.5]
                 if sub:
-                    sl, cw = bm.append_batch(sub)
+                    new = [next(fresh) for _ in sub]
+                    sl, cw = bm.append_batch(sub, new if ids else None)
                     for i, s in enumerate(sub):
                         if cw[i, 0] >= 0:
                             dev[cw[i, 1]] = dev[cw[i, 0]]
-                        model[s].append(next(fresh))
+                        model[s].append(new[i])
                         dev[sl[i] // B, sl[i] % B] = fp(model[s])[-1]
             elif op < 0.6:
                 s = pick(lambda s: s not in swapped)
                 if s is not None:
                     tok = next(fresh)
-                    slot, cow = bm.append(s)
+                    slot, cow = bm.append(s, tok if ids and u[(k * 17) % 3000] < 0.95 else None)
                     if cow is not None:
                         dev[cow[1]] = dev[cow[0]]
                     model[s].append(tok)
@@ -566,6 +683,7 @@ def test_model_based_contents_through_cow_swap_and_prefix_cache(N, batch):
                 s = pick()
                 if s is not None:
                     bm.free_seq(s)
+                    history.append(model[s])
                     del model[s]
                     swapped.discard(s)
             elif op < 0.89:
