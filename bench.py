@@ -1016,6 +1016,7 @@ def run_block_manager(args):
     counts = {"tokens": 0, "cached_tokens": 0, "forks": 0, "appends": 0, "cow": 0, "swapped_blocks": 0, "frees": 0,
               "steps": 0}
     ids = np.arange(len(prompts) * R, dtype=np.int32)
+    step_tokens = np.asarray(st.integers(0, 32000, len(ids)), np.int32)
     DECODE_STEPS = 8
     max_blocks = (max(len(p) for p in prompts) + DECODE_STEPS + B - 1) // B
 
@@ -1033,7 +1034,7 @@ def run_block_manager(args):
         def decode_step():
             # one decode step's host work: a token onto every sequence, then the
             # padded block-table matrix and context lengths the attention call takes
-            _, cows = bm.append_batch(ids)
+            _, cows = bm.append_batch(ids, step_tokens)  # with ids: filled blocks enter the prefix cache
             bm.block_tables(ids, max_blocks)
             return int((cows[:, 0] >= 0).sum())
 
@@ -1077,7 +1078,7 @@ def run_block_manager(args):
             "scaling": "none", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
             "config": {"workload": f"block_manager: {len(prompts)} prompts x {R} samples, {plan.prefix_len}-token "
                                    f"system prompt + U[1,512] tokens, B={B}; admit, fork, {DECODE_STEPS} decode steps (each one "
-                                   f"append_batch + block_tables call over all {len(ids)} sequences); 64 unshared "
+                                   f"append_batch with token ids + block_tables call over all {len(ids)} sequences); 64 unshared "
                                    f"1024-token sequences swapped out and in; free all; per step (host only, "
                                    f"through the C ABI from Python; prompts held as int32 arrays)"},
             "cached_fraction": round(counts["cached_tokens"] / max(counts["tokens"], 1), 4),
