@@ -437,7 +437,8 @@ int pa_bm_free_seq(pa_bm *bm, int seq_id) {
   for (int32_t b : it->second.blocks) {
     if (bm->ref[b] <= 0) return PA_ERR_STATE;  // cannot happen unless corrupted
   }
-  // Return blocks last-to-first so the sequence's first block is reused first.
+  // Last to first: an uncached first block is handed out again first, and a
+  // cached block stays longer than the blocks that continue it.
   const auto &bl = it->second.blocks;
   for (auto r = bl.rbegin(); r != bl.rend(); ++r) bm->drop(*r);
   bm->seqs.erase(it);
@@ -551,14 +552,15 @@ int pa_bm_swap_out(pa_bm *bm, int seq_id, int64_t *pairs_out, int cap, int *n) {
     if (bm->ref[b] != 1) return PA_ERR_STATE;  // shared blocks stay with their other users
   if ((int)bm->host_free.size() < *n) return PA_ERR_OOM;
   for (int i = 0; i < *n; ++i) {
-    const int32_t d = s.blocks[i];
     const int32_t h = bm->host_free.back();
     bm->host_free.pop_back();
-    pairs_out[2 * i] = d;
+    pairs_out[2 * i] = s.blocks[i];
     pairs_out[2 * i + 1] = h;
-    bm->drop(d);
     s.blocks[i] = h;
   }
+  // freed last to first, as by pa_bm_free_seq: a cached block then stays
+  // longer than the blocks that continue it
+  for (int i = *n - 1; i >= 0; --i) bm->drop((int32_t)pairs_out[2 * i]);
   s.swapped = true;
   return PA_OK;
 }

@@ -440,6 +440,22 @@ def test_batch_calls_reject_bad_arguments_through_the_c_abi():
     assert bm.seq_len(0) == 3 and bm.num_free() == 7                              # nothing appended
 
 
+def test_swapped_out_prompt_keeps_its_earlier_blocks_longest():
+    """A swapped-out sequence's device blocks are freed last to first, as by
+    free_seq: reusing one of them evicts the prompt's last cached block, and
+    the earlier ones stay findable."""
+    B = 4
+    bm = pa.BlockManager(4, B, num_host_blocks=4)
+    p = list(range(12))                                      # 3 full blocks, all cached
+    bm.add_seq_tokens(0, p)
+    bm.add_seq(1, B)                                         # the pool's last never-used block
+    bm.swap_out(0)
+    assert bm.num_free() == 3 and bm.num_cached_blocks() == 3
+    bm.add_seq(2, B)                                         # evicts the third block, a leaf
+    assert bm.num_cached_blocks() == 2
+    assert bm.add_seq_tokens(3, p[:8]) == 8
+
+
 def test_generated_blocks_serve_the_next_turn():
     """A conversation's second turn repeats the first turn's prompt and the
     answer generated for it.  Appends that give the token ids register every
