@@ -32,3 +32,27 @@ def test_reference_arm_takes_the_other_workloads():
     for w in ("tiny_decode", "prefix_sharing"):
         d = run("--impl", "reference", "--workload", w, "--steps", "1", "--warmup", "0")
         assert d["impl"] == "reference" and d["config"]["workload"] == w and d["value"] > 0
+
+
+def test_clock_summary_reads_the_timed_window():
+    """The bench's nvidia-smi sampler: median SM clock over the timed window,
+    the throttle reasons seen active in it, the nearest samples when none
+    fall inside, and a marker when there are none at all."""
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+
+    def row(sm, hw="Not Active", hwt="Not Active", swt="Not Active", cap="Not Active"):
+        return f"0, {sm}, 2070, 900.5, 0x0, {hw}, {hwt}, {swt}, {cap}"
+
+    c.samples = [(0.0, row(1200)), (1.0, row(2070)), (1.1, row(2040, cap="Active")), (1.2, row(2010)),
+                 (5.0, row(900, hw="Active")), (6.0, "garbled")]
+    s = c.summary(0.98, 1.22)
+    assert s["sm_mhz"] == 2040 and s["sm_max_mhz"] == 2070 and s["reasons"] == ["sw_power_cap"]
+    assert s["samples"] == 3 and s["window"] == "timed"
+    s = c.summary(2.0, 3.0)                       # no sample inside: the last ones before its end
+    assert s["window"] == "nearest" and s["samples"] == 4 and s["reasons"] == ["sw_power_cap"]
+    s = c.summary(4.9, 5.1)
+    assert s["reasons"] == ["hw_slowdown"] and s["sm_mhz"] == 900
+    c.samples = []
+    assert c.summary(0, 1)["reasons"] == ["no samples"]
