@@ -1014,7 +1014,8 @@ def run_block_manager(args):
     nblk = 4 * plan.num_blocks
     times = {k: 0.0 for k in ("admit", "fork", "append", "steady", "swap", "free")}
     counts = {"tokens": 0, "cached_tokens": 0, "forks": 0, "appends": 0, "cow": 0, "swapped_blocks": 0, "frees": 0,
-              "steps": 0}
+              "steps": 0, "turn_tokens": 0, "turn_cached": 0, "turn_generated": 0}
+    message = np.asarray(st.integers(0, 32000, 32), np.int32)
     ids = np.arange(len(prompts) * R, dtype=np.int32)
     step_tokens = np.asarray(st.integers(0, 32000, len(ids)), np.int32)
     DECODE_STEPS = 8
@@ -1060,6 +1061,14 @@ def run_block_manager(args):
         t5 = time.perf_counter()
         for k, a, b in (("admit", t0, t1), ("fork", t1, t2), ("append", t2, t3), ("swap", t3s, t4), ("free", t4, t5)):
             times[k] += b - a
+        # the next turn of each prompt's first sample: its history (the prompt and the tokens
+        # its decode steps appended, ids given) and a new message, after every sequence was freed
+        for p, toks in enumerate(prompts):
+            hist = np.concatenate([toks, np.full(DECODE_STEPS, step_tokens[p * R], np.int32), message])
+            got = bm.add_seq_tokens(base + 64 + p, hist)
+            counts["turn_tokens"] += len(hist)
+            counts["turn_cached"] += got
+            counts["turn_generated"] += max(0, got - len(toks) // B * B)  # in blocks the decode steps filled
 
     for _ in range(args.warmup):
         one_pass()
@@ -1087,6 +1096,9 @@ def run_block_manager(args):
                           "copy_on_write_share": round(counts["cow"] / max(counts["appends"], 1), 4),
                           "swap_blocks_out_and_in": rate(counts["swapped_blocks"], times["swap"]),
                           "free": rate(counts["frees"], times["free"])},
+            "next_turn": {"cached_fraction": round(counts["turn_cached"] / max(counts["turn_tokens"], 1), 4),
+                          "tokens_found_in_blocks_decode_filled_per_prompt": round(counts["turn_generated"] / max(
+                              args.steps * len(prompts), 1), 2)},
             "decode_step_host_us": {"first_after_fork": round(times["append"] / args.steps * 1e6, 2),
                                     "steady": round(times["steady"] / max(counts["steps"], 1) * 1e6, 2)},
             "gpu_launches": 0}

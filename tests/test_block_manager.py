@@ -742,3 +742,7 @@ def test_block_manager_benchmark_runs():
     # every prompt after the first finds the 2048-token system prompt cached (whole blocks)
     assert 0.5 < res["cached_fraction"] < 1.0
     assert 0.0 < res["ops_per_s"]["copy_on_write_share"] <= 1.0
+    # the next turn finds its history, including blocks the decode steps filled (their ids given)
+    assert res["next_turn"]["cached_fraction"] > res["cached_fraction"]
+    assert res["next_turn"]["tokens_found_in_blocks_decode_filled_per_prompt"] > 0
+    assert res["decode_step_host_us"]["steady"] > 0
