@@ -374,7 +374,9 @@ pa_bm *pa_bm_create_with_host(int num_blocks, int num_host_blocks, int block_siz
 void pa_bm_destroy(pa_bm *bm);
 
 /* New sequence seq_id (>= 0, unused) holding num_tokens (>= 0) tokens:
- * allocates ceil(num_tokens / B) blocks.  PA_ERR_OOM leaves no trace. */
+ * allocates ceil(num_tokens / B) blocks.  Its token ids are not known, so
+ * none of its blocks enters the prefix cache (pa_bm_add_seq_tokens admits a
+ * prompt by its ids).  PA_ERR_OOM leaves no trace. */
 int pa_bm_add_seq(pa_bm *bm, int seq_id, int num_tokens);
 
 /* child shares every block of parent (ref_count + 1 each), same length. */
