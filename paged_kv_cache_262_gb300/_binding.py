@@ -622,9 +622,11 @@ class BlockManager:
                "pa_bm_append_batch")
         return slots, cows
 
-    def block_tables(self, seq_ids, max_blocks: int, pad: int = 0):
+    def block_tables(self, seq_ids, max_blocks: int, pad: int = -1):
         """Padded block-table matrix int32 [n, max_blocks] and context lengths
-        int32 [n] of `seq_ids`, as the attention calls take them."""
+        int32 [n] of `seq_ids`, as the attention calls take them.  The default
+        pad is no block: an entry read past a context would be refused by the
+        kernels' page check rather than read block 0."""
         import numpy as np
         ids = np.ascontiguousarray(seq_ids, dtype=np.int32).reshape(-1)
         out = np.empty((ids.size, int(max_blocks)), np.int32)
