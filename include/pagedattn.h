@@ -19,8 +19,9 @@
  *  [SHARE] same page, "Zero-Copy Prefix Caching & Shared Sampling", and
  *         "vLLM Guide: High-Throughput Multi-GPU LLM Serving with
  *         PagedAttention", section "What Is PagedAttention?": blocks allocated
- *         on demand; shared prefixes point at the same physical pages, with
- *         copy-on-write.
+ *         on demand; shared prefixes (system prompts, few-shot examples,
+ *         earlier turns of a conversation) point at the same physical pages,
+ *         with copy-on-write.
  *  [TABLE] "vLLM High-Performance Inference Engine: PagedAttention Principles
  *         and Deployment Guide", section "PagedAttention Architecture Deep
  *         Dive": block table with per-page ref_count.
@@ -389,7 +390,7 @@ int pa_bm_fork(pa_bm *bm, int parent_id, int child_id);
  * cow_pair_out = {-1, -1}.  PA_ERR_OOM leaves the sequence unchanged. */
 int pa_bm_append(pa_bm *bm, int seq_id, int64_t *slot_out, int64_t cow_pair_out[2]);
 
-/* pa_bm_append with the token's id.  While every token id of seq_id is known
+/* pa_bm_append with the token's id [SHARE].  While every token id of seq_id is known
  * (it was admitted by pa_bm_add_seq_tokens, or forked from such a sequence,
  * and every append since gave its id), a block this token fills is
  * registered in the prefix cache like a prompt's full block -- when the
