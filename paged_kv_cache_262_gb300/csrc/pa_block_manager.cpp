@@ -5,11 +5,13 @@
 // and Deployment Guide" ("PagedAttention Architecture Deep Dive": block table
 // with ref_count, pages shared between sequences), "vLLM Guide: High-Throughput
 // Multi-GPU LLM Serving with PagedAttention" ("What Is PagedAttention?": blocks
-// allocated on demand, shared prefixes with copy-on-write) and "Configuring
+// allocated on demand, shared prefixes -- system prompts, few-shot examples,
+// earlier turns of a conversation -- with copy-on-write) and "Configuring
 // vLLM and PagedAttention for High Throughput Enterprise LLM Serving"
 // ("High-Throughput Batching": pages go back to the free pool on <eos>, and
 // the preemptive-swapping answer: a paused request's pages move to host RAM
-// and come back when device blocks free up).
+// and come back when device blocks free up; "Zero-Copy Prefix Caching &
+// Shared Sampling": requests with a common prefix point at the same pages).
 #include <algorithm>
 #include <climits>
 #include <cstdint>
