@@ -569,8 +569,9 @@ class BlockManager:
     def __init__(self, num_blocks: int, block_size: int, num_host_blocks: int = 0):
         self._lib = load()
         self._h = self._lib.pa_bm_create_with_host(int(num_blocks), int(num_host_blocks), int(block_size))
-        if not self._h:
-            raise PaError(PA_ERR_INVALID, "pa_bm_create")
+        if not self._h:  # NULL: bad sizes, or no host memory for valid ones
+            bad = int(num_blocks) <= 0 or int(num_host_blocks) < 0 or int(block_size) <= 0
+            raise PaError(PA_ERR_INVALID if bad else PA_ERR_OOM, "pa_bm_create")
         self.num_blocks = num_blocks
         self.block_size = block_size
 
