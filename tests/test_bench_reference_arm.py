@@ -56,3 +56,12 @@ def test_clock_summary_reads_the_timed_window():
     assert s["reasons"] == ["hw_slowdown"] and s["sm_mhz"] == 900
     c.samples = []
     assert c.summary(0, 1)["reasons"] == ["no samples"]
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun the reference arm runs on rank 0 alone; other ranks do no
+    work, print nothing and exit 0."""
+    env = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and not r.stdout.strip()
