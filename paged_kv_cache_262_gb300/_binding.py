@@ -60,7 +60,7 @@ def load(path: Optional[str] = None):
         p = path or _build.LIB
         if not os.path.exists(p):
             raise RuntimeError(f"libpagedattn is not built ({p} missing); run "
-                               "`python -m paged_kv_cache_262_gb300.build`")
+                               "`python -c \"import __graft_entry__ as g; g.build()\"` at the repository root")
         lib = _c.CDLL(p)
         i, sz, i64 = _c.c_int, _c.c_size_t, _c.c_int64
         lib.pa_version.restype = _c.c_char_p
