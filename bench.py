@@ -106,6 +106,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every timed step from the host (default: replay the K steps from a CUDA graph)")
+    ap.add_argument("--no-long-context", action="store_true",
+                    help="llama8b_decode: leave out the long-context (8 x 32768) sub-record measured after it")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -254,6 +256,15 @@ def n_layers(args, pool_bytes):
     return min(n, 64)
 
 
+def decode_describe(case, fused):
+    T = len(case.slot_mapping)
+    what = (f"decode with append of {T} tokens (one launch)" if fused
+            else f"reshape_and_cache of {T} tokens + decode")
+    return (f"{case.name}: {case.num_seqs} seqs, ctx {int(case.context_lens.min())}.."
+            f"{int(case.context_lens.max())} (mean {case.context_lens.mean():.0f}), {case.num_q_heads}q/"
+            f"{case.num_kv_heads}kv heads, D={case.head_dim}, B={case.block_size}, {what}")
+
+
 def build_decode(args, torch, pa, dev, case):
     up = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)  # noqa
     NL = n_layers(args, case.k_pool.nbytes * 2)
@@ -291,11 +302,7 @@ def build_decode(args, torch, pa, dev, case):
     dec = decode_bytes(case.context_lens, case.num_q_heads, case.num_kv_heads, case.head_dim, case.block_size)
     T = len(case.slot_mapping)
     cache = cache_bytes(T, case.num_kv_heads, case.head_dim)
-    what = (f"decode with append of {T} tokens (one launch)" if fused
-            else f"reshape_and_cache of {T} tokens + decode")
-    return Bench(case.name, f"{case.name}: {case.num_seqs} seqs, ctx {int(case.context_lens.min())}.."
-                 f"{int(case.context_lens.max())} (mean {case.context_lens.mean():.0f}), {case.num_q_heads}q/"
-                 f"{case.num_kv_heads}kv heads, D={case.head_dim}, B={case.block_size}, {what}",
+    return Bench(case.name, decode_describe(case, fused),
                  {"q": case.q, "new_k": case.new_k, "new_v": case.new_v, "slots": case.slot_mapping,
                   "bt": case.block_tables, "ctx": case.context_lens},
                  step, dec + cache, 1 if fused else 2, "decode_kernel", "hbm", dec + (cache if fused else 0),
@@ -351,6 +358,35 @@ def prefix_sharing_subgroups(plan, bt, ctx):
     return np.array(starts, np.int32), np.array(shared, np.int32)
 
 
+def prefix_modes(args, plan):
+    """(shared-prefix path?, sub-groups as a second level?) for a sharing plan."""
+    name = "prefix_sharing" if plan.prefix_len > 0 else "parallel_sampling"
+    shared = not args.plain_decode
+    sharing = args.sharing if args.sharing != "auto" else ("one-level" if name == "prefix_sharing" else "subgroups")
+    return shared, shared and sharing == "subgroups"
+
+
+def prefix_describe(args, plan, n_pairs):
+    name = "prefix_sharing" if plan.prefix_len > 0 else "parallel_sampling"
+    shared, two = prefix_modes(args, plan)
+    S = plan.num_prompts * plan.samples_per_prompt
+    if plan.prefix_len > 0:
+        mode = ("shared-prefix decode, two levels (prefix attended once on the tensor cores; each prompt's "
+                "suffix blocks once for its samples, each sample's own block for it alone)" if two else
+                "shared-prefix decode (prefix attended once on the tensor cores + per-sequence suffix)" if shared
+                else "plain decode")
+    else:
+        mode = ("sub-group decode (each prompt's blocks read once for its samples, each sample's own block "
+                "for it alone)" if two else
+                "shared-prefix decode, each prompt a group (prompt attended once on the tensor cores)" if shared
+                else "plain decode")
+    shape = (f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512]" if plan.prefix_len > 0
+             else f"prompts of {int(plan.suffix_lens.min())}..{int(plan.suffix_lens.max())} tokens, no common prefix")
+    return (f"{name}: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
+            f"{shape}, {plan.Hq}q/{plan.Hkv}kv, D={plan.D}, B={plan.B}; "
+            f"copy_blocks of {n_pairs} CoW pairs + reshape_and_cache of {S} tokens + {mode}")
+
+
 def build_prefix(args, torch, pa, dev, plan=None):
     plan, bt, ctx, slots, pairs = prefix_sharing_setup(pa, plan)
     name = "prefix_sharing" if plan.prefix_len > 0 else "parallel_sampling"
@@ -365,9 +401,7 @@ def build_prefix(args, torch, pa, dev, plan=None):
     ws = pa.decode_workspace(desc, dev)
     outs = {"out": torch.empty((S, Hq, D), dtype=torch.bfloat16, device=dev)}
 
-    shared = not args.plain_decode
-    sharing = args.sharing if args.sharing != "auto" else ("one-level" if name == "prefix_sharing" else "subgroups")
-    two = shared and sharing == "subgroups"  # the prompts' samples as sub-groups
+    shared, two = prefix_modes(args, plan)
     ss, sh = prefix_sharing_subgroups(plan, bt, ctx)
     if plan.prefix_len > 0:  # one group: the prefix every prompt starts with
         npre = plan.prefix_len // B
@@ -423,24 +457,10 @@ def build_prefix(args, torch, pa, dev, plan=None):
     dec_unique = kv_unique + 2 * S * Hq * D * 2 + int(((ctx.astype(np.int64) + B - 1) // B).sum()) * 4 + S * 4
     dec_logical = decode_bytes(ctx, Hq, Hkv, D, B)
     copy = len(pairs) * Hkv * B * D * 2 * 2 * 2
-    if plan.prefix_len > 0:
-        mode = ("shared-prefix decode, two levels (prefix attended once on the tensor cores; each prompt's "
-                "suffix blocks once for its samples, each sample's own block for it alone)" if two else
-                "shared-prefix decode (prefix attended once on the tensor cores + per-sequence suffix)" if shared
-                else "plain decode")
-    else:
-        mode = ("sub-group decode (each prompt's blocks read once for its samples, each sample's own block "
-                "for it alone)" if two else
-                "shared-prefix decode, each prompt a group (prompt attended once on the tensor cores)" if shared
-                else "plain decode")
     inputs = {"q": q, "new_k": nk, "new_v": nv, "slots": slots, "pairs": pairs, "bt": bt, "ctx": ctx}
     if shared:
         inputs.update(groups)
-    shape = (f"{plan.prefix_len}-token shared prefix (ref_count {S}), suffix U[1,512]" if plan.prefix_len > 0
-             else f"prompts of {int(plan.suffix_lens.min())}..{int(plan.suffix_lens.max())} tokens, no common prefix")
-    return Bench(name, f"{name}: {plan.num_prompts} prompts x {plan.samples_per_prompt} samples, "
-                 f"{shape}, {Hq}q/{Hkv}kv, D={D}, B={B}; "
-                 f"copy_blocks of {len(pairs)} CoW pairs + reshape_and_cache of {S} tokens + {mode}",
+    return Bench(name, prefix_describe(args, plan, len(pairs)),
                  inputs, step, dec_unique + copy + cache_bytes(S, Hkv, D),
                  3 + (1 if shared and len(groups["gp"]) else 0),  # copy, reshape, [prefix pass,] decode
                  "shared_prefix_decode" if shared else "decode_kernel", "hbm", dec_unique, S,
@@ -448,6 +468,13 @@ def build_prefix(args, torch, pa, dev, plan=None):
                         "unique_decode_bytes": dec_unique, "cow_pairs": int(len(pairs))},
                  layers=NL, pool_mb=kp.nbytes * 2 / 1e6,
                  kernels={"shared_prefix_decode" if shared else "decode_kernel": attend})
+
+
+def mixed_describe(cctx, dctx, B, n_new, fused):
+    what = "one mixed-step launch (prefill and decode side by side)" if fused else "prefill + decode"
+    return (f"mixed_step: {len(cctx)} prefill chunks x 512 tokens (ctx {int(min(cctx))}..{int(max(cctx))})"
+            f" + {len(dctx)} decodes (ctx {int(min(dctx))}..{int(max(dctx))}), 32q/8kv, D=128, B={B}; "
+            f"reshape_and_cache of {n_new} tokens + {what}")
 
 
 def build_mixed(args, torch, pa, dev):
@@ -534,10 +561,7 @@ def build_mixed(args, torch, pa, dev):
     new_k = np.concatenate([m.chunk_new_k, dec.new_k])
     new_v = np.concatenate([m.chunk_new_v, dec.new_v])
     slots = np.concatenate([m.chunk_slots, dec.slot_mapping])
-    what = "one mixed-step launch (prefill and decode side by side)" if fused else "prefill + decode"
-    return Bench("mixed_step", f"mixed_step: {len(cctx)} prefill chunks x 512 tokens (ctx {int(cctx.min())}..{int(cctx.max())})"
-                 f" + {dec.num_seqs} decodes (ctx {int(dctx.min())}..{int(dctx.max())}), 32q/8kv, D=128, B={B}; "
-                 f"reshape_and_cache of {Tn} tokens + {what}",
+    return Bench("mixed_step", mixed_describe(cctx, dctx, B, Tn, fused),
                  {"q_chunk": m.q_chunk, "cu_q": m.cu_q, "chunk_bt": m.chunk_tables, "chunk_ctx": m.chunk_ctx,
                   "q": dec.q, "bt": dec.block_tables, "ctx": dec.context_lens, "new_k": new_k, "new_v": new_v,
                   "slots": slots},
@@ -616,6 +640,39 @@ def build(args, torch, pa, dev):
 
 
 # ------------------------------------------------------------------ our arm
+def hbm_probe(torch, pa, dev):
+    """This GPU's HBM stream rates from the library's own probe kernel
+    (pa_hbm_probe): a read-only stream of 16-byte vector loads over 2 GiB, and
+    a 16-byte vector copy of 1 GiB (read + write bytes); best of 10 launches
+    each, CUDA events on the launch stream.  Decode is a read stream, so the
+    read rate is the ceiling its bytes are also reported against."""
+    src = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    src.random_(0, 256)  # nonzero data, so the probe's never-taken store stays never taken
+    sink = torch.zeros(16, dtype=torch.uint8, device=dev)
+    half = src[: 1 << 30]
+    dst = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def best(fn, nbytes):
+        for _ in range(3):
+            fn()
+        out = 0.0
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out = max(out, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
+        return out
+
+    read = best(lambda: pa.hbm_probe(src, sink=sink), src.numel())
+    copy = best(lambda: pa.hbm_probe(half, dst=dst), 2 * half.numel())
+    del src, dst, half, sink
+    torch.cuda.empty_cache()
+    return {"read_gbs": round(read, 1), "copy_gbs": round(copy, 1)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import paged_kv_cache_262_gb300 as pa
@@ -625,8 +682,34 @@ def run_ours(args, rank, world, local_rank):
     pa.load()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    probe = hbm_probe(torch, pa, dev)
     b = build(args, torch, pa, dev)
+    res = measure(args, b, torch, dev, world, rank, sampler, probe)
+    long_ctx = None
+    if args.workload == "llama8b_decode" and not args.no_long_context:
+        # the long-context decode target beside it, in the same process and clock record
+        del b
+        torch.cuda.empty_cache()
+        long_ctx = measure(args, build_decode(args, torch, pa, dev, wl.long_context_decode()), torch, dev, world,
+                           rank, sampler, probe)
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        return None
+    if long_ctx is not None:
+        res["long_context_decode"] = long_ctx
+    if not args.no_cpu_baseline and args.workload != "swap":  # (no attention arithmetic to time there)
+        res["cpu_baseline"] = cpu_baseline(args, args.cpu_seconds)
+    return res
 
+
+def measure(args, b, torch, dev, world, rank, sampler, probe):
+    """Warm-up, the K timed steps, each timed kernel's launch duration, e2e;
+    the JSON fields of one workload (rank 0; None elsewhere)."""
     def to_dev(a):
         t = torch.from_numpy(np.ascontiguousarray(a))
         if a.dtype == np.uint16:
@@ -638,10 +721,6 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     nev = 3 if b.kernel == "prefill_kernel" else 2
 
-    sampler = ClockSampler(local_rank) if rank == 0 else None
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     for i in range(args.warmup):
         b.step(i, x, None)
     torch.cuda.synchronize()
@@ -706,14 +785,14 @@ def run_ours(args, rank, world, local_rank):
             k1.record(stream)
             torch.cuda.synchronize()
             per[name] = k0.elapsed_time(k1) / args.steps
-        k_mean = k_median = per[b.kernel]
+        k_mean, k_median = per[b.kernel], None  # one event pair around K launches: a mean, no median
         if "decode_kernel" in per and b.kernel != "decode_kernel":
             side["decode_launch_ms_mean"] = per["decode_kernel"]
         if "prefill_kernel" in per and b.kernel != "prefill_kernel":
             side["prefill_launch_ms_mean"] = per["prefill_kernel"]
             side["prefill_tflops"] = round(b.extra["prefill_flops"] / (per["prefill_kernel"] / 1e3) / 1e12, 1)
         timing = (f"CUDA graph of the {args.steps} steps; per-kernel launch time from a graph of the kernel's "
-                  f"{args.steps} launches alone")
+                  f"{args.steps} launches alone (a mean)")
     if "decode_launch_ms_mean" in side:
         side["decode_gbs"] = round(b.extra["decode_bytes"] / (side["decode_launch_ms_mean"] / 1e3) / 1e9, 1)
     if world > 1:
@@ -723,8 +802,6 @@ def run_ours(args, rank, world, local_rank):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, b, torch, dev, stream, world)
-    if sampler:
-        sampler.stop()
     ms = max_over_ranks(ms, world, dev)
     if rank != 0:
         return None
@@ -743,6 +820,18 @@ def run_ours(args, rank, world, local_rank):
         peak, unit = peaks["bf16_sustained"], "TFLOP/s"
         peak_note = f"{peaks['source']} bf16_tflops_sustained (kernel timed inside a long step); burst {peaks['bf16']}"
     value = job_throughput(b.step_bytes, args.steps, world, ms)
+    roof = {"bound": b.bound, "kernel": b.kernel, "achieved": round(achieved, 1), "peak": peak,
+            "peak_source": peak_note, "unit": unit, "frac": round(achieved / peak, 4),
+            "traffic": kernel_traffic(b.kernel, b.name), "algorithmic_per_launch": b.kernel_work,
+            "launch_ms_mean": k_mean}
+    if k_median is not None:
+        roof["launch_ms_median"] = k_median
+    if b.bound == "hbm" and probe:
+        roof["read_peak"] = {"peak": probe["read_gbs"], "unit": "GB/s",
+                             "frac": round(achieved / probe["read_gbs"], 4),
+                             "source": "this run's pa_hbm_probe: read-only 16-byte vector loads over 2 GiB, best of "
+                                       "10 (decode streams reads only)",
+                             "copy_probe_gbs": probe["copy_gbs"]}
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -752,10 +841,7 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas{world}"},
         "decode_tokens_per_s": round(b.seqs * args.steps * world / (ms / 1e3), 1),
         "gpu_launches": b.launches * args.steps,
-        "roofline": {"bound": b.bound, "kernel": b.kernel, "achieved": round(achieved, 1), "peak": peak,
-                     "peak_source": peak_note, "unit": unit, "frac": round(achieved / peak, 4),
-                     "traffic": kernel_traffic(b.kernel, b.name), "algorithmic_per_launch": b.kernel_work,
-                     "launch_ms_mean": k_mean, "launch_ms_median": k_median},
+        "roofline": roof,
         "clocks": clocks,
         "timing": timing,
     }
@@ -771,8 +857,6 @@ def run_ours(args, rank, world, local_rank):
         res["workload_extra"] = b.extra
     if e2e:
         res["e2e"] = e2e
-    if not args.no_cpu_baseline and args.workload != "swap":  # (no attention arithmetic to time there)
-        res["cpu_baseline"] = cpu_baseline(args, args.cpu_seconds)
     return res
 
 
@@ -876,9 +960,11 @@ def run_e2e(args, b, torch, dev, stream, world):
 
 # ------------------------------------------------------------------ oracle (CPU) arm
 def oracle_units(args):
-    """The workload as a list of oracle work units; each returns the algorithmic
-    bytes it covered.  Units are whole (sequence, kv head) decode units or whole
-    prefill rows (all heads of one query position)."""
+    """The workload as a list of oracle work units, each returning the
+    algorithmic bytes it covered, with the kind of unit and the workload's
+    description (the GPU arm's config.workload).  Units are whole (sequence,
+    kv head) decode units or whole prefill rows (all heads of one query
+    position)."""
     import oracle
     ora = oracle.default()
     units: List[Callable[[], int]] = []
@@ -897,7 +983,8 @@ def oracle_units(args):
                         ora.prefill_row(m.q_chunk, m.cu_q, kp, vp, m.chunk_tables, m.chunk_ctx, m.decode.scale, r, i, h)
                     return (int(cctx[r]) - 512 + i + 1) * 8 * 128 * 4
                 units.append(u)
-        return units, "prefill rows (all 32 heads of one query position)"
+        return units, "prefill rows (all 32 heads of one query position)", mixed_describe(
+            cctx, dctx, args.block_size, int(m.cu_q[-1]) + len(dctx), args.mixed_launch == "fused")
     if args.workload in ("prefix_sharing", "parallel_sampling"):
         import paged_kv_cache_262_gb300 as pa
         plan, bt, ctx, slots, pairs = prefix_sharing_setup(
@@ -908,9 +995,11 @@ def oracle_units(args):
         ora.reshape_and_cache(nk, nv, kp, vp, slots)
         case = wl.DecodeCase("prefix_sharing", len(ctx), plan.Hq, plan.Hkv, plan.D, plan.B, plan.num_blocks,
                              bt.shape[1], 1 / math.sqrt(plan.D), ctx, bt, q, kp, vp)
+        describe = prefix_describe(args, plan, len(pairs))
     else:
         case = {"llama8b_decode": wl.llama8b_decode, "long_context_decode": wl.long_context_decode,
                 "tiny_decode": wl.tiny_decode}[args.workload]()
+        describe = decode_describe(case, not args.separate_append)
         if case.new_k is not None:
             ora.reshape_and_cache(case.new_k, case.new_v, case.k_pool, case.v_pool, case.slot_mapping)
     G = case.num_q_heads // case.num_kv_heads
@@ -922,7 +1011,7 @@ def oracle_units(args):
                                     case.scale, s, h)
                 return int(case.context_lens[s]) * case.head_dim * 2 * 2 + 2 * G * case.head_dim * 2
             units.append(u)
-    return units, "(sequence, kv head) decode units (all query heads of the group)"
+    return units, "(sequence, kv head) decode units (all query heads of the group)", describe
 
 
 def _run_parallel(ex, n, units, start, count):
@@ -946,7 +1035,7 @@ def host_threads():
 def cpu_baseline(args, budget_s):
     """The fp64 oracle on the host: single thread for half the budget, then
     every host core (independent units in parallel) for the other half."""
-    units, kind = oracle_units(args)
+    units, kind, _ = oracle_units(args)
     secs, nbytes, done = 0.0, 0, 0
     while done < len(units) and secs < budget_s / 2:
         t0 = time.perf_counter()
@@ -973,7 +1062,7 @@ def run_reference(args, rank, world):
         return None
     from oracle import build as obuild
     obuild.build()
-    units, kind = oracle_units(args)
+    units, kind, describe = oracle_units(args)
     n = host_threads()
     t0 = time.perf_counter()
     units[0]()
@@ -995,7 +1084,7 @@ def run_reference(args, rank, world):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "parallelism": f"{n} host threads"},
+            "config": {"workload": describe, "parallelism": f"{n} host threads"},
             "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": n, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

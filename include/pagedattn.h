@@ -251,8 +251,11 @@ int pa_paged_attention_decode_shared_prefix2(const pa_decode_desc *desc, const v
  *    scratch than PA_NOALLOC_SCRATCH_BYTES (pa_decode_workspace_bytes(desc)
  *    tells how much it needs).
  *  - The first call on a device looks up the array's device address with that
- *    device current (cudaGetSymbolAddress) and caches it; make that first call
- *    before any stream capture.
+ *    device current (cudaGetSymbolAddress) and caches it with the id of the
+ *    device's context; make that first call before any stream capture.  A
+ *    call under a different context (after cudaDeviceReset, say) looks the
+ *    address up again, so the first call after a reset must also come before
+ *    any capture.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents; nothing in it has to start at zero (its arrival counters are
  *    tagged per call).  Calls that may overlap on the GPU race on the array:
@@ -350,6 +353,35 @@ int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *con
                    void *const *dst_v_pools, int num_layers, const int64_t *block_pairs, int num_pairs,
                    int src_num_blocks, int dst_num_blocks, size_t block_bytes, int32_t *err_flag,
                    void *stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics
+ * ------------------------------------------------------------------------ */
+
+/* HBM bandwidth probe, the ceiling the decode kernels are measured against
+ * [PHASE] (decode streams the cache from HBM).  mode 0 reads `bytes` from src
+ * with 16-byte vector loads and writes nothing (sink: a device 16-byte word,
+ * written only if the loads' XOR equals a fixed constant -- never with random
+ * data -- so that no load can be dropped; dst unused); mode 1 copies src to
+ * dst with 16-byte vector loads and stores (read + write bytes).  A grid of 8
+ * CTAs of 256 threads per SM strides over the buffer, 8 independent loads in
+ * flight per thread.  src, dst, sink device memory, 16-byte aligned; bytes a
+ * nonzero multiple of 16; use a buffer several times the L2 (129 MB) so the
+ * stream comes from HBM.  PA_ERR_INVALID on bad arguments; asynchronous on
+ * stream (time it with events). */
+int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, void *stream);
+
+/* Self-test of the bounded on-chip wait.  Every kernel of this library waits
+ * on shared-memory mbarriers (for TMA copies and tensor-core MMAs) with a
+ * bound of about 2 s, after which it sets PA_DEVERR_TIMEOUT in *err_flag,
+ * skips the rest of its work and returns, so that a stuck wait cannot hang
+ * the GPU.  This launches one warp that waits, through the same bounded-wait
+ * routine and with the same reporting, on an mbarrier nothing arrives on, for
+ * at most limit_cycles SM cycles (1 .. the library's own bound, 4e9), then
+ * sets *done (device int32) to 1.  Expected result: PA_DEVERR_TIMEOUT in
+ * *err_flag (device int32, may be NULL), *done == 1, and a usable context.
+ * No page describes this call. */
+int pa_selftest_bounded_wait(long long limit_cycles, int32_t *err_flag, int32_t *done, void *stream);
 
 /* ------------------------------------------------------------------------
  * Host block manager [TABLE][SHARE][CHUNK] (plain C++, no GPU): a free list

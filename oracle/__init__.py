@@ -53,6 +53,8 @@ class Oracle:
         lib.ora_reshape_and_cache.argtypes = [i, i, i, i, i, _P, _P, _P, _P, _P]
         lib.ora_copy_blocks.restype = i
         lib.ora_copy_blocks.argtypes = [i, _P, _P, i, _c.c_int64, _P, i]
+        lib.ora_swap_blocks.restype = i
+        lib.ora_swap_blocks.argtypes = [i, _P, _P, _P, _P, i, i, _c.c_int64, _P, i]
         self.lib = lib
         self.path = path
 
@@ -177,6 +179,21 @@ class Oracle:
         vp = (_P * L)(*[_ptr(a) for a in v_pools])
         pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
         return self.lib.ora_copy_blocks(L, kp, vp, nblk, blk, _ptr(pr), pr.shape[0])
+
+    def swap_blocks(self, src_k_pools, src_v_pools, dst_k_pools, dst_v_pools, pairs):
+        """Moves blocks between two sets of pools (e.g. device -> host) IN
+        PLACE in the destination pools; returns the status."""
+        L = len(src_k_pools)
+        assert len(src_v_pools) == L and len(dst_k_pools) == L and len(dst_v_pools) == L
+        for a in list(src_k_pools) + list(src_v_pools) + list(dst_k_pools) + list(dst_v_pools):
+            assert a.dtype == np.uint16 and a.flags.c_contiguous
+        blk = int(np.prod(src_k_pools[0].shape[1:]))
+        assert int(np.prod(dst_k_pools[0].shape[1:])) == blk
+        arr = lambda pools: (_P * L)(*[_ptr(a) for a in pools])  # noqa: E731
+        pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+        return self.lib.ora_swap_blocks(L, arr(src_k_pools), arr(src_v_pools), arr(dst_k_pools), arr(dst_v_pools),
+                                        src_k_pools[0].shape[0], dst_k_pools[0].shape[0], blk, _ptr(pr),
+                                        pr.shape[0])
 
 
 _DEFAULT: Optional[Oracle] = None

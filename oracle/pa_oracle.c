@@ -26,6 +26,10 @@
  *  [SIZE] same page as [ATT] -- "Tuning Checklist for Production / KV Cache
  *         Memory Sizing Formula": bytes per token = 2 * layers * kv_heads *
  *         head_dim * bytes_per_element.
+ *  [SWAP] same page as [ATT] -- "Quick Answers" (KV cache offloading when VRAM
+ *         is full): a paused request's KV blocks move from GPU memory to host
+ *         memory and, once blocks are free again, back to the GPU, so that
+ *         generation resumes where it stopped.
  *
  * Readings where the pages are silent (each one is listed with its reason in
  * the design notes):
@@ -312,6 +316,31 @@ int ora_copy_blocks(int L, uint16_t *const *k_pools, uint16_t *const *v_pools, i
              sizeof(uint16_t) * (size_t)block_elems);
       memcpy(v_pools[l] + dst * block_elems, v_pools[l] + src * block_elems,
              sizeof(uint16_t) * (size_t)block_elems);
+    }
+  return st;
+}
+
+/* [SWAP] preemptive swapping: for each layer l and each (src, dst) pair in
+ * order, block dst of the destination pools (dst_k[l], dst_v[l]) becomes a
+ * copy of block src of the source pools (src_k[l], src_v[l]) -- K and V, every
+ * kv head, token and element.  Source and destination are different pools
+ * (device and host) with their own block counts; block_elems = Hkv * B * D.
+ * A pair outside either pool is skipped and ORA_ERR_PAGE returned. */
+int ora_swap_blocks(int L, const uint16_t *const *src_k, const uint16_t *const *src_v, uint16_t *const *dst_k,
+                    uint16_t *const *dst_v, int src_blocks, int dst_blocks, int64_t block_elems,
+                    const int64_t *pairs, int num_pairs) {
+  int st = ORA_OK;
+  for (int l = 0; l < L; ++l)
+    for (int i = 0; i < num_pairs; ++i) {
+      int64_t from = pairs[2 * i], to = pairs[2 * i + 1];
+      if (from < 0 || from >= src_blocks || to < 0 || to >= dst_blocks) {
+        st |= ORA_ERR_PAGE;
+        continue;
+      }
+      for (int64_t e = 0; e < block_elems; ++e) {
+        dst_k[l][to * block_elems + e] = src_k[l][from * block_elems + e];
+        dst_v[l][to * block_elems + e] = src_v[l][from * block_elems + e];
+      }
     }
   return st;
 }

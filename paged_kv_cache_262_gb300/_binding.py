@@ -31,7 +31,8 @@ EXPORTS = (
     "pa_bm_add_seq_tokens", "pa_bm_num_cached_blocks", "pa_reshape_and_cache", "pa_copy_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_fork", "pa_bm_append", "pa_bm_free_seq",
     "pa_bm_block_table", "pa_bm_seq_len", "pa_bm_ref_count", "pa_bm_num_free", "pa_bm_wasted_slots",
-    "pa_bm_append_batch", "pa_bm_block_tables", "pa_bm_append_token",
+    "pa_bm_append_batch", "pa_bm_block_tables", "pa_bm_append_token", "pa_hbm_probe",
+    "pa_selftest_bounded_wait",
 )
 
 
@@ -138,6 +139,10 @@ def load(path: Optional[str] = None):
         lib.pa_bm_num_free.argtypes = [_P]
         lib.pa_bm_wasted_slots.restype = i64
         lib.pa_bm_wasted_slots.argtypes = [_P]
+        lib.pa_hbm_probe.restype = i
+        lib.pa_hbm_probe.argtypes = [_P, _P, sz, i, _P, _P]
+        lib.pa_selftest_bounded_wait.restype = i
+        lib.pa_selftest_bounded_wait.argtypes = [_c.c_longlong, _P, _P, _P]
         if path is None:
             _LIB = lib
         return lib
@@ -700,3 +705,36 @@ class BlockManager:
 
     def wasted_slots(self) -> int:
         return self._lib.pa_bm_wasted_slots(self._h)
+
+
+# ------------------------------------------------------------------ diagnostics
+def hbm_probe(src, *, dst=None, sink=None, stream=None):
+    """Streams ``src`` (a contiguous CUDA tensor, nbytes a multiple of 16)
+    through 16-byte vector loads: read only (dst None; sink: a CUDA tensor of
+    at least 16 bytes, allocated here when not given) or copied into dst (same
+    nbytes).  Asynchronous; returns nothing."""
+    import torch
+    if not isinstance(src, torch.Tensor) or not src.is_cuda or not src.is_contiguous():
+        raise TypeError("src must be a contiguous CUDA tensor")
+    nbytes = src.numel() * src.element_size()
+    mode = 0 if dst is None else 1
+    if mode == 1:
+        if not isinstance(dst, torch.Tensor) or not dst.is_cuda or not dst.is_contiguous() or \
+                dst.numel() * dst.element_size() != nbytes or dst.device != src.device:
+            raise ValueError("dst must be a contiguous CUDA tensor of src's size on src's device")
+    elif sink is None:
+        sink = torch.empty(16, dtype=torch.uint8, device=src.device)
+    elif not isinstance(sink, torch.Tensor) or not sink.is_cuda or sink.numel() * sink.element_size() < 16:
+        raise ValueError("sink must be a CUDA tensor of at least 16 bytes")
+    _check(load().pa_hbm_probe(src.data_ptr(), _ptr(dst), nbytes, mode, _ptr(sink) if mode == 0 else None,
+                               _stream_ptr(stream)), "pa_hbm_probe")
+
+
+def selftest_bounded_wait(limit_cycles: int, err_flag, done, *, stream=None):
+    """Launches the bounded-wait self-test: one warp waits at most
+    ``limit_cycles`` SM cycles on an mbarrier nothing arrives on, reports
+    PA_DEVERR_TIMEOUT into ``err_flag`` and sets ``done`` (CUDA int32) to 1."""
+    import torch
+    _need(done, torch.int32, "done")
+    _check(load().pa_selftest_bounded_wait(int(limit_cycles), _flag(err_flag), done.data_ptr(), _stream_ptr(stream)),
+           "pa_selftest_bounded_wait")

@@ -10,6 +10,7 @@
 //
 // The call allocates nothing: it resolves the array's device address once per
 // device and hands it to the ordinary decode launcher as its workspace.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -24,23 +25,59 @@ namespace {
 // cudaGetSymbolAddress -- the host-side symbol is only a stand-in.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices];
+struct Cached {
+  unsigned long long ctx_id;  // the context the address belongs to (0: none yet)
+  void *ptr;
+};
+Cached g_scratch[kMaxDevices];
 
-// Device address of the scratch array on the current device, resolved once
-// per device (with that device current) and cached.
+// Id of the calling thread's current context, unique over the process's
+// lifetime (a context created after cudaDeviceReset gets a new one); 0 when
+// there is no current context.  The driver calls come through the runtime's
+// entry-point query, so the library links no driver library.
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch array on the current device.  It is looked
+// up (with that device current) on the first call and again whenever the
+// device's context has changed since -- after cudaDeviceReset the module is
+// loaded anew and the array may sit elsewhere.
 int scratch_address(void **out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  if (id == 0 || g_scratch[dev].ctx_id != id || !g_scratch[dev].ptr) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PA_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    g_scratch[dev] = Cached{current_ctx_id(), p};  // the lookup made the context current if it was not
   }
-  *out = g_scratch_ptr[dev];
+  *out = g_scratch[dev].ptr;
   return PA_OK;
 }
 

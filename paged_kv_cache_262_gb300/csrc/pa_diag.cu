@@ -1,0 +1,119 @@
+// Diagnostics of libpagedattn: the HBM bandwidth probe that the decode
+// kernels' roofline is read against, and a self-test of the bounded on-chip
+// wait that every kernel of the library relies on.
+//
+// Decode is a read stream: "Configuring vLLM and PagedAttention for High
+// Throughput Enterprise LLM Serving" ("Memory Bottlenecks in Autoregressive
+// LLM Inference") has each new token read every cached key and value from
+// HBM.  A copy benchmark (read + write) pays for the DRAM's read/write
+// turnarounds, which a read stream does not, so the probe measures both: a
+// read-only stream of 16-byte vector loads and a 16-byte vector copy.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+#include "pagedattn.h"
+
+namespace pa {
+namespace {
+
+constexpr int kProbeThreads = 256;
+constexpr int kProbeUnroll = 8;     // independent 16-byte loads in flight per thread
+constexpr int kProbeCtasPerSm = 8;  // 2048 threads per SM
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Reads n 16-byte words.  The loads feed an XOR that is stored only when it
+// equals `never` (with random data, never), so nothing is written yet no load
+// can be dropped.
+__global__ void __launch_bounds__(kProbeThreads) hbm_read_kernel(const uint4 *__restrict__ src, size_t n,
+                                                                 uint4 *sink, uint32_t never) {
+  const size_t stride = (size_t)gridDim.x * kProbeThreads;
+  size_t i = (size_t)blockIdx.x * kProbeThreads + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i + (kProbeUnroll - 1) * stride < n; i += kProbeUnroll * stride) {
+    uint4 v[kProbeUnroll];
+#pragma unroll
+    for (int u = 0; u < kProbeUnroll; ++u) v[u] = ld_stream(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kProbeUnroll; ++u) acc ^= v[u].x ^ v[u].y ^ v[u].z ^ v[u].w;
+  }
+  for (; i < n; i += stride) {
+    const uint4 v = ld_stream(src + i);
+    acc ^= v.x ^ v.y ^ v.z ^ v.w;
+  }
+  if (acc == never) *sink = make_uint4(acc, blockIdx.x, threadIdx.x, 0u);
+}
+
+// dst := src, n 16-byte words.
+__global__ void __launch_bounds__(kProbeThreads) hbm_copy_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                                 size_t n) {
+  const size_t stride = (size_t)gridDim.x * kProbeThreads;
+  size_t i = (size_t)blockIdx.x * kProbeThreads + threadIdx.x;
+  for (; i + (kProbeUnroll - 1) * stride < n; i += kProbeUnroll * stride) {
+    uint4 v[kProbeUnroll];
+#pragma unroll
+    for (int u = 0; u < kProbeUnroll; ++u) v[u] = ld_stream(src + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kProbeUnroll; ++u) __stcs(dst + i + u * stride, v[u]);
+  }
+  for (; i < n; i += stride) __stcs(dst + i, ld_stream(src + i));
+}
+
+// One warp waits, as every streaming warp of the decode kernel does, on an
+// mbarrier that nothing arrives on; the wait gives up after limit_cycles and
+// the kernel reports PA_DEVERR_TIMEOUT, then returns.  *done is set last, so
+// the host can tell the kernel ran to its end.
+__global__ void __launch_bounds__(32) bounded_wait_kernel(long long limit_cycles, int32_t *err, int32_t *done) {
+  __shared__ uint64_t bar;
+  const int lane = threadIdx.x;
+  if (lane == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool ok = __all_sync(0xffffffffu, mbar_wait_limit(&bar, 0u, limit_cycles));
+  if (!ok && lane == 0 && err) atomicOr(err, PA_DEVERR_TIMEOUT);
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    *done = 1;
+  }
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, void *stream) {
+  using namespace pa;
+  if (!src || bytes == 0 || (bytes & 15) || !aligned16(src)) return PA_ERR_INVALID;
+  if (mode != 0 && mode != 1) return PA_ERR_INVALID;
+  if (mode == 0 && (!sink || !aligned16(sink))) return PA_ERR_INVALID;
+  if (mode == 1 && (!dst || !aligned16(dst))) return PA_ERR_INVALID;
+  const int sms = current_sm_count();
+  if (sms <= 0) return PA_ERR_CUDA;
+  const size_t n = bytes / 16;
+  const size_t want = (n + kProbeThreads - 1) / kProbeThreads;
+  const unsigned grid = (unsigned)(want < (size_t)sms * kProbeCtasPerSm ? want : (size_t)sms * kProbeCtasPerSm);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode == 0)
+    hbm_read_kernel<<<grid, kProbeThreads, 0, st>>>(static_cast<const uint4 *>(src), n, static_cast<uint4 *>(sink),
+                                                    0x9e3779b9u);
+  else
+    hbm_copy_kernel<<<grid, kProbeThreads, 0, st>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n);
+  return launch_status(cudaGetLastError());
+}
+
+extern "C" int pa_selftest_bounded_wait(long long limit_cycles, int32_t *err_flag, int32_t *done, void *stream) {
+  using namespace pa;
+  if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles || !done) return PA_ERR_INVALID;
+  pa::bounded_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles, err_flag, done);
+  return launch_status(cudaGetLastError());
+}

@@ -2,6 +2,9 @@
 CUDA path's bf16 output with the fp64 oracle."""
 from __future__ import annotations
 
+import concurrent.futures
+import os
+
 import numpy as np
 import pytest
 
@@ -55,3 +58,27 @@ def upload_case(case, torch):
         d["new_v"] = bf16_dev(case.new_v, torch)
         d["slots"] = torch.from_numpy(np.ascontiguousarray(case.slot_mapping, dtype=np.int64)).cuda()
     return d
+
+
+def oracle_rows(ora, case, heads=None):
+    """The oracle's output rows of a decode case for the listed (sequence,
+    query head) pairs (every pair when None), [len(heads)][D], computed on a
+    thread pool over the host cores (the oracle's C calls release the GIL).
+    The case's pools must already hold what the GPU path read."""
+    if heads is None:
+        heads = [(s, h) for s in range(case.num_seqs) for h in range(case.num_q_heads)]
+    if not heads:
+        return np.zeros((0, case.head_dim))
+    try:
+        n = max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        n = max(1, os.cpu_count() or 1)
+
+    def row(sh):
+        out, st = ora.decode_head(case.q, case.k_pool, case.v_pool, case.block_tables, case.context_lens,
+                                  case.scale, sh[0], sh[1])
+        assert st == 0, f"oracle status {st} for {sh}"
+        return out
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        return np.stack(list(ex.map(row, heads)))

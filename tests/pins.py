@@ -377,6 +377,43 @@ def pin_copy_blocks(ora):
     assert np.array_equal(a, b)
 
 
+def pin_swap_blocks(ora):
+    """Preemptive swapping: a sequence's blocks go to a host pool of another
+    size and come back to other device blocks.  Each moved block is bitwise
+    its source, nothing else changes, a pair outside either pool is refused,
+    and the sequence decodes exactly as before through its new table."""
+    st = wl.Stream(13, 14)
+    L, nblk, nhost, Hkv, B, D, Hq = 2, 12, 5, 2, 16, 8, 4
+    dk = [_bf(st, (nblk, Hkv, B, D)) for _ in range(L)]
+    dv = [_bf(st, (nblk, Hkv, B, D)) for _ in range(L)]
+    hk = [np.zeros((nhost, Hkv, B, D), np.uint16) for _ in range(L)]
+    hv = [np.zeros((nhost, Hkv, B, D), np.uint16) for _ in range(L)]
+    table = [6, 1, 10]
+    q = _bf(st, (1, Hq, D))
+    before, _ = ora.decode(q, dk[1], dv[1], np.array([table], np.int32), np.array([37]), 0.3)
+    saved_k = [a.copy() for a in dk]
+    out_pairs = np.array([[6, 3], [1, 0], [10, 4]], np.int64)  # device block -> host block
+    assert ora.swap_blocks(dk, dv, hk, hv, out_pairs) == 0
+    for l in range(L):
+        for src, dst in out_pairs:
+            assert np.array_equal(hk[l][dst], dk[l][src]) and np.array_equal(hv[l][dst], dv[l][src])
+        assert not hk[l][1].any() and not hv[l][2].any()  # untouched host blocks
+        assert np.array_equal(dk[l], saved_k[l])  # the source is only read
+        for b in table:  # the device blocks are handed to someone else
+            dk[l][b] = 0
+            dv[l][b] = 0
+    in_pairs = np.array([[3, 2], [0, 8], [4, 11]], np.int64)  # host block -> new device block
+    assert ora.swap_blocks(hk, hv, dk, dv, in_pairs) == 0
+    after, _ = ora.decode(q, dk[1], dv[1], np.array([[2, 8, 11]], np.int32), np.array([37]), 0.3)
+    assert np.array_equal(before, after)
+    for l in range(L):
+        assert np.array_equal(dk[l][[2, 8, 11]], saved_k[l][table])
+    snap = [a.copy() for a in hk]
+    assert ora.swap_blocks(dk, dv, hk, hv, np.array([[0, nhost]], np.int64)) & 2  # past the host pool
+    assert ora.swap_blocks(dk, dv, hk, hv, np.array([[nblk, 0]], np.int64)) & 2  # past the device pool
+    assert all(np.array_equal(a, b) for a, b in zip(hk, snap))
+
+
 def pin_kv_sizing(ora):
     """The pages' KV sizing example: 2 x 80 x 8 x 128 x 2 = 327,680 bytes/token."""
     fx = json.load(open(os.path.join(GOLDEN, "kv_sizing_llama31_70b.json")))

@@ -123,6 +123,24 @@ def test_new_entry_points_validate_before_any_gpu_work(lib):
     assert call_sp2(_desc(num_seqs=0), 2, 16, 16, 4) == pa.PA_OK  # nothing to decode
 
 
+def test_diagnostics_validate_before_any_gpu_work(lib):
+    """The HBM probe and the bounded-wait self-test refuse bad arguments on the
+    host: sizes that are not whole 16-byte words, misaligned or missing
+    buffers, an unknown mode, a wait bound outside 1 .. the library's own."""
+    probe = lib.pa_hbm_probe
+    assert probe(16, None, 0, 0, 16, None) == pa.PA_ERR_INVALID      # no bytes
+    assert probe(16, None, 24, 0, 16, None) == pa.PA_ERR_INVALID     # not a multiple of 16
+    assert probe(8, None, 32, 0, 16, None) == pa.PA_ERR_INVALID      # misaligned source
+    assert probe(None, None, 32, 0, 16, None) == pa.PA_ERR_INVALID
+    assert probe(16, None, 32, 0, None, None) == pa.PA_ERR_INVALID   # read mode needs its sink
+    assert probe(16, None, 32, 1, 16, None) == pa.PA_ERR_INVALID     # copy mode needs dst
+    assert probe(16, 16, 32, 2, 16, None) == pa.PA_ERR_INVALID       # unknown mode
+    wait = lib.pa_selftest_bounded_wait
+    assert wait(0, None, 16, None) == pa.PA_ERR_INVALID
+    assert wait(4000000001, None, 16, None) == pa.PA_ERR_INVALID
+    assert wait(1000, None, None, None) == pa.PA_ERR_INVALID
+
+
 def test_binding_checks_shapes_and_devices_before_any_call():
     """The plain-pointer C ABI cannot see buffer sizes, so the binding refuses
     arguments that would make a kernel read or write past a tensor: K and V

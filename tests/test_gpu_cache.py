@@ -173,13 +173,21 @@ def test_swap_out_and_back_in_is_bit_exact(torch, ora):
     out_pairs = np.array([(d, h) for h, d in enumerate(table2)], np.int64)  # device block -> host block
     pa.swap_blocks(dk, dv, hk, hv, torch.from_numpy(out_pairs).cuda(), err_flag=err)
     torch.cuda.synchronize()
+    # the oracle applies the same moves to host copies of every pool
+    ok_ = [a.copy() for a in kps]
+    ov_ = [a.copy() for a in vps]
+    ohk = [np.zeros((nhost,) + case.k_pool.shape[1:], np.uint16) for _ in range(L)]
+    ohv = [np.zeros_like(a) for a in ohk]
+    assert ora.swap_blocks(ok_, ov_, ohk, ohv, out_pairs) == 0
     for l in range(L):
-        got_k = hk[l].view(torch.int16).numpy().view(np.uint16)
-        assert np.array_equal(got_k[: len(table2)], kps[l][table2])
+        assert np.array_equal(hk[l].view(torch.int16).numpy().view(np.uint16), ohk[l])
+        assert np.array_equal(hv[l].view(torch.int16).numpy().view(np.uint16), ohv[l])
     # the device blocks get reused by someone else
     for l in range(L):
         dk[l][table2] = 0
         dv[l][table2] = 0
+        ok_[l][table2] = 0
+        ov_[l][table2] = 0
     # bring the pages back into other (free) device blocks
     used = set(int(b) for b in case.block_tables.flatten() if b >= 0)
     free = [b for b in range(case.num_blocks) if b not in used][: len(table2)]
@@ -187,9 +195,9 @@ def test_swap_out_and_back_in_is_bit_exact(torch, ora):
     pa.swap_blocks(hk, hv, dk, dv, torch.from_numpy(in_pairs).cuda(), err_flag=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+    assert ora.swap_blocks(ohk, ohv, ok_, ov_, in_pairs) == 0
     for l in range(L):
-        assert np.array_equal(bf16_host(dk[l])[free], kps[l][table2])
-        assert np.array_equal(bf16_host(dv[l])[free], vps[l][table2])
+        assert np.array_equal(bf16_host(dk[l]), ok_[l]) and np.array_equal(bf16_host(dv[l]), ov_[l])
     bt = case.block_tables.copy()
     bt[2, : len(table2)] = free
     again = bf16_host(pa.paged_attention_decode(bf16_dev(case.q, torch), dk[0], dv[0], torch.from_numpy(bt).cuda(),

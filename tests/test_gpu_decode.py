@@ -7,7 +7,7 @@ import pytest
 
 import paged_kv_cache_262_gb300 as pa
 import workloads as wl
-from gpu_util import assert_close, bf16_host, need_gpu, upload_case
+from gpu_util import assert_close, bf16_host, need_gpu, oracle_rows, upload_case
 
 pytestmark = pytest.mark.gpu
 
@@ -74,19 +74,19 @@ def test_llama8b_decode_full(torch, ora, parts, pp):
     assert_close(bf16_host(out), ref, f"llama8b_decode pp={pp}")
 
 
-def test_long_context_decode_sampled(torch, ora):
-    """8 x 32768 tokens, GQA 8, split-K: sampled heads against the oracle."""
+def test_long_context_decode_full(torch, ora):
+    """8 x 32768 tokens, GQA 8, split-K: every (sequence, query head) row
+    against the oracle."""
     case = wl.long_context_decode()
     d = upload_case(case, torch)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = run_step(torch, case, d, err)
     kp, vp = oracle_step(ora, case)
     got = bf16_host(out)
-    heads = [(s, h) for s in range(case.num_seqs) for h in (0, 7, 8, 37, 63)]
     sub = case.__class__(**{**case.__dict__, "k_pool": kp, "v_pool": vp})
-    ref = ora.decode_case(sub, heads=heads)
+    ref = oracle_rows(ora, sub).reshape(got.shape)
     assert int(err.item()) == 0
-    assert_close(np.stack([got[s, h] for s, h in heads]), ref, "long_context_decode")
+    assert_close(got, ref, "long_context_decode")
 
 
 SHAPES = [  # (Hq, Hkv, D, B)

@@ -29,6 +29,10 @@ MUTANTS = {
     "cache_negative_slot_written": ("if (slot < 0) continue;", "if (slot < 0) slot = 0;"),
     "copy_reversed": ("int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];",
                       "int64_t dst = pairs[2 * i], src = pairs[2 * i + 1];"),
+    "swap_reversed": ("int64_t from = pairs[2 * i], to = pairs[2 * i + 1];",
+                      "int64_t to = pairs[2 * i], from = pairs[2 * i + 1];"),
+    "swap_bound_of_other_pool": ("from >= src_blocks || to < 0 || to >= dst_blocks",
+                                 "from >= dst_blocks || to < 0 || to >= src_blocks"),
     "sizing_one_tensor": ("return 2 * layers * kv_heads * head_dim * elem_bytes;",
                           "return layers * kv_heads * head_dim * elem_bytes;"),
 }
