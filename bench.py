@@ -95,8 +95,8 @@ def parse():
                          "which one goes to the side stream and whether that stream has high priority")
     ap.add_argument("--sharing", default="auto", choices=["auto", "one-level", "subgroups"],
                     help="prefix_sharing / parallel_sampling: groups only (one level), or each prompt's samples "
-                         "as sub-groups too; auto = one level for prefix_sharing (short suffixes: the per-sample "
-                         "units win), sub-groups for parallel_sampling (long prompts: reading them once wins)")
+                         "as sub-groups too (auto: sub-groups; each prompt's blocks are read once for its "
+                         "samples)")
     ap.add_argument("--separate-append", action="store_true",
                     help="decode workloads: reshape_and_cache and decode as two launches instead of one "
                          "decode-with-append launch")
@@ -362,7 +362,7 @@ def prefix_modes(args, plan):
     """(shared-prefix path?, sub-groups as a second level?) for a sharing plan."""
     name = "prefix_sharing" if plan.prefix_len > 0 else "parallel_sampling"
     shared = not args.plain_decode
-    sharing = args.sharing if args.sharing != "auto" else ("one-level" if name == "prefix_sharing" else "subgroups")
+    sharing = args.sharing if args.sharing != "auto" else "subgroups"
     return shared, shared and sharing == "subgroups"
 
 
@@ -641,11 +641,12 @@ def build(args, torch, pa, dev):
 
 # ------------------------------------------------------------------ our arm
 def hbm_probe(torch, pa, dev):
-    """This GPU's HBM stream rates from the library's own probe kernel
-    (pa_hbm_probe): a read-only stream of 16-byte vector loads over 2 GiB, and
-    a 16-byte vector copy of 1 GiB (read + write bytes); best of 10 launches
-    each, CUDA events on the launch stream.  Decode is a read stream, so the
-    read rate is the ceiling its bytes are also reported against."""
+    """This GPU's HBM stream rates from the library's own probe kernels
+    (pa_hbm_probe): read-only streams over 2 GiB through 16-byte vector loads
+    and through TMA bulk copies into shared memory, and a 16-byte vector copy
+    of 1 GiB (read + write bytes); best of 10 launches each, CUDA events on
+    the launch stream.  Decode is a read stream (TMA page gathers), so the
+    faster read rate is the ceiling its bytes are also reported against."""
     src = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
     src.random_(0, 256)  # nonzero data, so the probe's never-taken store stays never taken
     sink = torch.zeros(16, dtype=torch.uint8, device=dev)
@@ -666,11 +667,17 @@ def hbm_probe(torch, pa, dev):
             out = max(out, nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9)
         return out
 
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
     read = best(lambda: pa.hbm_probe(src, sink=sink), src.numel())
+    tma = best(lambda: pa.hbm_probe(src, tma=True, err_flag=err), src.numel())
     copy = best(lambda: pa.hbm_probe(half, dst=dst), 2 * half.numel())
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"HBM probe: device error flag {int(err.item())}")
     del src, dst, half, sink
     torch.cuda.empty_cache()
-    return {"read_gbs": round(read, 1), "copy_gbs": round(copy, 1)}
+    return {"read_gbs": round(max(read, tma), 1), "read_lsu_gbs": round(read, 1), "read_tma_gbs": round(tma, 1),
+            "copy_gbs": round(copy, 1)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -829,8 +836,10 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
     if b.bound == "hbm" and probe:
         roof["read_peak"] = {"peak": probe["read_gbs"], "unit": "GB/s",
                              "frac": round(achieved / probe["read_gbs"], 4),
-                             "source": "this run's pa_hbm_probe: read-only 16-byte vector loads over 2 GiB, best of "
-                                       "10 (decode streams reads only)",
+                             "source": "this run's pa_hbm_probe, the faster of two read-only streams over 2 GiB "
+                                       "(16-byte vector loads; TMA bulk copies into shared memory), best of 10 "
+                                       "(decode streams reads only)",
+                             "read_lsu_gbs": probe["read_lsu_gbs"], "read_tma_gbs": probe["read_tma_gbs"],
                              "copy_probe_gbs": probe["copy_gbs"]}
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,

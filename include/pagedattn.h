@@ -359,17 +359,23 @@ int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *con
  * ------------------------------------------------------------------------ */
 
 /* HBM bandwidth probe, the ceiling the decode kernels are measured against
- * [PHASE] (decode streams the cache from HBM).  mode 0 reads `bytes` from src
- * with 16-byte vector loads and writes nothing (sink: a device 16-byte word,
- * written only if the loads' XOR equals a fixed constant -- never with random
- * data -- so that no load can be dropped; dst unused); mode 1 copies src to
- * dst with 16-byte vector loads and stores (read + write bytes).  A grid of 8
- * CTAs of 256 threads per SM strides over the buffer, 8 independent loads in
- * flight per thread.  src, dst, sink device memory, 16-byte aligned; bytes a
- * nonzero multiple of 16; use a buffer several times the L2 (129 MB) so the
- * stream comes from HBM.  PA_ERR_INVALID on bad arguments; asynchronous on
- * stream (time it with events). */
-int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, void *stream);
+ * [PHASE] (decode streams the cache from HBM).
+ *  mode 0: reads `bytes` from src with 16-byte vector loads and writes nothing
+ *          (sink: a device 16-byte word, written only if the loads' XOR equals
+ *          a fixed constant -- never with random data -- so that no load can
+ *          be dropped); 8 CTAs of 256 threads per SM stride over the buffer,
+ *          8 independent loads in flight per thread.
+ *  mode 1: copies src to dst with 16-byte vector loads and stores (read +
+ *          write bytes), same grid.
+ *  mode 2: reads `bytes` from src through the TMA engine (bulk copies of 16 KB
+ *          into an 8-slot shared-memory ring, one CTA per SM), the path the
+ *          decode kernels' page gathers take; its bounded waits report
+ *          PA_DEVERR_TIMEOUT into *err_flag (device int32, may be NULL).
+ * src, dst, sink device memory, 16-byte aligned (dst only for mode 1, sink
+ * only for mode 0); bytes a nonzero multiple of 16; use a buffer several times
+ * the L2 (129 MB) so the stream comes from HBM.  PA_ERR_INVALID on bad
+ * arguments; asynchronous on stream (time it with events). */
+int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, int32_t *err_flag, void *stream);
 
 /* Self-test of the bounded on-chip wait.  Every kernel of this library waits
  * on shared-memory mbarriers (for TMA copies and tensor-core MMAs) with a

@@ -140,7 +140,7 @@ def load(path: Optional[str] = None):
         lib.pa_bm_wasted_slots.restype = i64
         lib.pa_bm_wasted_slots.argtypes = [_P]
         lib.pa_hbm_probe.restype = i
-        lib.pa_hbm_probe.argtypes = [_P, _P, sz, i, _P, _P]
+        lib.pa_hbm_probe.argtypes = [_P, _P, sz, i, _P, _P, _P]
         lib.pa_selftest_bounded_wait.restype = i
         lib.pa_selftest_bounded_wait.argtypes = [_c.c_longlong, _P, _P, _P]
         if path is None:
@@ -708,17 +708,21 @@ class BlockManager:
 
 
 # ------------------------------------------------------------------ diagnostics
-def hbm_probe(src, *, dst=None, sink=None, stream=None):
-    """Streams ``src`` (a contiguous CUDA tensor, nbytes a multiple of 16)
-    through 16-byte vector loads: read only (dst None; sink: a CUDA tensor of
-    at least 16 bytes, allocated here when not given) or copied into dst (same
+def hbm_probe(src, *, dst=None, sink=None, tma=False, err_flag=None, stream=None):
+    """Streams ``src`` (a contiguous CUDA tensor, nbytes a multiple of 16):
+    read only through 16-byte vector loads (dst None; sink: a CUDA tensor of
+    at least 16 bytes, allocated here when not given), read only through TMA
+    bulk copies into shared memory (tma=True), or copied into dst (same
     nbytes).  Asynchronous; returns nothing."""
     import torch
     if not isinstance(src, torch.Tensor) or not src.is_cuda or not src.is_contiguous():
         raise TypeError("src must be a contiguous CUDA tensor")
     nbytes = src.numel() * src.element_size()
-    mode = 0 if dst is None else 1
-    if mode == 1:
+    mode = 2 if tma else 0 if dst is None else 1
+    if mode == 2:
+        if dst is not None:
+            raise ValueError("the TMA read mode takes no dst")
+    elif mode == 1:
         if not isinstance(dst, torch.Tensor) or not dst.is_cuda or not dst.is_contiguous() or \
                 dst.numel() * dst.element_size() != nbytes or dst.device != src.device:
             raise ValueError("dst must be a contiguous CUDA tensor of src's size on src's device")
@@ -727,7 +731,7 @@ def hbm_probe(src, *, dst=None, sink=None, stream=None):
     elif not isinstance(sink, torch.Tensor) or not sink.is_cuda or sink.numel() * sink.element_size() < 16:
         raise ValueError("sink must be a CUDA tensor of at least 16 bytes")
     _check(load().pa_hbm_probe(src.data_ptr(), _ptr(dst), nbytes, mode, _ptr(sink) if mode == 0 else None,
-                               _stream_ptr(stream)), "pa_hbm_probe")
+                               _flag(err_flag), _stream_ptr(stream)), "pa_hbm_probe")
 
 
 def selftest_bounded_wait(limit_cycles: int, err_flag, done, *, stream=None):

@@ -67,6 +67,43 @@ __global__ void __launch_bounds__(kProbeThreads) hbm_copy_kernel(const uint4 *__
   for (; i < n; i += stride) __stcs(dst + i, ld_stream(src + i));
 }
 
+// Reads n_bytes through the TMA engine: bulk copies (cp.async.bulk) of
+// kBulkChunk bytes from global into a ring of kBulkSlots shared-memory slots,
+// the path the decode kernels' page gathers take.  Chunk c goes to CTA
+// c mod gridDim.x; one thread issues, reusing a slot once its copy has landed.
+constexpr int kBulkChunk = 16384;
+constexpr int kBulkSlots = 8;
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__global__ void __launch_bounds__(32) hbm_bulk_read_kernel(const uint8_t *__restrict__ src, size_t n_bytes,
+                                                           int32_t *err) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t bars[kBulkSlots];
+  if (threadIdx.x != 0) return;
+  for (int i = 0; i < kBulkSlots; ++i) mbar_init(&bars[i], 1);
+  fence_mbar_init();
+  const size_t nchunks = (n_bytes + kBulkChunk - 1) / kBulkChunk;
+  long long k = 0;  // this CTA's copies issued so far
+  for (size_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++k) {
+    const int slot = (int)(k % kBulkSlots);
+    if (k >= kBulkSlots && !mbar_wait(&bars[slot], (uint32_t)(((k / kBulkSlots) - 1) & 1))) {
+      if (err) atomicOr(err, PA_DEVERR_TIMEOUT);
+      break;  // the copies still in flight are waited for below
+    }
+    const size_t off = c * kBulkChunk;
+    const uint32_t bytes = (uint32_t)(n_bytes - off < (size_t)kBulkChunk ? n_bytes - off : (size_t)kBulkChunk);
+    mbar_arrive_expect_tx(&bars[slot], bytes);
+    bulk_load(ring + slot * kBulkChunk, src + off, bytes, &bars[slot]);
+  }
+  // the last use of every slot: its copy must land before the CTA exits
+  for (long long j = k - kBulkSlots < 0 ? 0 : k - kBulkSlots; j < k; ++j)
+    if (!mbar_wait(&bars[j % kBulkSlots], (uint32_t)((j / kBulkSlots) & 1)) && err) atomicOr(err, PA_DEVERR_TIMEOUT);
+}
+
 // One warp waits, as every streaming warp of the decode kernel does, on an
 // mbarrier that nothing arrives on; the wait gives up after limit_cycles and
 // the kernel reports PA_DEVERR_TIMEOUT, then returns.  *done is set last, so
@@ -91,10 +128,11 @@ __global__ void __launch_bounds__(32) bounded_wait_kernel(long long limit_cycles
 }  // namespace
 }  // namespace pa
 
-extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, void *stream) {
+extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, void *sink, int32_t *err_flag,
+                            void *stream) {
   using namespace pa;
   if (!src || bytes == 0 || (bytes & 15) || !aligned16(src)) return PA_ERR_INVALID;
-  if (mode != 0 && mode != 1) return PA_ERR_INVALID;
+  if (mode < 0 || mode > 2) return PA_ERR_INVALID;
   if (mode == 0 && (!sink || !aligned16(sink))) return PA_ERR_INVALID;
   if (mode == 1 && (!dst || !aligned16(dst))) return PA_ERR_INVALID;
   const int sms = current_sm_count();
@@ -103,6 +141,16 @@ extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, 
   const size_t want = (n + kProbeThreads - 1) / kProbeThreads;
   const unsigned grid = (unsigned)(want < (size_t)sms * kProbeCtasPerSm ? want : (size_t)sms * kProbeCtasPerSm);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (mode == 2) {
+    constexpr int kRing = kBulkSlots * kBulkChunk;
+    if (cudaFuncSetAttribute(hbm_bulk_read_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRing) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    const size_t chunks = (bytes + kBulkChunk - 1) / kBulkChunk;
+    const unsigned g = (unsigned)(chunks < (size_t)sms ? chunks : (size_t)sms);  // one CTA (its ring) per SM
+    hbm_bulk_read_kernel<<<g, 32, kRing, st>>>(static_cast<const uint8_t *>(src), bytes, err_flag);
+    return launch_status(cudaGetLastError());
+  }
   if (mode == 0)
     hbm_read_kernel<<<grid, kProbeThreads, 0, st>>>(static_cast<const uint4 *>(src), n, static_cast<uint4 *>(sink),
                                                     0x9e3779b9u);

@@ -92,4 +92,32 @@ int prefill_launch(const pa_decode_desc *d, const void *q, const int32_t *cu_q, 
 // Most key ranges the shared-prefix pass splits a prefix into.
 constexpr int kMaxPrefixParts = 8;
 
+// Task decode (pa_decode_tasks.cu): parts a unit's pages are cut into at
+// most, and sub-groups (or sequences) one launch takes at most.
+constexpr int kTaskMaxParts = 16;
+constexpr int kTaskMaxSub = 512;
+
+// Workspace of the task decode: per-part partial states of every query row,
+// arrival counters, the task counters.
+size_t task_workspace_bytes(const pa_decode_desc *d);
+
+// Whether the task decode takes this call: head_dim 128, 1 .. kTaskMaxSub
+// sub-groups (at most num_seqs), at most 16 query rows a unit.
+bool tasks_supported(const pa_decode_desc *d, int nsg, int rows);
+
+// Zeroes the task decode's counters in its workspace (stream-ordered); must
+// precede decode_tasks_launch on the stream.
+int decode_tasks_clear(const pa_decode_desc *d, void *workspace, void *stream);
+
+// The shared-prefix decode's second launch as a queue of small tasks: every
+// (sub-group, kv head) -- or (sequence, kv head) when pre.nsub == 0 -- with
+// the group prefix's partial states (pre) folded in.  rows bounds a unit's
+// query rows (members x heads).  workspace: task_workspace_bytes(d), cleared
+// by decode_tasks_clear.  Launched as a programmatic dependent of the kernel
+// before it (it reads nothing that kernel writes) and followed by a merge
+// launch that reads pre's states.
+int decode_tasks_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
+                        const int32_t *block_tables, const int32_t *context_lens, const DecodePrefix &pre, int rows,
+                        void *out, void *workspace, int32_t *err_flag, void *stream);
+
 }  // namespace pa

@@ -56,6 +56,10 @@ template <int B, int G, bool PARTIAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const PrefillArgs a) {
+  // The partial-state pass (a group's shared prefix) lets a programmatic
+  // dependent start beside it at once: the shared-prefix decode's task grid
+  // reads nothing this pass writes.
+  if constexpr (PARTIAL) asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   prefill_tile<B, G, PARTIAL>(&tmK, &tmV, a, blockIdx.x, blockIdx.y, blockIdx.z, gridDim.x, smem);

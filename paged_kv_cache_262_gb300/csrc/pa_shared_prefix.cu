@@ -17,6 +17,7 @@
 // prompt -- are decoded as one unit per (sub-group, kv head), reading those
 // blocks once for all members (the sub-group mode of the decode unit).
 #include <cuda_runtime.h>
+#include <stdlib.h>
 
 #include <algorithm>
 
@@ -28,8 +29,8 @@ namespace {
 size_t up256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 struct Layout {
-  size_t decode, pre_o, pre_ml;
-  size_t total() const { return decode + pre_o + pre_ml; }
+  size_t decode, pre_o, pre_ml, tasks;
+  size_t total() const { return decode + pre_o + pre_ml + tasks; }
 };
 
 Layout layout(const pa_decode_desc *d) {
@@ -37,7 +38,23 @@ Layout layout(const pa_decode_desc *d) {
   l.decode = up256(pa::make_decode_plan(d, pa::current_sm_count()).total());
   l.pre_o = up256((size_t)pa::kMaxPrefixParts * d->num_seqs * d->num_q_heads * d->head_dim * sizeof(float));
   l.pre_ml = up256((size_t)pa::kMaxPrefixParts * d->num_seqs * d->num_q_heads * 2 * sizeof(float));
+  l.tasks = d->head_dim == 128 ? up256(pa::task_workspace_bytes(d)) : 0;
   return l;
+}
+
+// The second launch as a task queue (pa_decode_tasks.cu) for sub-groups
+// behind a group prefix: what is left past the prefix is short (a prompt's
+// own blocks and each sample's copy-on-write block), where one CTA per unit
+// spends most of its life starting and finishing (prefix sharing, 64 prompts
+// x 4 samples: 55.6 us one level, 59.6 us sub-groups, 42-43 us as tasks).
+// Long units stay with the one-CTA-per-unit decode (parallel sampling: 124
+// us against 137-142 as tasks; one level with groups: 55.6 against 68-70).
+// PA_DECODE_TASKS=0 / 1 in the environment forces the choice (comparison).
+bool use_tasks(const pa_decode_desc *d, int nsg, int rows, bool subgroups_behind_prefix) {
+  const char *env = getenv("PA_DECODE_TASKS");
+  if (env && env[0] == '0') return false;
+  if (!(env && env[0] == '1') && !subgroups_behind_prefix) return false;
+  return pa::tasks_supported(d, nsg, rows);
 }
 
 }  // namespace
@@ -74,9 +91,19 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
     sub.nsub = num_subgroups;
     sub.sub_rows = max_subgroup_size * G;
   }
-  if (num_groups == 0)
+  if (num_groups == 0) {
+    if (num_subgroups > 0 && use_tasks(d, num_subgroups, sub.sub_rows, false)) {
+      const Layout l = layout(d);
+      if (!workspace || workspace_bytes < l.total() || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+      uint8_t *tws = static_cast<uint8_t *>(workspace) + l.decode + l.pre_o + l.pre_ml;
+      st = decode_tasks_clear(d, tws, stream);
+      if (st != PA_OK) return st;
+      return decode_tasks_launch(d, q, k_pool, v_pool, block_tables, context_lens, sub, sub.sub_rows, out, tws,
+                                 err_flag, stream);
+    }
     return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, workspace, workspace_bytes, err_flag,
                          stream, num_subgroups > 0 ? &sub : nullptr);
+  }
   if (!group_starts || !group_prefix_lens || !prefix_tables || prefix_max_blocks == 0 || max_group_size == 0 ||
       max_prefix_len == 0)
     return PA_ERR_INVALID;
@@ -95,6 +122,13 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
   kparts = std::min(kparts, (max_prefix_len + 127) / 128);
   const int kpart_len = ((max_prefix_len + kparts - 1) / kparts + 127) / 128 * 128;
   kparts = (max_prefix_len + kpart_len - 1) / kpart_len;
+  const int nsg = num_subgroups > 0 ? num_subgroups : d->num_seqs;
+  const int rows = num_subgroups > 0 ? sub.sub_rows : G;
+  const bool tasks = use_tasks(d, nsg, rows, num_subgroups > 0);
+  if (tasks) {  // before the prefix pass: the task grid may start beside it
+    st = decode_tasks_clear(d, ws + l.decode + l.pre_o + l.pre_ml, stream);
+    if (st != PA_OK) return st;
+  }
   pa_decode_desc pd = *d;
   pd.num_seqs = num_groups;
   pd.max_blocks_per_seq = prefix_max_blocks;
@@ -111,6 +145,9 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
   pre.pre_o = pre_o;
   pre.pre_ml = pre_ml;
   pre.npre = kparts;
+  if (tasks)
+    return decode_tasks_launch(d, q, k_pool, v_pool, block_tables, context_lens, pre, rows, out,
+                               ws + l.decode + l.pre_o + l.pre_ml, err_flag, stream);
   return decode_launch(d, q, k_pool, v_pool, block_tables, context_lens, out, ws, l.decode, err_flag, stream, &pre);
 }
 

@@ -128,13 +128,13 @@ def test_diagnostics_validate_before_any_gpu_work(lib):
     host: sizes that are not whole 16-byte words, misaligned or missing
     buffers, an unknown mode, a wait bound outside 1 .. the library's own."""
     probe = lib.pa_hbm_probe
-    assert probe(16, None, 0, 0, 16, None) == pa.PA_ERR_INVALID      # no bytes
-    assert probe(16, None, 24, 0, 16, None) == pa.PA_ERR_INVALID     # not a multiple of 16
-    assert probe(8, None, 32, 0, 16, None) == pa.PA_ERR_INVALID      # misaligned source
-    assert probe(None, None, 32, 0, 16, None) == pa.PA_ERR_INVALID
-    assert probe(16, None, 32, 0, None, None) == pa.PA_ERR_INVALID   # read mode needs its sink
-    assert probe(16, None, 32, 1, 16, None) == pa.PA_ERR_INVALID     # copy mode needs dst
-    assert probe(16, 16, 32, 2, 16, None) == pa.PA_ERR_INVALID       # unknown mode
+    assert probe(16, None, 0, 0, 16, None, None) == pa.PA_ERR_INVALID      # no bytes
+    assert probe(16, None, 24, 0, 16, None, None) == pa.PA_ERR_INVALID     # not a multiple of 16
+    assert probe(8, None, 32, 0, 16, None, None) == pa.PA_ERR_INVALID      # misaligned source
+    assert probe(None, None, 32, 0, 16, None, None) == pa.PA_ERR_INVALID
+    assert probe(16, None, 32, 0, None, None, None) == pa.PA_ERR_INVALID   # read mode needs its sink
+    assert probe(16, None, 32, 1, 16, None, None) == pa.PA_ERR_INVALID     # copy mode needs dst
+    assert probe(16, 16, 32, 3, 16, None, None) == pa.PA_ERR_INVALID       # unknown mode
     wait = lib.pa_selftest_bounded_wait
     assert wait(0, None, 16, None) == pa.PA_ERR_INVALID
     assert wait(4000000001, None, 16, None) == pa.PA_ERR_INVALID

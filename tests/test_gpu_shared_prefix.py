@@ -19,6 +19,17 @@ def torch():
     return need_gpu()
 
 
+@pytest.fixture(params=["auto", "tasks", "units"])
+def decode_kernel(request, monkeypatch):
+    """The second launch of the shared-prefix decode: the library's choice,
+    the task-queue kernel forced, or one CTA per unit forced."""
+    if request.param == "auto":
+        monkeypatch.delenv("PA_DECODE_TASKS", raising=False)
+    else:
+        monkeypatch.setenv("PA_DECODE_TASKS", "1" if request.param == "tasks" else "0")
+    return request.param
+
+
 def grouped_case(Hq, Hkv, D, B, groups, ungrouped, seed):
     """groups: list of (members, prefix_len); each member gets a random suffix
     (0 .. 300 tokens); ungrouped: number of extra sequences without a shared
@@ -81,7 +92,7 @@ SHAPES = [(32, 8, 128, 16), (64, 8, 128, 32), (16, 16, 128, 16), (32, 2, 128, 16
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "q%dkv%dd%db%d" % s)
 @pytest.mark.parametrize("pp", [None, 2])
-def test_shared_prefix_small(torch, ora, monkeypatch, shape, pp):
+def test_shared_prefix_small(torch, ora, monkeypatch, shape, pp, decode_kernel):
     if pp is None:
         monkeypatch.delenv("PA_PARTITION_PAGES", raising=False)
     else:
@@ -123,7 +134,7 @@ def test_shared_prefix_workload(torch, ora):
     assert_close(shared, (plain.astype(np.uint32) << 16).view(np.float32).astype(np.float64), "shared vs plain")
 
 
-def test_prefix_not_block_multiple_flagged(torch):
+def test_prefix_not_block_multiple_flagged(torch, decode_kernel):
     case, gs, gp, pt = grouped_case(32, 8, 128, 16, [(3, 64)], 2, seed=5)
     gp = gp + 3  # not a whole number of blocks
     pt = np.concatenate([pt, pt[:, :1]], axis=1)  # room for the extra tokens
@@ -131,11 +142,12 @@ def test_prefix_not_block_multiple_flagged(torch):
     shared, plain = run_both(torch, case, gs, gp, pt, err)
     assert int(err.item()) & pa.DEVERR_CTX
     assert not np.any(shared[:3])                  # the group's rows: zeros, as for any bad context
-    assert np.array_equal(shared[3:], plain[3:])   # sequences outside the group: plain decode
+    # sequences outside the group: decoded as usual (plain decode's result, within rounding)
+    assert_close(shared[3:], to_f64(plain[3:]), "sequences outside the bad group")
 
 
 @pytest.mark.parametrize("pp", [None, 2])
-def test_shared_prefix_graph_replay(torch, monkeypatch, pp):
+def test_shared_prefix_graph_replay(torch, monkeypatch, pp, decode_kernel):
     """Captured once and replayed: the merge counters are reset by each merge,
     so every replay (same epoch) merges again and gives the same bits."""
     if pp is None:
@@ -257,7 +269,7 @@ NESTED = {
 
 @pytest.mark.parametrize("shape", list(NESTED), ids=lambda s: "q%dkv%dd%db%d" % s)
 @pytest.mark.parametrize("pp", [None, 2])
-def test_subgroups_against_oracle(torch, ora, monkeypatch, shape, pp):
+def test_subgroups_against_oracle(torch, ora, monkeypatch, shape, pp, decode_kernel):
     if pp is None:
         monkeypatch.delenv("PA_PARTITION_PAGES", raising=False)
     else:
@@ -272,7 +284,7 @@ def test_subgroups_against_oracle(torch, ora, monkeypatch, shape, pp):
     assert_close(got, ref, f"sub-groups {shape} pp={pp}")
 
 
-def test_subgroup_bad_shared_length_flagged(torch):
+def test_subgroup_bad_shared_length_flagged(torch, decode_kernel):
     spec = [(4, [(2, [3, 5]), (1, [8, 9])])]
     case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, spec, seed=3)
     sh = sh.copy()
@@ -289,7 +301,7 @@ def test_subgroup_bad_shared_length_flagged(torch):
     assert_close(got[2:], to_f64(bf16_host(plain)[2:]), "the other sub-group")
 
 
-def test_subgroups_graph_replay(torch):
+def test_subgroups_graph_replay(torch, decode_kernel):
     case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, NESTED[(32, 8, 128, 16)], seed=7)
     x = nested_inputs(torch, case, gs, gp, pt, ss, sh)
     want = bf16_host(launch_nested(x))
@@ -344,7 +356,7 @@ def test_subgroups_prefix_sharing_workload(torch, ora, which):
     assert_close(got, ref, f"{which}, sub-groups")
 
 
-def test_subgroup_guards(torch):
+def test_subgroup_guards(torch, decode_kernel):
     """A sub-group wider than max_subgroup_size promised (more query rows than
     the launch's MMA width) and sub-group starts outside the batch are refused
     in the kernel: PA_DEVERR_CTX, nothing read or written for them, the other
@@ -377,3 +389,21 @@ def test_subgroup_guards(torch):
     assert int(err.item()) & pa.DEVERR_CTX
     assert_close(got[:5], to_f64(plain[:5]), "in-range sub-groups")
     assert not np.any(got[5:])  # the refused sub-group's rows are left alone (zeros from the caller)
+
+
+def test_task_decode_edges(torch, ora, monkeypatch):
+    """The task-queue kernel on its edge cases, against the oracle: a unit cut
+    into the most parts (four long members behind a shared stretch), units
+    with no keys past the group prefix (every member ends at the prefix: the
+    rows are the prefix's states alone), one-member units, and a sub-group
+    outside every group beside them."""
+    monkeypatch.setenv("PA_DECODE_TASKS", "1")
+    spec = [(3, [(20, [600, 601, 590, 615]), (0, [0, 0]), (0, [0]), (1, [7])]),
+            (None, [(2, [1, 300])])]
+    case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, spec, seed=23)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = run_nested(torch, case, gs, gp, pt, ss, sh, err)
+    assert int(err.item()) == 0
+    ref, st = ora.decode_case(case)
+    assert np.all(st == 0)
+    assert_close(got, ref, "task decode edges")
