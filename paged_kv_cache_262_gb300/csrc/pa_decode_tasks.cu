@@ -47,6 +47,7 @@
 
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
+#include "pa_units.cuh"
 #include "pagedattn.h"
 
 namespace pa {
@@ -104,42 +105,6 @@ struct TaskSmem {
   static constexpr int kBytes = kStageOff + (kStageSeqs + 2 * kStageGroups + 1) * 4;
   static constexpr int kAlloc = kBytes + 1024;
 };
-
-// Sub-group sg (first sequence s0, s1 past its last; kshared: the end of the
-// keys its members share, -1 for a sequence alone): its group prefix (the
-// unit's first key) and page count past that prefix (-1: invalid).  One
-// thread; contexts and groups through the accessors (shared or global memory).
-template <class Ctx, class Gs, class Gp>
-__device__ void subgroup_plan(const TaskArgs &a, int B, int s0, int s1, int kshared, Ctx ctx_at, Gs gstart_at,
-                              Gp gprefix_at, int *kstart_out, int *pages_out) {
-  const int nm = s1 - s0;
-  int kstart = 0;
-  if (a.ngroups > 0 && s0 >= 0 && s0 < a.S && s0 >= gstart_at(0) && s0 < gstart_at(a.ngroups)) {
-    int lo = 0, hi = a.ngroups;  // grp_start[lo] <= s0 < grp_start[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (gstart_at(mid) <= s0) lo = mid;
-      else hi = mid;
-    }
-    kstart = gprefix_at(lo);
-  }
-  if (kshared < 0) kshared = kstart;
-  bool ok = s0 >= 0 && nm > 0 && s1 <= a.S && nm * a.G <= a.rows && kstart >= 0 && kshared >= kstart &&
-            kshared % B == 0 && kstart % B == 0;
-  int own = 0;
-  int c[16];  // a valid sub-group has at most 16 members (16 query rows); loads issued together
-#pragma unroll
-  for (int m = 0; m < 16; ++m) c[m] = ok && m < nm ? ctx_at(s0 + m) : 0;
-#pragma unroll
-  for (int m = 0; m < 16; ++m)
-    if (m < nm) {
-      ok = ok && c[m] >= kshared && c[m] > 0 && c[m] <= a.max_blocks * B && c[m] <= a.max_ctx;
-      own += (c[m] + B - 1) / B - kshared / B;
-    }
-  const int n = (kshared - kstart) / B + own;
-  *kstart_out = kstart;
-  *pages_out = ok && n <= kTaskMaxParts * 32 ? n : -1;
-}
 
 // Pages per part of a unit of n pages: at least min_pages, at most 16 parts
 // (a part's entries fit the 32 lanes: n <= 512).
@@ -199,15 +164,16 @@ __global__ void __launch_bounds__(W * 32, 1)
     if (sg < a.nsg) sg_kshared[sg] = a.sub_start ? __ldg(a.sub_shared + sg) : -1;
   }
   __syncthreads();
+  const UnitShape us{a.S, a.G, a.rows, a.max_blocks, a.max_ctx, a.ngroups};
   for (int sg = tid; sg < a.nsg; sg += NTH) {
     int ks, n;
     if (staged)
       subgroup_plan(
-          a, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return ctx_s[i]; },
+          us, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return ctx_s[i]; },
           [&](int i) { return gstart_s[i]; }, [&](int i) { return gprefix_s[i]; }, &ks, &n);
     else
       subgroup_plan(
-          a, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return __ldg(a.ctx + i); },
+          us, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return __ldg(a.ctx + i); },
           [&](int i) { return __ldg(a.grp_start + i); }, [&](int i) { return __ldg(a.grp_prefix + i); }, &ks, &n);
     if (sg_kshared[sg] < 0) sg_kshared[sg] = ks;
     sg_kstart[sg] = ks;
@@ -726,6 +692,13 @@ bool tasks_supported(const pa_decode_desc *d, int nsg, int rows) {
   return d->head_dim == kTD && nsg > 0 && nsg <= kTaskMaxSub && nsg <= d->num_seqs && rows > 0 && rows <= 16 &&
          (long long)d->num_kv_heads * nsg * (kTaskMaxParts + 1) < (1ll << 30) &&
          (long long)d->num_seqs * d->num_q_heads < (1ll << 31);
+}
+
+unsigned int *task_counter(const pa_decode_desc *d, void *workspace) {
+  const size_t R = (size_t)d->num_seqs * d->num_q_heads;
+  return reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(workspace) +
+                                          up256(kTaskMaxParts * R * kTD * sizeof(float)) +
+                                          up256(kTaskMaxParts * R * 2 * sizeof(float)));
 }
 
 int decode_tasks_clear(const pa_decode_desc *d, void *workspace, void *stream) {

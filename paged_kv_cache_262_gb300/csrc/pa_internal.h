@@ -109,6 +109,26 @@ bool tasks_supported(const pa_decode_desc *d, int nsg, int rows);
 // precede decode_tasks_launch on the stream.
 int decode_tasks_clear(const pa_decode_desc *d, void *workspace, void *stream);
 
+// The task decode's counter word in its workspace (zeroed by
+// decode_tasks_clear); the wide-group decode takes its units from it.
+unsigned int *task_counter(const pa_decode_desc *d, void *workspace);
+
+// Whether the wide-group decode (pa_decode_wide.cu) takes this call: head_dim
+// 128, 1 .. kTaskMaxSub units' sub-groups (at most num_seqs), at most 16 query
+// rows a unit.
+bool wide_supported(const pa_decode_desc *d, int nsg, int rows);
+
+// The shared-prefix decode's second launch on the tensor cores: every
+// (sub-group, kv head) -- or (sequence, kv head) when pre.nsub == 0 -- with
+// its rows (at most 16) as the MMA N side and 128-token key tiles as M, the
+// group prefix's partial states folded in.  counter: a zeroed word
+// (task_counter after decode_tasks_clear).  Launched as a programmatic
+// dependent of the kernel before it (it waits for that kernel before reading
+// pre's states).
+int decode_wide_launch(const pa_decode_desc *d, const void *q, const void *k_pool, const void *v_pool,
+                       const int32_t *block_tables, const int32_t *context_lens, const DecodePrefix &pre, int rows,
+                       void *out, unsigned int *counter, int32_t *err_flag, void *stream);
+
 // The shared-prefix decode's second launch as a queue of small tasks: every
 // (sub-group, kv head) -- or (sequence, kv head) when pre.nsub == 0 -- with
 // the group prefix's partial states (pre) folded in.  rows bounds a unit's

@@ -237,6 +237,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 #undef PA_R32
+#define PA_R16(i) "=r"(r[i])
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : PA_R16(0), PA_R16(1), PA_R16(2), PA_R16(3), PA_R16(4), PA_R16(5), PA_R16(6), PA_R16(7), PA_R16(8),
+        PA_R16(9), PA_R16(10), PA_R16(11), PA_R16(12), PA_R16(13), PA_R16(14), PA_R16(15)
+      : "r"(taddr)
+      : "memory");
+}
+#undef PA_R16
 #define PA_W32(i) "r"(r[i])
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(

@@ -57,6 +57,19 @@ bool use_tasks(const pa_decode_desc *d, int nsg, int rows, bool subgroups_behind
   return pa::tasks_supported(d, nsg, rows);
 }
 
+// The second launch on the tensor cores (pa_decode_wide.cu), taken only with
+// PA_DECODE_WIDE=1 in the environment: on these units it is slower than the
+// warp-MMA kernels (parallel sampling 160 us against 123 us one CTA per unit;
+// prefix sharing 84 us against 43.6 us as tasks) -- each 128-token tile
+// passes through a chain of S MMA, TMEM load, a four-warp maxima exchange,
+// P^T through shared memory behind a proxy fence, the P V MMA and a TMEM
+// fold, and three 64 KB tiles in flight per SM do not cover that chain.
+bool use_wide(const pa_decode_desc *d, int nsg, int rows) {
+  const char *env = getenv("PA_DECODE_WIDE");
+  if (!(env && env[0] == '1')) return false;
+  return pa::wide_supported(d, nsg, rows);
+}
+
 }  // namespace
 
 extern "C" size_t pa_shared_prefix_workspace_bytes(const pa_decode_desc *desc) {
@@ -92,6 +105,15 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
     sub.sub_rows = max_subgroup_size * G;
   }
   if (num_groups == 0) {
+    if (num_subgroups > 0 && use_wide(d, num_subgroups, sub.sub_rows)) {
+      const Layout l = layout(d);
+      if (!workspace || workspace_bytes < l.total() || !aligned16(workspace)) return PA_ERR_WORKSPACE;
+      uint8_t *tws = static_cast<uint8_t *>(workspace) + l.decode + l.pre_o + l.pre_ml;
+      st = decode_tasks_clear(d, tws, stream);
+      if (st != PA_OK) return st;
+      return decode_wide_launch(d, q, k_pool, v_pool, block_tables, context_lens, sub, sub.sub_rows, out,
+                                task_counter(d, tws), err_flag, stream);
+    }
     if (num_subgroups > 0 && use_tasks(d, num_subgroups, sub.sub_rows, false)) {
       const Layout l = layout(d);
       if (!workspace || workspace_bytes < l.total() || !aligned16(workspace)) return PA_ERR_WORKSPACE;
@@ -124,8 +146,9 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
   kparts = (max_prefix_len + kpart_len - 1) / kpart_len;
   const int nsg = num_subgroups > 0 ? num_subgroups : d->num_seqs;
   const int rows = num_subgroups > 0 ? sub.sub_rows : G;
-  const bool tasks = use_tasks(d, nsg, rows, num_subgroups > 0);
-  if (tasks) {  // before the prefix pass: the task grid may start beside it
+  const bool wide = use_wide(d, nsg, rows);
+  const bool tasks = !wide && use_tasks(d, nsg, rows, num_subgroups > 0);
+  if (tasks || wide) {  // before the prefix pass: the second grid may start beside it
     st = decode_tasks_clear(d, ws + l.decode + l.pre_o + l.pre_ml, stream);
     if (st != PA_OK) return st;
   }
@@ -145,6 +168,9 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
   pre.pre_o = pre_o;
   pre.pre_ml = pre_ml;
   pre.npre = kparts;
+  if (wide)
+    return decode_wide_launch(d, q, k_pool, v_pool, block_tables, context_lens, pre, rows, out,
+                              task_counter(d, ws + l.decode + l.pre_o + l.pre_ml), err_flag, stream);
   if (tasks)
     return decode_tasks_launch(d, q, k_pool, v_pool, block_tables, context_lens, pre, rows, out,
                                ws + l.decode + l.pre_o + l.pre_ml, err_flag, stream);

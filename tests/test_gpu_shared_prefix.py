@@ -19,14 +19,20 @@ def torch():
     return need_gpu()
 
 
-@pytest.fixture(params=["auto", "tasks", "units"])
+@pytest.fixture(params=["auto", "tasks", "units", "wide"])
 def decode_kernel(request, monkeypatch):
     """The second launch of the shared-prefix decode: the library's choice,
-    the task-queue kernel forced, or one CTA per unit forced."""
-    if request.param == "auto":
-        monkeypatch.delenv("PA_DECODE_TASKS", raising=False)
-    else:
-        monkeypatch.setenv("PA_DECODE_TASKS", "1" if request.param == "tasks" else "0")
+    the task-queue kernel, one CTA per unit, or the tensor-core (wide-group)
+    kernel, forced."""
+    monkeypatch.delenv("PA_DECODE_TASKS", raising=False)
+    monkeypatch.delenv("PA_DECODE_WIDE", raising=False)
+    if request.param == "tasks":
+        monkeypatch.setenv("PA_DECODE_TASKS", "1")
+    elif request.param == "units":
+        monkeypatch.setenv("PA_DECODE_TASKS", "0")
+        monkeypatch.setenv("PA_DECODE_WIDE", "0")
+    elif request.param == "wide":
+        monkeypatch.setenv("PA_DECODE_WIDE", "1")
     return request.param
 
 
@@ -326,7 +332,7 @@ def test_subgroups_graph_replay(torch, decode_kernel):
 
 
 @pytest.mark.parametrize("which", ["prefix_sharing", "parallel_sampling"])
-def test_subgroups_prefix_sharing_workload(torch, ora, which):
+def test_subgroups_prefix_sharing_workload(torch, ora, which, decode_kernel):
     """The prefix-sharing workload with its second level (the 4 samples of each
     prompt share the prompt's full suffix blocks), and the parallel-sampling
     workload (no common prefix, sub-groups only) -- bench --workload ..."""
@@ -391,13 +397,15 @@ def test_subgroup_guards(torch, decode_kernel):
     assert not np.any(got[5:])  # the refused sub-group's rows are left alone (zeros from the caller)
 
 
-def test_task_decode_edges(torch, ora, monkeypatch):
-    """The task-queue kernel on its edge cases, against the oracle: a unit cut
-    into the most parts (four long members behind a shared stretch), units
-    with no keys past the group prefix (every member ends at the prefix: the
-    rows are the prefix's states alone), one-member units, and a sub-group
-    outside every group beside them."""
-    monkeypatch.setenv("PA_DECODE_TASKS", "1")
+@pytest.mark.parametrize("kernel", ["tasks", "wide"])
+def test_unit_kernel_edges(torch, ora, monkeypatch, kernel):
+    """The task-queue and wide-group kernels on their edge cases, against the
+    oracle: a long unit (four long members behind a shared stretch: the most
+    parts of a task unit, many key tiles of a wide one), units with no keys
+    past the group prefix (every member ends at the prefix: the rows are the
+    prefix's states alone), one-member units, and a sub-group outside every
+    group beside them."""
+    monkeypatch.setenv("PA_DECODE_TASKS" if kernel == "tasks" else "PA_DECODE_WIDE", "1")
     spec = [(3, [(20, [600, 601, 590, 615]), (0, [0, 0]), (0, [0]), (1, [7])]),
             (None, [(2, [1, 300])])]
     case, gs, gp, pt, ss, sh = nested_case(32, 8, 128, 16, spec, seed=23)
@@ -406,4 +414,4 @@ def test_task_decode_edges(torch, ora, monkeypatch):
     assert int(err.item()) == 0
     ref, st = ora.decode_case(case)
     assert np.all(st == 0)
-    assert_close(got, ref, "task decode edges")
+    assert_close(got, ref, f"{kernel} decode edges")
