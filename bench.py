@@ -108,6 +108,8 @@ def parse():
                     help="launch every timed step from the host (default: replay the K steps from a CUDA graph)")
     ap.add_argument("--no-long-context", action="store_true",
                     help="llama8b_decode: leave out the long-context (8 x 32768) sub-record measured after it")
+    ap.add_argument("--no-probe", action="store_true",
+                    help="skip the HBM read/copy probe (its launches would crowd a profiler's launch list)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     return ap.parse_args()
@@ -693,7 +695,7 @@ def run_ours(args, rank, world, local_rank):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    probe = hbm_probe(torch, pa, dev)
+    probe = None if args.no_probe else hbm_probe(torch, pa, dev)
     b = build(args, torch, pa, dev)
     res = measure(args, b, torch, dev, world, rank, sampler, probe)
     long_ctx = None
