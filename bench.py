@@ -647,8 +647,10 @@ def hbm_probe(torch, pa, dev):
     (pa_hbm_probe): read-only streams over 2 GiB through 16-byte vector loads
     and through TMA bulk copies into shared memory, and a 16-byte vector copy
     of 1 GiB (read + write bytes); best of 10 launches each, CUDA events on
-    the launch stream.  Decode is a read stream (TMA page gathers), so the
-    faster read rate is the ceiling its bytes are also reported against."""
+    the launch stream; and the same bytes read as paged decode reads them
+    (4 KB runs at scattered places, the decode kernel's concurrency).  Decode
+    is a read stream of page gathers, so it is also reported against the
+    faster read rate and against the gather rate."""
     src = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
     src.random_(0, 256)  # nonzero data, so the probe's never-taken store stays never taken
     sink = torch.zeros(16, dtype=torch.uint8, device=dev)
@@ -672,6 +674,8 @@ def hbm_probe(torch, pa, dev):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     read = best(lambda: pa.hbm_probe(src, sink=sink), src.numel())
     tma = best(lambda: pa.hbm_probe(src, tma=True, err_flag=err), src.numel())
+    runs = 1 << (int(src.numel() // 2 // 4096).bit_length() - 1)  # 4 KB runs read in each half
+    gather = best(lambda: pa.hbm_probe(src, gather=True, err_flag=err), 2 * 4096 * runs)
     copy = best(lambda: pa.hbm_probe(half, dst=dst), 2 * half.numel())
     torch.cuda.synchronize()
     if int(err.item()):
@@ -679,7 +683,7 @@ def hbm_probe(torch, pa, dev):
     del src, dst, half, sink
     torch.cuda.empty_cache()
     return {"read_gbs": round(max(read, tma), 1), "read_lsu_gbs": round(read, 1), "read_tma_gbs": round(tma, 1),
-            "copy_gbs": round(copy, 1)}
+            "gather_gbs": round(gather, 1), "copy_gbs": round(copy, 1)}
 
 
 def run_ours(args, rank, world, local_rank):
@@ -843,6 +847,11 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
                                        "(decode streams reads only)",
                              "read_lsu_gbs": probe["read_lsu_gbs"], "read_tma_gbs": probe["read_tma_gbs"],
                              "copy_probe_gbs": probe["copy_gbs"]}
+        roof["gather_peak"] = {"peak": probe["gather_gbs"], "unit": "GB/s",
+                               "frac": round(achieved / probe["gather_gbs"], 4),
+                               "source": "this run's pa_hbm_probe mode 3: 4 KB K/V runs at scattered places with "
+                                         "the decode kernel's concurrency and no arithmetic (what paged reads can "
+                                         "reach), best of 10"}
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",

@@ -371,6 +371,13 @@ int pa_swap_blocks(void *const *src_k_pools, void *const *src_v_pools, void *con
  *          into an 8-slot shared-memory ring, one CTA per SM), the path the
  *          decode kernels' page gathers take; its bounded waits report
  *          PA_DEVERR_TIMEOUT into *err_flag (device int32, may be NULL).
+ *  mode 3: reads like paged decode: 4 KB runs (a (block, kv head) of 16
+ *          tokens x 128 bf16) as K/V pairs at pseudo-random places (a
+ *          permutation of the runs of each half of src), with the decode
+ *          kernel's concurrency (2 CTAs of 4 warps per SM, three 8 KB slots a
+ *          warp); reads the largest power-of-two number of runs fitting each
+ *          half (bytes read: 2 x 4096 x that number, which the caller counts);
+ *          timeouts as in mode 2.
  * src, dst, sink device memory, 16-byte aligned (dst only for mode 1, sink
  * only for mode 0); bytes a nonzero multiple of 16; use a buffer several times
  * the L2 (129 MB) so the stream comes from HBM.  PA_ERR_INVALID on bad

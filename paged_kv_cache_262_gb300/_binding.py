@@ -708,20 +708,22 @@ class BlockManager:
 
 
 # ------------------------------------------------------------------ diagnostics
-def hbm_probe(src, *, dst=None, sink=None, tma=False, err_flag=None, stream=None):
+def hbm_probe(src, *, dst=None, sink=None, tma=False, gather=False, err_flag=None, stream=None):
     """Streams ``src`` (a contiguous CUDA tensor, nbytes a multiple of 16):
     read only through 16-byte vector loads (dst None; sink: a CUDA tensor of
     at least 16 bytes, allocated here when not given), read only through TMA
-    bulk copies into shared memory (tma=True), or copied into dst (same
-    nbytes).  Asynchronous; returns nothing."""
+    bulk copies into shared memory (tma=True), read as paged decode reads
+    (gather=True: 4 KB K/V runs at scattered places; the bytes read are the
+    largest power-of-two number of runs fitting each half, times 2 x 4096), or
+    copied into dst (same nbytes).  Asynchronous; returns nothing."""
     import torch
     if not isinstance(src, torch.Tensor) or not src.is_cuda or not src.is_contiguous():
         raise TypeError("src must be a contiguous CUDA tensor")
     nbytes = src.numel() * src.element_size()
-    mode = 2 if tma else 0 if dst is None else 1
-    if mode == 2:
+    mode = 3 if gather else 2 if tma else 0 if dst is None else 1
+    if mode >= 2:
         if dst is not None:
-            raise ValueError("the TMA read mode takes no dst")
+            raise ValueError("the TMA read modes take no dst")
     elif mode == 1:
         if not isinstance(dst, torch.Tensor) or not dst.is_cuda or not dst.is_contiguous() or \
                 dst.numel() * dst.element_size() != nbytes or dst.device != src.device:

@@ -104,6 +104,53 @@ __global__ void __launch_bounds__(32) hbm_bulk_read_kernel(const uint8_t *__rest
     if (!mbar_wait(&bars[j % kBulkSlots], (uint32_t)((j / kBulkSlots) & 1)) && err) atomicOr(err, PA_DEVERR_TIMEOUT);
 }
 
+// Reads like paged decode: K and V runs of 4 KB (one (block, kv head) of 16
+// tokens x 128 bf16) at scattered places, with the decode kernel's
+// concurrency -- 2 CTAs per SM, 4 warps each, every warp a ring of three 8 KB
+// slots (a K run and a V run).  The buffer's first half holds the K runs, the
+// second the V runs; run i of a warp's stream is at (i * 0x9E3779B1) mod the
+// number of runs in a half (a power of two: a permutation), so consecutive
+// reads land far apart as a block table's scattered pages do.
+constexpr int kGatherRun = 4096;
+constexpr int kGatherSlots = 3;
+__global__ void __launch_bounds__(128) hbm_gather_kernel(const uint8_t *__restrict__ src, uint32_t runs_log2,
+                                                         int per_warp, int32_t *err) {
+  extern __shared__ uint8_t raw[];
+  __shared__ uint64_t bars[4 * kGatherSlots];
+  uint8_t *ring = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t *mb = bars + warp * kGatherSlots;
+  uint8_t *slots = ring + warp * kGatherSlots * 2 * kGatherRun;
+  if (lane == 0) {
+    for (int i = 0; i < kGatherSlots; ++i) mbar_init(&mb[i], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint32_t mask = (1u << runs_log2) - 1u;
+  const size_t half = (size_t)kGatherRun << runs_log2;
+  const uint32_t base = (uint32_t)(blockIdx.x * 4 + warp) * (uint32_t)per_warp;
+  auto issue = [&](int i) {
+    const size_t r = (size_t)(((base + (uint32_t)i) * 0x9E3779B1u) & mask) * kGatherRun;
+    uint64_t *b = &mb[i % kGatherSlots];
+    uint8_t *d = slots + (i % kGatherSlots) * 2 * kGatherRun;
+    mbar_arrive_expect_tx(b, 2 * kGatherRun);
+    bulk_load(d, src + r, kGatherRun, b);
+    bulk_load(d + kGatherRun, src + half + r, kGatherRun, b);
+  };
+  if (lane == 0)
+    for (int i = 0; i < kGatherSlots && i < per_warp; ++i) issue(i);
+  int i = 0;
+  for (; i < per_warp; ++i) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&mb[i % kGatherSlots], (uint32_t)((i / kGatherSlots) & 1)))) {
+      if (lane == 0 && err) atomicOr(err, PA_DEVERR_TIMEOUT);
+      break;
+    }
+    if (lane == 0 && i + kGatherSlots < per_warp) issue(i + kGatherSlots);
+  }
+  for (int k = i + 1; k < per_warp && k < i + kGatherSlots; ++k)  // after a timeout: copies in flight land
+    mbar_wait(&mb[k % kGatherSlots], (uint32_t)((k / kGatherSlots) & 1));
+}
+
 // One warp waits, as every streaming warp of the decode kernel does, on an
 // mbarrier that nothing arrives on; the wait gives up after limit_cycles and
 // the kernel reports PA_DEVERR_TIMEOUT, then returns.  *done is set last, so
@@ -132,9 +179,13 @@ extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, 
                             void *stream) {
   using namespace pa;
   if (!src || bytes == 0 || (bytes & 15) || !aligned16(src)) return PA_ERR_INVALID;
-  if (mode < 0 || mode > 2) return PA_ERR_INVALID;
+  if (mode < 0 || mode > 3) return PA_ERR_INVALID;
   if (mode == 0 && (!sink || !aligned16(sink))) return PA_ERR_INVALID;
   if (mode == 1 && (!dst || !aligned16(dst))) return PA_ERR_INVALID;
+  // mode 3: the largest power-of-two number of 4 KB runs that fits each half of the buffer
+  uint32_t lg = 0;
+  while (lg < 30 && ((size_t)kGatherRun << (lg + 1)) * 2 <= bytes) ++lg;
+  if (mode == 3 && ((size_t)kGatherRun << lg) * 2 > bytes) return PA_ERR_INVALID;
   const int sms = current_sm_count();
   if (sms <= 0) return PA_ERR_CUDA;
   const size_t n = bytes / 16;
@@ -149,6 +200,17 @@ extern "C" int pa_hbm_probe(const void *src, void *dst, size_t bytes, int mode, 
     const size_t chunks = (bytes + kBulkChunk - 1) / kBulkChunk;
     const unsigned g = (unsigned)(chunks < (size_t)sms ? chunks : (size_t)sms);  // one CTA (its ring) per SM
     hbm_bulk_read_kernel<<<g, 32, kRing, st>>>(static_cast<const uint8_t *>(src), bytes, err_flag);
+    return launch_status(cudaGetLastError());
+  }
+  if (mode == 3) {
+    const int ctas = 2 * sms;
+    const size_t runs = (size_t)1 << lg;
+    const int per_warp = (int)(runs / ((size_t)ctas * 4) > 0 ? runs / ((size_t)ctas * 4) : 1);
+    constexpr int kRingBytes = 4 * kGatherSlots * 2 * kGatherRun + 1024;
+    if (cudaFuncSetAttribute(hbm_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes) !=
+        cudaSuccess)
+      return PA_ERR_CUDA;
+    hbm_gather_kernel<<<ctas, 128, kRingBytes, st>>>(static_cast<const uint8_t *>(src), lg, per_warp, err_flag);
     return launch_status(cudaGetLastError());
   }
   if (mode == 0)

@@ -134,7 +134,8 @@ def test_diagnostics_validate_before_any_gpu_work(lib):
     assert probe(None, None, 32, 0, 16, None, None) == pa.PA_ERR_INVALID
     assert probe(16, None, 32, 0, None, None, None) == pa.PA_ERR_INVALID   # read mode needs its sink
     assert probe(16, None, 32, 1, 16, None, None) == pa.PA_ERR_INVALID     # copy mode needs dst
-    assert probe(16, 16, 32, 3, 16, None, None) == pa.PA_ERR_INVALID       # unknown mode
+    assert probe(16, 16, 32, 4, 16, None, None) == pa.PA_ERR_INVALID       # unknown mode
+    assert probe(16, None, 4096, 3, None, None, None) == pa.PA_ERR_INVALID  # gather: not one 4 KB run a half
     wait = lib.pa_selftest_bounded_wait
     assert wait(0, None, 16, None) == pa.PA_ERR_INVALID
     assert wait(4000000001, None, 16, None) == pa.PA_ERR_INVALID
