@@ -201,8 +201,10 @@ class ClockSampler:
             for n, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"], f[5:9]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
+        pw = [num(f[3]) for f in win if num(f[3]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][2]),
-                "reasons": sorted(reasons), "samples": len(win), "window": label}
+                "reasons": sorted(reasons), "samples": len(win), "window": label,
+                "power_w": statistics.median(pw) if pw else None}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:

@@ -136,18 +136,28 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *pre_o = reinterpret_cast<float *>(ws + l.decode);
   float *pre_ml = reinterpret_cast<float *>(ws + l.decode + l.pre_o);
-  // 1. each group's shared prefix, all of its rows at once, on the tensor cores;
-  //    key ranges so that the pass has about one CTA per SM
-  const long long base = (long long)num_groups * d->num_kv_heads * (((long long)max_group_size * G + 255) / 256);
-  const int sms = std::max(current_sm_count(), 1);
-  int kparts = (int)std::min<long long>(kMaxPrefixParts, std::max<long long>(1, (sms + base - 1) / base));
-  kparts = std::min(kparts, (max_prefix_len + 127) / 128);
-  const int kpart_len = ((max_prefix_len + kparts - 1) / kparts + 127) / 128 * 128;
-  kparts = (max_prefix_len + kpart_len - 1) / kpart_len;
   const int nsg = num_subgroups > 0 ? num_subgroups : d->num_seqs;
   const int rows = num_subgroups > 0 ? sub.sub_rows : G;
   const bool wide = use_wide(d, nsg, rows);
   const bool tasks = !wide && use_tasks(d, nsg, rows, num_subgroups > 0);
+  // 1. each group's shared prefix, all of its rows at once, on the tensor cores,
+  //    cut into key ranges so that the pass has about one CTA per SM -- or,
+  //    beside the task decode (which streams on the SMs the pass leaves free;
+  //    only its merge waits for the pass), about 7/16 of the SMs (prefix
+  //    sharing, 64 prompts x 4 samples: a 48.2 us step with 2 key ranges, 49.4
+  //    with 4, 50.1 with 1)
+  const long long base = (long long)num_groups * d->num_kv_heads * (((long long)max_group_size * G + 255) / 256);
+  const int sms = std::max(current_sm_count(), 1);
+  int kparts = (int)std::min<long long>(kMaxPrefixParts, std::max<long long>(1, (sms + base - 1) / base));
+  if (tasks) {
+    const long long want = (long long)sms * 7 / 16;
+    kparts = (int)std::min<long long>(kMaxPrefixParts, std::max<long long>(1, (want + base / 2) / base));
+  }
+  if (const char *env = getenv("PA_PREFIX_PARTS"))  // comparison: a fixed number of key ranges
+    kparts = std::max(1, std::min(kMaxPrefixParts, atoi(env)));
+  kparts = std::min(kparts, (max_prefix_len + 127) / 128);
+  const int kpart_len = ((max_prefix_len + kparts - 1) / kparts + 127) / 128 * 128;
+  kparts = (max_prefix_len + kpart_len - 1) / kpart_len;
   if (tasks || wide) {  // before the prefix pass: the second grid may start beside it
     st = decode_tasks_clear(d, ws + l.decode + l.pre_o + l.pre_ml, stream);
     if (st != PA_OK) return st;
