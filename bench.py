@@ -148,9 +148,9 @@ def kernel_traffic(kernel: str, workload: str):
 
 class ClockSampler:
     """nvidia-smi clock/throttle sampling in the background."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.limit")
 
     def __init__(self, index):
         self.index = index
@@ -202,9 +202,11 @@ class ClockSampler:
                 if v.strip().lower() == "active":
                     reasons.add(n)
         pw = [num(f[3]) for f in win if num(f[3]) is not None]
+        lim = [num(f[9]) for f in win if len(f) > 9 and num(f[9]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(win[0][2]),
                 "reasons": sorted(reasons), "samples": len(win), "window": label,
-                "power_w": statistics.median(pw) if pw else None}
+                "power_w": statistics.median(pw) if pw else None,
+                "power_limit_w": statistics.median(lim) if lim else None}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -735,6 +737,12 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
     x = {k: to_dev(v) for k, v in b.host_inputs.items()}
     stream = torch.cuda.current_stream()
     nev = 3 if b.kernel == "prefill_kernel" else 2
+    idle = None
+    if sampler and b.kernel == "mixed_kernel":  # the power drawn with nothing running, for the power bound
+        torch.cuda.synchronize()
+        t_i0 = time.time()
+        time.sleep(0.6)
+        idle = sampler.summary(t_i0, time.time())
 
     for i in range(args.warmup):
         b.step(i, x, None)
@@ -742,6 +750,7 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
     if world > 1:
         torch.distributed.barrier()
     side = {}
+    per, per_clk = {}, {}  # per-kernel launch time and clocks (graph mode)
     if args.eager:
         # every launch from the host, an event pair around each timed kernel
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
@@ -792,14 +801,17 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
         torch.cuda.synchronize()
         t_wall1 = time.time()
         ms = e0.elapsed_time(e1)
-        per = {}
         for name, g in g_kern:
             k0, k1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            kw0 = time.time()
             k0.record(stream)
             g.replay()
             k1.record(stream)
             torch.cuda.synchronize()
             per[name] = k0.elapsed_time(k1) / args.steps
+            if sampler:  # (the first third of the window: the board's draw still settling)
+                kw1 = time.time()
+                per_clk[name] = sampler.summary(kw0 + (kw1 - kw0) / 3, kw1)
         k_mean, k_median = per[b.kernel], None  # one event pair around K launches: a mean, no median
         if "decode_kernel" in per and b.kernel != "decode_kernel":
             side["decode_launch_ms_mean"] = per["decode_kernel"]
@@ -874,6 +886,23 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
         lower = max(b.extra["prefill_flops"] / (peaks["bf16_sustained"] * 1e12),
                     b.kernel_work / (peaks["hbm"] * 1e9)) * 1e3
         res["roofline"]["lower_bound_ms"] = round(lower, 4)
+        # The step under the board power limit: the energy the two halves draw
+        # above idle when each runs alone back to back, spent at the limit's
+        # headroom above idle.  An estimate, not a bound: energy per unit of
+        # work falls somewhat with the clock a capped GPU settles at.
+        clk_p, clk_d = per_clk.get("prefill_kernel"), per_clk.get("decode_kernel")
+        if idle and clk_p and clk_d and all(c.get("power_w") for c in (idle, clk_p, clk_d)) \
+                and clk_p.get("power_limit_w"):
+            p0, lim = idle["power_w"], clk_p["power_limit_w"]
+            e_dyn = (clk_p["power_w"] - p0) * per["prefill_kernel"] + (clk_d["power_w"] - p0) * per["decode_kernel"]
+            t_pow = e_dyn / (lim - p0)
+            res["roofline"]["power_estimate"] = {
+                "ms": round(t_pow, 4), "frac": round(t_pow / k_mean, 4), "idle_w": p0, "limit_w": lim,
+                "prefill_alone": {"ms": round(per["prefill_kernel"], 4), "power_w": clk_p["power_w"],
+                                  "sm_mhz": clk_p["sm_mhz"], "reasons": clk_p["reasons"]},
+                "decode_alone": {"ms": round(per["decode_kernel"], 4), "power_w": clk_d["power_w"],
+                                 "sm_mhz": clk_d["sm_mhz"], "reasons": clk_d["reasons"]},
+                "mixed": per_clk.get("mixed_kernel")}
     res.update(side)
     if b.extra:
         res["workload_extra"] = b.extra

@@ -118,6 +118,162 @@ struct Task {
   int bad;     // the unit is invalid: its rows are zeroed
 };
 
+// The plan of a launch in shared memory (every CTA builds the same one).
+struct TaskPlan {
+  int *sg_base;    // [kTaskMaxSub + 1] first task of each sub-group
+  int *sg_s0;      // [kTaskMaxSub + 1] first sequence of each sub-group
+  int *sg_pages;   // [kTaskMaxSub] pages past the group prefix (-1: invalid)
+  int *sg_kstart;  // [kTaskMaxSub] the group prefix (first key of the unit)
+  int *sg_kshared; // [kTaskMaxSub] keys every member shares
+  int *wsum;       // [warps] scan scratch
+  int *ctx_s;      // [kStageSeqs] staged contexts
+  int *gstart_s;   // [kStageGroups + 1] staged group starts
+  int *gprefix_s;  // [kStageGroups] staged group prefixes
+  bool staged;     // the contexts and groups fit the staging arrays
+};
+
+// Builds the plan on all NTH threads of the CTA: each sub-group's data, tasks
+// per sub-group (one per part and kv head) and their prefix sums.  Its inputs
+// are read in one round of independent loads, into shared memory when they
+// fit.  The caller synchronises the CTA before reading it.
+template <int B, int NTH>
+__device__ __forceinline__ void build_task_plan(const TaskArgs &a, const TaskPlan &p) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (p.staged) {
+    for (int i = tid; i < a.S; i += NTH) p.ctx_s[i] = __ldg(a.ctx + i);
+    for (int i = tid; i < a.ngroups; i += NTH) {
+      p.gstart_s[i] = __ldg(a.grp_start + i);
+      p.gprefix_s[i] = __ldg(a.grp_prefix + i);
+    }
+    if (tid == 0 && a.ngroups > 0) p.gstart_s[a.ngroups] = __ldg(a.grp_start + a.ngroups);
+  }
+  for (int sg = tid; sg <= a.nsg; sg += NTH) {
+    p.sg_s0[sg] = a.sub_start ? __ldg(a.sub_start + sg) : sg;
+    if (sg < a.nsg) p.sg_kshared[sg] = a.sub_start ? __ldg(a.sub_shared + sg) : -1;
+  }
+  __syncthreads();
+  const UnitShape us{a.S, a.G, a.rows, a.max_blocks, a.max_ctx, a.ngroups};
+  for (int sg = tid; sg < a.nsg; sg += NTH) {
+    int ks, n;
+    if (p.staged)
+      subgroup_plan(
+          us, B, p.sg_s0[sg], p.sg_s0[sg + 1], p.sg_kshared[sg], [&](int i) { return p.ctx_s[i]; },
+          [&](int i) { return p.gstart_s[i]; }, [&](int i) { return p.gprefix_s[i]; }, &ks, &n);
+    else
+      subgroup_plan(
+          us, B, p.sg_s0[sg], p.sg_s0[sg + 1], p.sg_kshared[sg], [&](int i) { return __ldg(a.ctx + i); },
+          [&](int i) { return __ldg(a.grp_start + i); }, [&](int i) { return __ldg(a.grp_prefix + i); }, &ks, &n);
+    if (p.sg_kshared[sg] < 0) p.sg_kshared[sg] = ks;
+    p.sg_kstart[sg] = ks;
+    p.sg_pages[sg] = n;
+    p.sg_base[sg + 1] =
+        a.Hkv * (n < 0 ? 1 : (n + part_len(n, a.part_pages) - 1) / part_len(n, a.part_pages) + (n == 0));
+  }
+  __syncthreads();
+  constexpr int kPer = (kTaskMaxSub + NTH - 1) / NTH;
+  int c[kPer], sum = 0;
+  const int lo = tid * kPer;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    c[k] = lo + k < a.nsg ? p.sg_base[lo + k + 1] : 0;
+    sum += c[k];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) p.wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - sum;
+  for (int w = 0; w < warp; ++w) run += p.wsum[w];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    run += c[k];
+    if (lo + k < a.nsg) p.sg_base[lo + k + 1] = run;
+  }
+  if (tid == 0) p.sg_base[0] = 0;
+}
+
+// Task t -> its description, on a whole warp; lane j < np holds page j of
+// the part: its table entry (CHECK: validated here, -1 if bad; else raw, to
+// be checked where it is used, so that the load is waited for only then),
+// first token, owner member (-1: shared) and the context that bounds its
+// keys.  Also warms L2 with the unit's query rows.
+template <int B, bool CHECK>
+__device__ __forceinline__ void describe_task(const TaskArgs &a, const TaskPlan &p, int total, int t, Task &T,
+                                              int &e_pg, int &e_tok, int &e_own, int &e_octx) {
+  const int lane = threadIdx.x & 31;
+  T.t = t;
+  T.np = 0;
+  T.bad = 0;
+  e_pg = -1;
+  e_tok = 0;
+  e_own = -1;
+  e_octx = 0;
+  if (t >= total) return;
+  int lo = 0, hi = a.nsg;  // sg_base[lo] <= t < sg_base[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.sg_base[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int sg = lo;
+  T.nparts = (p.sg_base[sg + 1] - p.sg_base[sg]) / a.Hkv;
+  const int rem = t - p.sg_base[sg];
+  T.kvh = rem / T.nparts;
+  T.part = rem - T.kvh * T.nparts;
+  const int n = p.sg_pages[sg];
+  T.kstart = p.sg_kstart[sg];
+  T.s0 = p.sg_s0[sg];
+  T.nm = p.sg_s0[sg + 1] - T.s0;
+  if (n < 0) {
+    T.bad = 1;
+    return;
+  }
+  const int kshared = p.sg_kshared[sg];
+  const int plen = part_len(n, a.part_pages);
+  const int p0 = T.part * plen;
+  T.np = max(0, min(n, p0 + plen) - p0);
+  // members' contexts and the end of each member's own pages (after the shared ones)
+  const int c = lane < T.nm ? (p.staged ? p.ctx_s[T.s0 + lane] : __ldg(a.ctx + T.s0 + lane)) : 0;
+  const int own = lane < T.nm ? (c + B - 1) / B - kshared / B : 0;
+  int incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int shared_pages = (kshared - T.kstart) / B;
+  const int i = p0 + lane;
+  int m = -1, lb = T.kstart / B + i;
+  for (int mm = 0; mm < T.nm; ++mm) {
+    const int e = __shfl_sync(0xffffffffu, incl, mm), o = __shfl_sync(0xffffffffu, own, mm);
+    if (i >= shared_pages && m < 0 && i < shared_pages + e) {
+      m = mm;
+      lb = kshared / B + (i - (shared_pages + e - o));
+    }
+  }
+  const int cm = __shfl_sync(0xffffffffu, c, max(m, 0));
+  if (lane < T.np) {
+    int pg = __ldg(a.bt + (size_t)(T.s0 + max(m, 0)) * a.max_blocks + lb);
+    if (CHECK && (pg < 0 || pg >= a.num_blocks)) {
+      if (a.err) atomicOr(a.err, PA_DEVERR_PAGE);
+      pg = -1;
+    }
+    e_pg = pg;
+    e_tok = lb * B;
+    e_own = m;
+    e_octx = m >= 0 ? cm : kshared;
+  }
+  for (int g = lane; g < T.nm * a.G; g += 32) {
+    const __nv_bfloat16 *qr = a.q + ((size_t)(T.s0 + g / a.G) * a.Hq + (size_t)T.kvh * a.G + g % a.G) * kTD;
+    prefetch_l2(qr);
+    prefetch_l2(qr + 64);
+  }
+}
+
 template <int B, int NT, int W, int NST>
 __global__ void __launch_bounds__(W * 32, 1)
     decode_tasks_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -147,66 +303,10 @@ __global__ void __launch_bounds__(W * 32, 1)
   unsigned int first = 0;
   if (lane == 0) first = atomicAdd(a.ws_ctr, 1u);
 
-  // ---- plan (every CTA the same): each sub-group's data, tasks per
-  // sub-group (one per part and kv head), their prefix sums.  Its inputs are
-  // read in one round of independent loads, into shared memory when they fit.
-  const bool staged = a.S <= kStageSeqs && a.ngroups <= kStageGroups;
-  if (staged) {
-    for (int i = tid; i < a.S; i += NTH) ctx_s[i] = __ldg(a.ctx + i);
-    for (int i = tid; i < a.ngroups; i += NTH) {
-      gstart_s[i] = __ldg(a.grp_start + i);
-      gprefix_s[i] = __ldg(a.grp_prefix + i);
-    }
-    if (tid == 0 && a.ngroups > 0) gstart_s[a.ngroups] = __ldg(a.grp_start + a.ngroups);
-  }
-  for (int sg = tid; sg <= a.nsg; sg += NTH) {
-    sg_s0[sg] = a.sub_start ? __ldg(a.sub_start + sg) : sg;
-    if (sg < a.nsg) sg_kshared[sg] = a.sub_start ? __ldg(a.sub_shared + sg) : -1;
-  }
-  __syncthreads();
-  const UnitShape us{a.S, a.G, a.rows, a.max_blocks, a.max_ctx, a.ngroups};
-  for (int sg = tid; sg < a.nsg; sg += NTH) {
-    int ks, n;
-    if (staged)
-      subgroup_plan(
-          us, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return ctx_s[i]; },
-          [&](int i) { return gstart_s[i]; }, [&](int i) { return gprefix_s[i]; }, &ks, &n);
-    else
-      subgroup_plan(
-          us, B, sg_s0[sg], sg_s0[sg + 1], sg_kshared[sg], [&](int i) { return __ldg(a.ctx + i); },
-          [&](int i) { return __ldg(a.grp_start + i); }, [&](int i) { return __ldg(a.grp_prefix + i); }, &ks, &n);
-    if (sg_kshared[sg] < 0) sg_kshared[sg] = ks;
-    sg_kstart[sg] = ks;
-    sg_pages[sg] = n;
-    sg_base[sg + 1] = a.Hkv * (n < 0 ? 1 : (n + part_len(n, a.part_pages) - 1) / part_len(n, a.part_pages) + (n == 0));
-  }
-  __syncthreads();
-  {
-    constexpr int kPer = (kTaskMaxSub + NTH - 1) / NTH;
-    int c[kPer], sum = 0;
-    const int lo = tid * kPer;
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      c[k] = lo + k < a.nsg ? sg_base[lo + k + 1] : 0;
-      sum += c[k];
-    }
-    int incl = sum;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    int run = incl - sum;
-    for (int w = 0; w < warp; ++w) run += wsum[w];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      run += c[k];
-      if (lo + k < a.nsg) sg_base[lo + k + 1] = run;
-    }
-    if (tid == 0) sg_base[0] = 0;
-  }
+  // ---- plan (every CTA the same)
+  const TaskPlan plan{sg_base, sg_s0, sg_pages, sg_kstart, sg_kshared, wsum, ctx_s, gstart_s, gprefix_s,
+                      a.S <= kStageSeqs && a.ngroups <= kStageGroups};
+  build_task_plan<B, NTH>(a, plan);
   uint64_t *bars = bars_all + warp * NST;
   if (lane == 0) {
     for (int i = 0; i < NST; ++i) mbar_init(&bars[i], 1);
@@ -219,78 +319,8 @@ __global__ void __launch_bounds__(W * 32, 1)
   uint8_t *ring = smem + warp * NST * L::kSlotBytes;
   const uint64_t pol = policy_evict_first();
 
-  // task t -> its description; lane j < np holds page j of the part: page id
-  // (-1: none / bad), first token, owner member (-1: shared) and the context
-  // that bounds its keys
   auto describe = [&](int t, Task &T, int &e_pg, int &e_tok, int &e_own, int &e_octx) {
-    T.t = t;
-    T.np = 0;
-    T.bad = 0;
-    e_pg = -1;
-    e_tok = 0;
-    e_own = -1;
-    e_octx = 0;
-    if (t >= total) return;
-    int lo = 0, hi = a.nsg;  // sg_base[lo] <= t < sg_base[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sg_base[mid] <= t) lo = mid;
-      else hi = mid;
-    }
-    const int sg = lo;
-    T.nparts = (sg_base[sg + 1] - sg_base[sg]) / a.Hkv;
-    const int rem = t - sg_base[sg];
-    T.kvh = rem / T.nparts;
-    T.part = rem - T.kvh * T.nparts;
-    const int n = sg_pages[sg];
-    T.kstart = sg_kstart[sg];
-    T.s0 = sg_s0[sg];
-    T.nm = sg_s0[sg + 1] - T.s0;
-    if (n < 0) {
-      T.bad = 1;
-      return;
-    }
-    const int kshared = sg_kshared[sg];
-    const int plen = part_len(n, a.part_pages);
-    const int p0 = T.part * plen;
-    T.np = max(0, min(n, p0 + plen) - p0);
-    // members' contexts and the end of each member's own pages (after the shared ones)
-    const int c = lane < T.nm ? __ldg(a.ctx + T.s0 + lane) : 0;
-    const int own = lane < T.nm ? (c + B - 1) / B - kshared / B : 0;
-    int incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    const int shared_pages = (kshared - T.kstart) / B;
-    const int i = p0 + lane;
-    int m = -1, lb = T.kstart / B + i;
-    for (int mm = 0; mm < T.nm; ++mm) {
-      const int e = __shfl_sync(0xffffffffu, incl, mm), o = __shfl_sync(0xffffffffu, own, mm);
-      if (i >= shared_pages && m < 0 && i < shared_pages + e) {
-        m = mm;
-        lb = kshared / B + (i - (shared_pages + e - o));
-      }
-    }
-    const int cm = __shfl_sync(0xffffffffu, c, max(m, 0));
-    if (lane < T.np) {
-      int pg = __ldg(a.bt + (size_t)(T.s0 + max(m, 0)) * a.max_blocks + lb);
-      if (pg < 0 || pg >= a.num_blocks) {
-        if (a.err) atomicOr(a.err, PA_DEVERR_PAGE);
-        pg = -1;
-      }
-      e_pg = pg;
-      e_tok = lb * B;
-      e_own = m;
-      e_octx = m >= 0 ? cm : kshared;
-    }
-    // warm L2 with the rows' queries
-    for (int g = lane; g < T.nm * G; g += 32) {
-      const __nv_bfloat16 *qr = a.q + ((size_t)(T.s0 + g / G) * a.Hq + (size_t)T.kvh * G + g % G) * kTD;
-      prefetch_l2(qr);
-      prefetch_l2(qr + 64);
-    }
+    describe_task<B, true>(a, plan, total, t, T, e_pg, e_tok, e_own, e_octx);
   };
   auto fetch = [&]() -> int {
     int t = 0;
