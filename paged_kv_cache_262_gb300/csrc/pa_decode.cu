@@ -66,17 +66,18 @@ __global__ void __launch_bounds__(NW * 32)
   decode_unit<D, B, NT, NW, NST, PRE, APP, GRP>(&tmK, &tmV, a, lin, threadIdx.x, smem, 0);
 }
 
-template <int D, int B, int NT, bool PRE, bool APP, bool GRP = false>
+template <int D, int B, int NT, bool PRE, bool APP, bool GRP = false, int NST16 = 3>
 int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a, dim3 grid,
                   cudaStream_t st) {
-  // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM); 32-token pages:
-  // 1 slot a warp (64 KB, 3 CTAs per SM) -- with 2 slots a CTA would hold
-  // 128 KB and one CTA per SM could not hide its own set-up and merge.  The
-  // shared-prefix launch, whose own key ranges are typically short, takes 2
-  // slots with 16-token pages (64 KB, 3 CTAs per SM): more CTAs in flight
-  // hide the set-up of short units (prefix sharing: 72.6 -> 61.1 us).
+  // 16-token pages: 3 slots a warp (96 KB, 2 CTAs per SM), or NST16 = 2 (64
+  // KB, 3 CTAs per SM) when the caller asks; 32-token pages: 1 slot a warp
+  // (64 KB, 3 CTAs per SM) -- with 2 slots a CTA would hold 128 KB and one
+  // CTA per SM could not hide its own set-up and merge.  The shared-prefix
+  // launch, whose own key ranges are typically short, takes 2 slots with
+  // 16-token pages: more CTAs in flight hide the set-up of short units
+  // (prefix sharing: 72.6 -> 61.1 us).
   constexpr int NW = 4;
-  constexpr int NST = (B == 16) ? (PRE || GRP ? 2 : 3) : 1;
+  constexpr int NST = (B == 16) ? (PRE || GRP ? 2 : NST16) : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
   auto kern = decode_kernel<D, B, NT, NW, NST, PRE, APP, GRP>;
@@ -99,6 +100,14 @@ int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const Decod
   if (a.ngroups > 0)
     return G <= 8 ? launch_decode<D, B, 1, true, false>(tk, tv, a, grid, st)
                   : launch_decode<D, B, 2, true, false>(tk, tv, a, grid, st);
+  // A launch whose units all fit one wave at 2 CTAs per SM takes 2 slots a
+  // warp (32K contexts, 256 units of 512 pages: 165.1 -> 160.1 us); more
+  // units keep 3 (Llama-3-8B-shaped decode, 512 units: 51.2 us, 53.3 with 2).
+  const bool one_wave = (long long)grid.x * grid.y * grid.z <= 2ll * current_sm_count();
+  if (B == 16 && G <= 8 && one_wave) {
+    if (a.app_slots) return launch_decode<D, B, 1, false, true, false, 2>(tk, tv, a, grid, st);
+    return launch_decode<D, B, 1, false, false, false, 2>(tk, tv, a, grid, st);
+  }
   if (a.app_slots)
     return G <= 8 ? launch_decode<D, B, 1, false, true>(tk, tv, a, grid, st)
                   : launch_decode<D, B, 2, false, true>(tk, tv, a, grid, st);
