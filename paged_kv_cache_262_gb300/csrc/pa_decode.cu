@@ -77,7 +77,7 @@ int launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs
   // 16-token pages: more CTAs in flight hide the set-up of short units
   // (prefix sharing: 72.6 -> 61.1 us).
   constexpr int NW = 4;
-  constexpr int NST = (B == 16) ? (PRE || GRP ? 2 : NST16) : 1;
+  constexpr int NST = (B == 16) ? (PRE ? 2 : NST16) : 1;
   using L = DecodeSmem<D, B, NW, NST>;
   static_assert(L::kAlloc <= 227 * 1024, "decode shared memory over the per-CTA limit");
   auto kern = decode_kernel<D, B, NT, NW, NST, PRE, APP, GRP>;
@@ -93,17 +93,22 @@ int dispatch_nt(int G, const CUtensorMap &tk, const CUtensorMap &tv, const Decod
   // Separate instances keep the plain decode's registers: the shared-prefix
   // launch (prefix states prefetched), the sub-group launch and the decode
   // with append.
+  // A launch whose units all fit one wave at 2 CTAs per SM takes 2 slots a
+  // warp (32K contexts, 256 units of 512 pages: 165.1 -> 160.1 us); more
+  // units keep 3 (Llama-3-8B-shaped decode, 512 units: 51.2 us, 53.3 with 2;
+  // parallel sampling, 512 sub-group units: 120.7 us, 124.6 with 2).
+  const bool one_wave = (long long)grid.x * grid.y * grid.z <= 2ll * current_sm_count();
   if constexpr (D == 128)
-    if (a.nsub > 0)
+    if (a.nsub > 0) {
+      if (B == 16 && one_wave)
+        return a.sub_rows <= 8 ? launch_decode<D, B, 1, false, false, true, 2>(tk, tv, a, grid, st)
+                               : launch_decode<D, B, 2, false, false, true, 2>(tk, tv, a, grid, st);
       return a.sub_rows <= 8 ? launch_decode<D, B, 1, false, false, true>(tk, tv, a, grid, st)
                              : launch_decode<D, B, 2, false, false, true>(tk, tv, a, grid, st);
+    }
   if (a.ngroups > 0)
     return G <= 8 ? launch_decode<D, B, 1, true, false>(tk, tv, a, grid, st)
                   : launch_decode<D, B, 2, true, false>(tk, tv, a, grid, st);
-  // A launch whose units all fit one wave at 2 CTAs per SM takes 2 slots a
-  // warp (32K contexts, 256 units of 512 pages: 165.1 -> 160.1 us); more
-  // units keep 3 (Llama-3-8B-shaped decode, 512 units: 51.2 us, 53.3 with 2).
-  const bool one_wave = (long long)grid.x * grid.y * grid.z <= 2ll * current_sm_count();
   if (B == 16 && G <= 8 && one_wave) {
     if (a.app_slots) return launch_decode<D, B, 1, false, true, false, 2>(tk, tv, a, grid, st);
     return launch_decode<D, B, 1, false, false, false, 2>(tk, tv, a, grid, st);
