@@ -690,6 +690,45 @@ def hbm_probe(torch, pa, dev):
             "gather_gbs": round(gather, 1), "copy_gbs": round(copy, 1)}
 
 
+def tensor_probe(torch, dev, sampler):
+    """This GPU's dense bf16 tensor rate from cuBLAS (torch.matmul, 8192^3,
+    fp32 accumulate): best of 10 single GEMMs (burst), and GEMMs back to back
+    for about 1.5 s under the board's power limit (sustained), with the clocks
+    and power sampled over the sustained loop."""
+    n = 8192
+    a = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+    b = torch.randn((n, n), device=dev, dtype=torch.bfloat16)
+    c = torch.empty((n, n), device=dev, dtype=torch.bfloat16)
+    flop = 2.0 * n * n * n
+    stream = torch.cuda.current_stream()
+    for _ in range(5):
+        torch.matmul(a, b, out=c)
+    torch.cuda.synchronize()
+    burst = 0.0
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        torch.matmul(a, b, out=c)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        burst = max(burst, flop / (e0.elapsed_time(e1) / 1e3) / 1e12)
+    reps = max(1, int(1.5 / (flop / (burst * 1e12))))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(reps):
+        torch.matmul(a, b, out=c)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    sustained = flop * reps / (e0.elapsed_time(e1) / 1e3) / 1e12
+    clk = sampler.summary(t0 + (t1 - t0) / 3, t1) if sampler else None
+    del a, b, c
+    torch.cuda.empty_cache()
+    return {"burst_tflops": round(burst, 1), "sustained_tflops": round(sustained, 1), "gemm": f"bf16 {n}^3, cuBLAS",
+            "sustained_reps": reps, "clocks": clk}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import paged_kv_cache_262_gb300 as pa
@@ -704,6 +743,8 @@ def run_ours(args, rank, world, local_rank):
         sampler.start()
         time.sleep(0.3)
     probe = None if args.no_probe else hbm_probe(torch, pa, dev)
+    if probe is not None and args.workload == "mixed_step":  # the tensor side's own ceiling, this run
+        probe["tensor"] = tensor_probe(torch, dev, sampler)
     b = build(args, torch, pa, dev)
     res = measure(args, b, torch, dev, world, rank, sampler, probe)
     long_ctx = None
@@ -818,6 +859,9 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
         if "prefill_kernel" in per and b.kernel != "prefill_kernel":
             side["prefill_launch_ms_mean"] = per["prefill_kernel"]
             side["prefill_tflops"] = round(b.extra["prefill_flops"] / (per["prefill_kernel"] / 1e3) / 1e12, 1)
+            if probe and probe.get("tensor"):  # the prefill alone against this run's sustained cuBLAS rate
+                side["prefill_frac_of_probe_sustained"] = round(
+                    side["prefill_tflops"] / probe["tensor"]["sustained_tflops"], 4)
         timing = (f"CUDA graph of the {args.steps} steps; per-kernel launch time from a graph of the kernel's "
                   f"{args.steps} launches alone (a mean)")
     if "decode_launch_ms_mean" in side:
@@ -879,10 +923,16 @@ def measure(args, b, torch, dev, world, rank, sampler, probe):
         "clocks": clocks,
         "timing": timing,
     }
+    tp = (probe or {}).get("tensor")
+    if tp and b.bound == "tensor":  # the prefill against this run's cuBLAS rate too
+        res["roofline"]["tensor_probe"] = dict(tp, frac_sustained=round(achieved / tp["sustained_tflops"], 4),
+                                               frac_burst=round(achieved / tp["burst_tflops"], 4))
     if b.kernel == "mixed_kernel":  # one launch doing both: the prefill's tensor work in the same time
         tf = b.extra["prefill_flops"] / (k_mean / 1e3) / 1e12
         res["roofline"]["tensor"] = {"achieved": round(tf, 1), "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                                      "frac": round(tf / peaks["bf16_sustained"], 4)}
+        if tp:
+            res["roofline"]["tensor"]["probe"] = dict(tp, frac_sustained=round(tf / tp["sustained_tflops"], 4))
         lower = max(b.extra["prefill_flops"] / (peaks["bf16_sustained"] * 1e12),
                     b.kernel_work / (peaks["hbm"] * 1e9)) * 1e3
         res["roofline"]["lower_bound_ms"] = round(lower, 4)
