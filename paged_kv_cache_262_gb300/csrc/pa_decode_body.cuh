@@ -465,10 +465,16 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
         }
       }
 
-      // online softmax: mask tokens past the context, page max, rescale
+      // online softmax: mask tokens past the context, page max.  The running
+      // maximum moves only when a column's page maximum passes it by more
+      // than kSlack (a factor 2^kSlack): the probabilities are taken against
+      // it while the page maxima are still being reduced, and the rescale of
+      // the column's state is rare.
+      constexpr float kSlack = 8.f;
+      float t[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float t0 = -INFINITY, t1 = -INFINITY;
+        t[nt][0] = t[nt][1] = -INFINITY;
         // GRP: a member's own page counts only for its columns
         const bool own0 = !GRP || owner < 0 || (nt * 8 + 2 * (lane & 3)) / G == owner;
         const bool own1 = !GRP || owner < 0 || (nt * 8 + 2 * (lane & 3) + 1) / G == owner;
@@ -480,30 +486,55 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
           sc[mt][nt][1] = v0 && own1 ? sc[mt][nt][1] * a.scale_log2 : -INFINITY;
           sc[mt][nt][2] = v1 && own0 ? sc[mt][nt][2] * a.scale_log2 : -INFINITY;
           sc[mt][nt][3] = v1 && own1 ? sc[mt][nt][3] * a.scale_log2 : -INFINITY;
-          t0 = fmaxf(t0, fmaxf(sc[mt][nt][0], sc[mt][nt][2]));
-          t1 = fmaxf(t1, fmaxf(sc[mt][nt][1], sc[mt][nt][3]));
+          t[nt][0] = fmaxf(t[nt][0], fmaxf(sc[mt][nt][0], sc[mt][nt][2]));
+          t[nt][1] = fmaxf(t[nt][1], fmaxf(sc[mt][nt][1], sc[mt][nt][3]));
         }
+      }
+      // P (bf16 pairs) against the running maxima; a column that has seen no
+      // key yet (maximum -inf) takes 0, so that no -inf - -inf appears
+      uint32_t plo[MT][NT], phi[MT][NT];
+      auto probabilities = [&]() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float e0 = m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
+          const float e1 = m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            plo[mt][nt] = pack_bf16(exp2f(sc[mt][nt][0] - e0), exp2f(sc[mt][nt][1] - e1));
+            phi[mt][nt] = pack_bf16(exp2f(sc[mt][nt][2] - e0), exp2f(sc[mt][nt][3] - e1));
+          }
+        }
+      };
+      probabilities();
+      bool grow = false;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
-          t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-          t1 = fmaxf(t1, __shfl_xor_sync(0xffffffffu, t1, off));
+          t[nt][0] = fmaxf(t[nt][0], __shfl_xor_sync(0xffffffffu, t[nt][0], off));
+          t[nt][1] = fmaxf(t[nt][1], __shfl_xor_sync(0xffffffffu, t[nt][1], off));
         }
-        const float mn0 = fmaxf(m_run[nt][0], t0), mn1 = fmaxf(m_run[nt][1], t1);
-        // GRP: a column may have seen only other members' pages so far (max
-        // still -inf): rescale against 0 there, so no -inf - -inf appears
-        const float su0 = GRP && mn0 == -INFINITY ? 0.f : mn0, su1 = GRP && mn1 == -INFINITY ? 0.f : mn1;
-        const float al0 = exp2f(m_run[nt][0] - su0), al1 = exp2f(m_run[nt][1] - su1);
-        m_run[nt][0] = mn0;
-        m_run[nt][1] = mn1;
-        l_run[nt][0] *= al0;
-        l_run[nt][1] *= al1;
+        grow |= t[nt][0] > m_run[nt][0] + kSlack || t[nt][1] > m_run[nt][1] + kSlack;
+      }
+      if (__any_sync(0xffffffffu, grow)) {  // new maxima: rescale the state, retake P
 #pragma unroll
-        for (int dt = 0; dt < DT; ++dt) {
-          o[nt][dt][0] *= al0;
-          o[nt][dt][1] *= al1;
-          o[nt][dt][2] *= al0;
-          o[nt][dt][3] *= al1;
+        for (int nt = 0; nt < NT; ++nt) {
+          const float mn0 = fmaxf(m_run[nt][0], t[nt][0]), mn1 = fmaxf(m_run[nt][1], t[nt][1]);
+          const float su0 = mn0 == -INFINITY ? 0.f : mn0, su1 = mn1 == -INFINITY ? 0.f : mn1;
+          const float al0 = exp2f(m_run[nt][0] - su0), al1 = exp2f(m_run[nt][1] - su1);
+          m_run[nt][0] = mn0;
+          m_run[nt][1] = mn1;
+          l_run[nt][0] *= al0;
+          l_run[nt][1] *= al1;
+#pragma unroll
+          for (int dt = 0; dt < DT; ++dt) {
+            o[nt][dt][0] *= al0;
+            o[nt][dt][1] *= al1;
+            o[nt][dt][2] *= al0;
+            o[nt][dt][3] *= al1;
+          }
         }
+        probabilities();
       }
 
       // Value rows past the context (the tail of the last page) may hold
@@ -527,14 +558,10 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const float e0 = GRP && m_run[nt][0] == -INFINITY ? 0.f : m_run[nt][0];
-          const float e1 = GRP && m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
-          const uint32_t lo = pack_bf16(exp2f(sc[mt][nt][0] - e0), exp2f(sc[mt][nt][1] - e1));
-          const uint32_t hi = pack_bf16(exp2f(sc[mt][nt][2] - e0), exp2f(sc[mt][nt][3] - e1));
-          l_run[nt][0] += bf16_lo(lo) + bf16_lo(hi);
-          l_run[nt][1] += bf16_hi(lo) + bf16_hi(hi);
-          pb[nt][0] = movmatrix_t(lo);
-          pb[nt][1] = movmatrix_t(hi);
+          l_run[nt][0] += bf16_lo(plo[mt][nt]) + bf16_lo(phi[mt][nt]);
+          l_run[nt][1] += bf16_hi(plo[mt][nt]) + bf16_hi(phi[mt][nt]);
+          pb[nt][0] = movmatrix_t(plo[mt][nt]);
+          pb[nt][1] = movmatrix_t(phi[mt][nt]);
         }
 #pragma unroll
         for (int dt = 0; dt < DT; ++dt) {
