@@ -500,8 +500,8 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
           const float e1 = m_run[nt][1] == -INFINITY ? 0.f : m_run[nt][1];
 #pragma unroll
           for (int mt = 0; mt < MT; ++mt) {
-            plo[mt][nt] = pack_bf16(exp2f(sc[mt][nt][0] - e0), exp2f(sc[mt][nt][1] - e1));
-            phi[mt][nt] = pack_bf16(exp2f(sc[mt][nt][2] - e0), exp2f(sc[mt][nt][3] - e1));
+            plo[mt][nt] = pack_bf16(ex2_ftz(sc[mt][nt][0] - e0), ex2_ftz(sc[mt][nt][1] - e1));
+            phi[mt][nt] = pack_bf16(ex2_ftz(sc[mt][nt][2] - e0), ex2_ftz(sc[mt][nt][3] - e1));
           }
         }
       };
