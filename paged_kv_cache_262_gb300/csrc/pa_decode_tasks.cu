@@ -139,17 +139,45 @@ struct TaskPlan {
 template <int B, int NTH>
 __device__ __forceinline__ void build_task_plan(const TaskArgs &a, const TaskPlan &p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // every input load is issued before the first store waits for one: a
+  // single round trip
+  constexpr int kC = (kStageSeqs + NTH - 1) / NTH, kG = (kStageGroups + NTH) / NTH, kS = (kTaskMaxSub + NTH) / NTH;
+  int vc[kC], vgs[kG], vgp[kG], vs0[kS], vsh[kS];
   if (p.staged) {
-    for (int i = tid; i < a.S; i += NTH) p.ctx_s[i] = __ldg(a.ctx + i);
-    for (int i = tid; i < a.ngroups; i += NTH) {
-      p.gstart_s[i] = __ldg(a.grp_start + i);
-      p.gprefix_s[i] = __ldg(a.grp_prefix + i);
+#pragma unroll
+    for (int k = 0; k < kC; ++k) {
+      const int i = tid + k * NTH;
+      vc[k] = i < a.S ? __ldg(a.ctx + i) : 0;
     }
-    if (tid == 0 && a.ngroups > 0) p.gstart_s[a.ngroups] = __ldg(a.grp_start + a.ngroups);
+#pragma unroll
+    for (int k = 0; k < kG; ++k) {
+      const int i = tid + k * NTH;
+      vgs[k] = i <= a.ngroups && a.ngroups > 0 ? __ldg(a.grp_start + i) : 0;
+      vgp[k] = i < a.ngroups ? __ldg(a.grp_prefix + i) : 0;
+    }
   }
-  for (int sg = tid; sg <= a.nsg; sg += NTH) {
-    p.sg_s0[sg] = a.sub_start ? __ldg(a.sub_start + sg) : sg;
-    if (sg < a.nsg) p.sg_kshared[sg] = a.sub_start ? __ldg(a.sub_shared + sg) : -1;
+#pragma unroll
+  for (int k = 0; k < kS; ++k) {
+    const int sg = tid + k * NTH;
+    vs0[k] = sg <= a.nsg ? (a.sub_start ? __ldg(a.sub_start + sg) : sg) : 0;
+    vsh[k] = sg < a.nsg ? (a.sub_start ? __ldg(a.sub_shared + sg) : -1) : 0;
+  }
+  if (p.staged) {
+#pragma unroll
+    for (int k = 0; k < kC; ++k)
+      if (tid + k * NTH < a.S) p.ctx_s[tid + k * NTH] = vc[k];
+#pragma unroll
+    for (int k = 0; k < kG; ++k) {
+      const int i = tid + k * NTH;
+      if (i <= a.ngroups && a.ngroups > 0) p.gstart_s[i] = vgs[k];
+      if (i < a.ngroups) p.gprefix_s[i] = vgp[k];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kS; ++k) {
+    const int sg = tid + k * NTH;
+    if (sg <= a.nsg) p.sg_s0[sg] = vs0[k];
+    if (sg < a.nsg) p.sg_kshared[sg] = vsh[k];
   }
   __syncthreads();
   const UnitShape us{a.S, a.G, a.rows, a.max_blocks, a.max_ctx, a.ngroups};
@@ -339,14 +367,24 @@ __global__ void __launch_bounds__(W * 32, 1)
   nxt.np = 0;
   auto describe_next = [&]() {
     if (nxt_ready) return;
-    if (more) {
-      describe(fetch(), nxt, n_pg, n_tok, n_own, n_octx);
+    if (more) {  // (table entries checked where they are used: no wait here)
+      describe_task<B, false>(a, plan, total, fetch(), nxt, n_pg, n_tok, n_own, n_octx);
       more = nxt.t < total;
     } else {
       nxt.t = total;
       nxt.np = 0;
     }
     nxt_ready = true;
+  };
+
+  // a table entry of the next task, at its first use: -1 (and the error
+  // flag) if it is outside the pool
+  auto checked = [&](int pg, bool flag) {
+    if (pg < 0 || pg >= a.num_blocks) {
+      if (flag && a.err) atomicOr(a.err, PA_DEVERR_PAGE);
+      pg = -1;
+    }
+    return pg;
   };
 
   // ring positions: pages issued / consumed so far; the issue pointer is in
@@ -385,8 +423,52 @@ __global__ void __launch_bounds__(W * 32, 1)
         at = 0;
       }
       if (at >= nxt.np) return;
-      issue_one(__shfl_sync(0xffffffffu, n_pg, at), nxt.kvh);
+      issue_one(checked(__shfl_sync(0xffffffffu, n_pg, at), lane == 0), nxt.kvh);
       ++at;
+    }
+  };
+
+  // Q^T fragments (MMA B operand) of a task: query row 8nt + lane/4 of its
+  // unit, d pairs; loaded before the task's gathers are issued (which may
+  // wait for its table entries), so that the two round trips overlap.  A
+  // lane needs the bf16 pairs (words) c, c + 4, c + 8, ... of its two rows
+  // (c = lane % 4); it loads their 16-byte blocks c + 4m (m < 4) instead,
+  // a quarter of the load instructions, and the four lanes of a row trade
+  // words in one 4 x 4 transpose per m: rotate the block left by c, take
+  // word j from lane c - j, rotate back.
+  uint32_t qf[NT][KS][2];
+  static_assert(KS == 8, "a row is 16 blocks of 16 bytes");
+  auto load_q = [&](const Task &T) {
+    const int c = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = nt * 8 + (lane >> 2);
+      const bool ok = !T.bad && g < T.nm * G;
+      const uint4 *qr = reinterpret_cast<const uint4 *>(
+          a.q + ((size_t)(T.s0 + g / G) * a.Hq + (size_t)T.kvh * G + g % G) * kTD);
+      uint4 v[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) v[m] = ok ? __ldg(qr + c + 4 * m) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t r[4] = {v[m].x, v[m].y, v[m].z, v[m].w};  // words 4 (c + 4m) + k
+        uint32_t t[4], p[4], u[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) t[j] = (c & 1) ? r[(j + 1) & 3] : r[j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = (c & 2) ? t[(j + 2) & 3] : t[j];
+        u[0] = p[0];
+#pragma unroll
+        for (int j = 1; j < 4; ++j) u[j] = __shfl_sync(0xffffffffu, p[j], (lane & ~3) | ((c - j) & 3));
+        // u[j] = word 4 (((c - j) & 3) + 4m) + c; rotate (u0, u3, u2, u1) right by c
+        const uint32_t w[4] = {u[0], u[3], u[2], u[1]};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) t[j] = (c & 1) ? w[(j + 3) & 3] : w[j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = (c & 2) ? t[(j + 2) & 3] : t[j];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qf[nt][(4 * m + j) >> 1][(4 * m + j) & 1] = p[j];  // word 4 (4m + j) + c
+      }
     }
   };
 
@@ -396,25 +478,9 @@ __global__ void __launch_bounds__(W * 32, 1)
     auto row_of = [&](int g) -> size_t {
       return (size_t)(cur.s0 + g / G) * a.Hq + (size_t)cur.kvh * G + g % G;
     };
+    load_q(cur);
     if (cur.np == 0) describe_next();  // nothing of cur to overlap it with
     top_up();
-    // Q^T fragments (MMA B operand): query row 8nt + lane/4 of the unit, d pairs
-    uint32_t qf[NT][KS][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = nt * 8 + (lane >> 2);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int d0 = kk * 16 + 2 * (lane & 3);
-        if (!cur.bad && g < ncols) {
-          const __nv_bfloat16 *qg = a.q + row_of(g) * kTD;
-          qf[nt][kk][0] = __ldg(reinterpret_cast<const uint32_t *>(qg + d0));
-          qf[nt][kk][1] = __ldg(reinterpret_cast<const uint32_t *>(qg + d0 + 8));
-        } else {
-          qf[nt][kk][0] = qf[nt][kk][1] = 0u;
-        }
-      }
-    }
     float m_run[NT][2], l_run[NT][2], o[NT][DT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -609,7 +675,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     // ---- the next task becomes current
     describe_next();
     cur = nxt;
-    c_pg = n_pg;
+    c_pg = lane < nxt.np ? checked(n_pg, true) : n_pg;
     c_tok = n_tok;
     c_own = n_own;
     c_octx = n_octx;

@@ -93,6 +93,9 @@ int shared_prefix(const pa_decode_desc *d, const void *q, const void *k_pool, co
       max_subgroup_size < 0)
     return PA_ERR_INVALID;
   if (d->num_seqs == 0) return PA_OK;
+  if (!q || !k_pool || !v_pool || !out || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned16(out))
+    return PA_ERR_INVALID;
   const int G = d->num_q_heads / d->num_kv_heads;
   DecodePrefix sub{};  // the sub-group partition (the prefix states are filled in below)
   if (num_subgroups > 0) {

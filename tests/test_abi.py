@@ -121,6 +121,9 @@ def test_new_entry_points_validate_before_any_gpu_work(lib):
     assert call_sp2(d, 2, 16, 16, 5) == pa.PA_ERR_UNSUPPORTED   # 5 members x 4 heads > 16 query rows
     assert call_sp2(_desc(head_dim=64), 2, 16, 16, 2) == pa.PA_ERR_UNSUPPORTED
     assert call_sp2(_desc(num_seqs=0), 2, 16, 16, 4) == pa.PA_OK  # nothing to decode
+    for q, out in ((18, 16), (16, 24), (None, 16)):  # q and out: 16-byte aligned device pointers
+        assert sp2(ctypes.byref(d), q, 16, 16, 16, 16, 0, None, None, None, 0, 0, 0, 2, 16, 16, 4, out, 16, 1 << 20,
+                   None, None) == pa.PA_ERR_INVALID
 
 
 def test_diagnostics_validate_before_any_gpu_work(lib):

@@ -362,6 +362,55 @@ def test_subgroups_prefix_sharing_workload(torch, ora, which, decode_kernel):
     assert_close(got, ref, f"{which}, sub-groups")
 
 
+@pytest.mark.parametrize("kernel", ["tasks", "units"])
+def test_out_of_pool_page_in_late_task_flagged(torch, monkeypatch, kernel):
+    """A table entry outside the pool in the last prompt's suffix of the full
+    prefix-sharing workload.  Its tasks have the highest numbers, so the task
+    kernel hands them out after every warp's first one (their entries are
+    checked when first used, not when described).  The page is flagged
+    (PA_DEVERR_PAGE) and read by nothing; every row outside that prompt's
+    sub-group is bit-identical to the call without the bad entry."""
+    import bench
+    monkeypatch.setenv("PA_DECODE_TASKS", "1" if kernel == "tasks" else "0")
+    plan, bt, ctx, slots, pairs = bench.prefix_sharing_setup(pa, None)
+    kp, vp, q, nk, nv = wl.prefix_sharing_values(plan)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    k_d, v_d = bf16_dev(kp, torch), bf16_dev(vp, torch)
+    if len(pairs):
+        pa.copy_blocks([k_d], [v_d], dev(np.asarray(pairs, np.int64).reshape(-1, 2)))
+    pa.reshape_and_cache(bf16_dev(nk, torch), bf16_dev(nv, torch), k_d, v_d, dev(slots))
+    S, B = len(ctx), plan.B
+    ss, sh = bench.prefix_sharing_subgroups(plan, bt, ctx)
+    npre = plan.prefix_len // B
+    gs, gp, pt = np.array([0, S], np.int32), np.array([plan.prefix_len], np.int32), bt[:1, :npre].copy()
+    # the last sub-group with at least two shared blocks past the prefix:
+    # members a .. b-1, its shared block j
+    k = max(i for i in range(len(sh)) if int(sh[i]) // B - npre >= 2)
+    assert k >= len(sh) - 8
+    a, b = int(ss[k]), int(ss[k + 1])
+    j = (npre + int(sh[k]) // B) // 2
+    assert npre <= j < int(sh[k]) // B
+    bad = bt.copy()
+    bad[a:b, j] = plan.num_blocks + 7
+    outs = []
+    for table in (bt, bad):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        res = pa.paged_attention_decode_shared_prefix(
+            bf16_dev(q, torch), k_d, v_d, dev(table), dev(ctx), dev(gs), dev(gp), dev(pt), None, err_flag=err,
+            subgroup_starts=dev(ss), subgroup_shared_lens=dev(sh), max_group_size=S,
+            max_prefix_len=plan.prefix_len, scale=1 / math.sqrt(plan.D), max_context_len=int(ctx.max()),
+            max_subgroup_size=int(np.diff(ss).max()))
+        torch.cuda.synchronize()
+        outs.append((bf16_host(res), int(err.item())))
+    (clean, e0), (got, e1) = outs
+    assert e0 == 0
+    assert e1 & pa.DEVERR_PAGE
+    keep = np.ones(S, bool)
+    keep[a:b] = False
+    assert np.array_equal(got[keep], clean[keep])
+    assert np.all(np.isfinite(to_f64(got[a:b])))
+
+
 def test_subgroup_guards(torch, decode_kernel):
     """A sub-group wider than max_subgroup_size promised (more query rows than
     the launch's MMA width) and sub-group starts outside the batch are refused
