@@ -274,6 +274,10 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   const int p0 = part * a.part_pages;
   const int np = GRP ? npages : max(0, min(npages - p0, a.part_pages));  // GRP units are never split
   const int32_t *bt_row = a.bt + (size_t)s * a.max_blocks + kp0 + p0;
+  // append: the new token's slot, loaded with the table entries (checked
+  // once the first gathers are out)
+  const bool app_unit = APP && part == nparts - 1 && np > 0;
+  const int64_t app_slot = app_unit ? __ldg(a.app_slots + s) : -1;
   for (int i = tid; i < np; i += NW * 32) {
     int pg;
     if constexpr (GRP) {  // shared pages from the first member's row, then each member's own
@@ -301,24 +305,6 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   }
   unit_sync<NW * 32>(bar);
 
-  // ---- append: the part holding the last page owns the new token.  Its slot
-  // must be the one of position ctx-1; any other slot (out of the pool or
-  // elsewhere in it) is refused, so nothing this launch reads is written.
-  constexpr int kRowChunks = D / 8;  // 16-byte chunks in one K or V row: lane c < 2 kRowChunks moves chunk c
-  static_assert(2 * kRowChunks <= 32, "one K and one V row fit a warp's lanes");
-  int app_row = -1;                  // the new token's row in the last page, for the warp streaming it
-  if (APP && part == nparts - 1 && np > 0) {
-    const int64_t slot = __ldg(a.app_slots + s);
-    const int pg = tbl[np - 1];
-    if (slot >= 0 && pg >= 0) {
-      if (slot == (int64_t)pg * B + (ctx - 1) % B) {
-        if (warp == (np - 1) % NW) app_row = (ctx - 1) % B;
-      } else if (tid == 0 && a.err) {
-        atomicOr(a.err, PA_DEVERR_SLOT);
-      }
-    }
-  }
-
   uint8_t *ring = smem + warp * NST * L::kSlotBytes;
   const int nmine = np > warp ? (np - warp + NW - 1) / NW : 0;
   const uint64_t pol = policy_evict_first();
@@ -341,6 +327,25 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
   };
   if (lane == 0)
     for (int i = 0; i < NST && i < nmine; ++i) issue(i);
+
+  // ---- append: the part holding the last page owns the new token.  Its slot
+  // must be the one of position ctx-1; any other slot (out of the pool or
+  // elsewhere in it) is refused, so nothing this launch reads is written.
+  // (Checked after the first gathers are issued: the token is written only
+  // below, and the streamed copy of its page is patched from the stage.)
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks in one K or V row: lane c < 2 kRowChunks moves chunk c
+  static_assert(2 * kRowChunks <= 32, "one K and one V row fit a warp's lanes");
+  int app_row = -1;                  // the new token's row in the last page, for the warp streaming it
+  if (app_unit) {
+    const int pg = tbl[np - 1];
+    if (app_slot >= 0 && pg >= 0) {
+      if (app_slot == (int64_t)pg * B + (ctx - 1) % B) {
+        if (warp == (np - 1) % NW) app_row = (ctx - 1) % B;
+      } else if (tid == 0 && a.err) {
+        atomicOr(a.err, PA_DEVERR_SLOT);
+      }
+    }
+  }
 
   // ---- Q^T fragments (MMA B operand): head 8nt + lane/4, d pairs
   uint32_t qf[NT][KS][2];
