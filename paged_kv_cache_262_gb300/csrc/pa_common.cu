@@ -68,6 +68,19 @@ bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_kv_halves_3d(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, 2};
+  cuuint64_t strides[2] = {256, 128};  // a row, a 64-column half (bytes)
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int validate_decode_desc(const pa_decode_desc *d) {
   if (!d) return PA_ERR_INVALID;
   if (d->num_seqs < 0 || d->num_q_heads <= 0 || d->num_kv_heads <= 0 || d->num_blocks <= 0 ||

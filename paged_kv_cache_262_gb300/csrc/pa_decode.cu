@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(NW * 32)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
-  decode_unit<D, B, NT, NW, NST, PRE, APP, GRP>(&tmK, &tmV, a, lin, threadIdx.x, smem, 0);
+  decode_unit<D, B, NT, NW, NST, PRE, APP, GRP, D == 128>(&tmK, &tmV, a, lin, threadIdx.x, smem, 0);
 }
 
 template <int D, int B, int NT, bool PRE, bool APP, bool GRP = false, int NST16 = 3>
@@ -144,9 +144,11 @@ int decode_launch(const pa_decode_desc *d, const void *q, const void *k_pool, co
   if (plan.total() > 0 && (!workspace || workspace_bytes < plan.total() || !aligned16(workspace)))
     return PA_ERR_WORKSPACE;
   const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
-  CUtensorMap tk, tv;
-  if (!encode_2d_bf16(&tk, k_pool, rows, d->head_dim, d->block_size, 64, true) ||
-      !encode_2d_bf16(&tv, v_pool, rows, d->head_dim, d->block_size, 64, true))
+  CUtensorMap tk, tv;  // head_dim 128: a page's two 64-column halves in one copy
+  if (d->head_dim == 128 ? !encode_kv_halves_3d(&tk, k_pool, rows, d->block_size) ||
+                               !encode_kv_halves_3d(&tv, v_pool, rows, d->block_size)
+                         : !encode_2d_bf16(&tk, k_pool, rows, d->head_dim, d->block_size, 64, true) ||
+                               !encode_2d_bf16(&tv, v_pool, rows, d->head_dim, d->block_size, 64, true))
     return PA_ERR_CUDA;
   DecodeArgs a;
   fill_decode_args(&a, d, plan, q, block_tables, context_lens, out, workspace, err_flag,

@@ -175,7 +175,7 @@ __device__ int seq_of_rank(int r, const int32_t *ctx, int S, int B, int max_bloc
 // unit's shared memory at `smem` (1024-aligned, DecodeSmem<...>::kBytes) and
 // barrier `bar` for its own NW * 32 threads.  The decode kernel runs one unit
 // per CTA; the mixed-step kernel runs several side by side in one CTA.
-template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP, bool GRP = false>
+template <int D, int B, int NT, int NW, int NST, bool PRE, bool APP, bool GRP = false, bool TMA3 = false>
 __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtensorMap *tmV, const DecodeArgs &a,
                                             int lin, int tid, uint8_t *smem, int bar) {
   using L = DecodeSmem<D, B, NW, NST>;
@@ -318,12 +318,17 @@ __device__ __forceinline__ void decode_unit(const CUtensorMap *tmK, const CUtens
     }
     mbar_arrive_expect_tx(bar, L::kSlotBytes);
     const int row = (pg * a.Hkv + kvh) * B;
+    if constexpr (TMA3) {  // both halves in one copy (maps from encode_kv_halves_3d)
+      tma_load_3d_hint(slot, tmK, 0, row, 0, bar, pol);
+      tma_load_3d_hint(slot + L::kPageBytes, tmV, 0, row, 0, bar, pol);
+    } else {
 #pragma unroll
-    for (int h = 0; h < L::kHalves; ++h)
-      tma_load_2d_hint(slot + h * L::kBoxBytes, tmK, h * 64, row, bar, pol);
+      for (int h = 0; h < L::kHalves; ++h)
+        tma_load_2d_hint(slot + h * L::kBoxBytes, tmK, h * 64, row, bar, pol);
 #pragma unroll
-    for (int h = 0; h < L::kHalves; ++h)
-      tma_load_2d_hint(slot + L::kPageBytes + h * L::kBoxBytes, tmV, h * 64, row, bar, pol);
+      for (int h = 0; h < L::kHalves; ++h)
+        tma_load_2d_hint(slot + L::kPageBytes + h * L::kBoxBytes, tmV, h * 64, row, bar, pol);
+    }
   };
   if (lane == 0)
     for (int i = 0; i < NST && i < nmine; ++i) issue(i);

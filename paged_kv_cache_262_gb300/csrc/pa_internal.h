@@ -18,6 +18,11 @@ int current_sm_count();
 // Returns false when the driver encoder is unavailable or rejects the map.
 bool encode_2d_bf16(CUtensorMap *map, const void *base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows, uint32_t box_cols, bool swizzle128);
+// K or V pool rows of 128 bf16 as (64 columns, row, half): one box of
+// box_rows rows and both 64-column halves lands as the two halves one after
+// the other, each box_rows x 128 bytes, 128-byte swizzled -- the layout two
+// 64-column 2-D boxes give, in one copy.
+bool encode_kv_halves_3d(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
