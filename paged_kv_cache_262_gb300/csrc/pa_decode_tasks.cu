@@ -402,10 +402,8 @@ __global__ void __launch_bounds__(W * 32, 1)
         mbar_arrive_expect_tx(bar, L::kSlotBytes);
         uint8_t *dst = ring + slot * L::kSlotBytes;
         const int row = (pg * a.Hkv + kvh) * B;
-        tma_load_2d_hint(dst, &tmK, 0, row, bar, pol);
-        tma_load_2d_hint(dst + L::kBoxBytes, &tmK, 64, row, bar, pol);
-        tma_load_2d_hint(dst + L::kPageBytes, &tmV, 0, row, bar, pol);
-        tma_load_2d_hint(dst + L::kPageBytes + L::kBoxBytes, &tmV, 64, row, bar, pol);
+        tma_load_3d_hint(dst, &tmK, 0, row, 0, bar, pol);  // both 64-column halves
+        tma_load_3d_hint(dst + L::kPageBytes, &tmV, 0, row, 0, bar, pol);
       }
     }
     ++issued;
@@ -839,8 +837,8 @@ int decode_tasks_launch(const pa_decode_desc *d, const void *q, const void *k_po
   if (sms <= 0) return PA_ERR_CUDA;
   const uint64_t nrows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
   CUtensorMap tk, tv;
-  if (!encode_2d_bf16(&tk, k_pool, nrows, kTD, d->block_size, 64, true) ||
-      !encode_2d_bf16(&tv, v_pool, nrows, kTD, d->block_size, 64, true))
+  if (!encode_kv_halves_3d(&tk, k_pool, nrows, d->block_size) ||
+      !encode_kv_halves_3d(&tv, v_pool, nrows, d->block_size))
     return PA_ERR_CUDA;
   const size_t R = (size_t)d->num_seqs * d->num_q_heads;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
