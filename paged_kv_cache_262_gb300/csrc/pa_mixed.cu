@@ -66,7 +66,10 @@ struct MixedPlan {
 template <int B, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     mixed_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmK3, const __grid_constant__ CUtensorMap tmV3,
                  const PrefillArgs pf, const DecodeArgs dc, const MixedPlan m) {
+  // tmK / tmV: 64-column boxes (prefill tiles); tmK3 / tmV3: a page's two
+  // halves in one copy (decode units)
   using M = MixedSmem<B>;
   constexpr int NT = G <= 8 ? 1 : 2;
   extern __shared__ uint8_t smem_raw[];
@@ -89,8 +92,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = threadIdx.x >> 7;
     const int lin = before * kUnitsPerCta + sub;
     if (lin < m.decode_units)
-      decode_unit<128, B, NT, 4, M::kDecodeStages, false, false>(&tmK, &tmV, dc, lin, threadIdx.x & 127,
-                                                                 smem + sub * M::kUnitStride, 1 + sub);
+      decode_unit<128, B, NT, 4, M::kDecodeStages, false, false, false, true>(
+          &tmK3, &tmV3, dc, lin, threadIdx.x & 127, smem + sub * M::kUnitStride, 1 + sub);
     return;
   }
   const int p = b - before;  // prefill CTA number, in the prefill kernel's launch order
@@ -99,8 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int B, int G>
-int launch_mixed(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &pf, const DecodeArgs &dc,
-                 const MixedPlan &m, cudaStream_t st) {
+int launch_mixed(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk3, const CUtensorMap &tv3,
+                 const PrefillArgs &pf, const DecodeArgs &dc, const MixedPlan &m, cudaStream_t st) {
   using M = MixedSmem<B>;
   auto kern = mixed_kernel<B, G>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, M::kBytes) != cudaSuccess)
@@ -108,19 +111,19 @@ int launch_mixed(const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PA_ERR_CUDA;
   if (fa.numRegs < kRegsLaunch) return PA_ERR_UNSUPPORTED;  // the prefill register split would not fit
-  kern<<<m.n_prefill + m.n_decode, kThreads, M::kBytes, st>>>(tk, tv, pf, dc, m);
+  kern<<<m.n_prefill + m.n_decode, kThreads, M::kBytes, st>>>(tk, tv, tk3, tv3, pf, dc, m);
   return launch_status(cudaGetLastError());
 }
 
 template <int B>
-int dispatch_mixed(int G, const CUtensorMap &tk, const CUtensorMap &tv, const PrefillArgs &pf, const DecodeArgs &dc,
-                   const MixedPlan &m, cudaStream_t st) {
+int dispatch_mixed(int G, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tk3, const CUtensorMap &tv3,
+                   const PrefillArgs &pf, const DecodeArgs &dc, const MixedPlan &m, cudaStream_t st) {
   switch (G) {
-    case 1: return launch_mixed<B, 1>(tk, tv, pf, dc, m, st);
-    case 2: return launch_mixed<B, 2>(tk, tv, pf, dc, m, st);
-    case 4: return launch_mixed<B, 4>(tk, tv, pf, dc, m, st);
-    case 8: return launch_mixed<B, 8>(tk, tv, pf, dc, m, st);
-    case 16: return launch_mixed<B, 16>(tk, tv, pf, dc, m, st);
+    case 1: return launch_mixed<B, 1>(tk, tv, tk3, tv3, pf, dc, m, st);
+    case 2: return launch_mixed<B, 2>(tk, tv, tk3, tv3, pf, dc, m, st);
+    case 4: return launch_mixed<B, 4>(tk, tv, tk3, tv3, pf, dc, m, st);
+    case 8: return launch_mixed<B, 8>(tk, tv, tk3, tv3, pf, dc, m, st);
+    case 16: return launch_mixed<B, 16>(tk, tv, tk3, tv3, pf, dc, m, st);
     default: return PA_ERR_UNSUPPORTED;
   }
 }
@@ -183,11 +186,13 @@ extern "C" int pa_paged_attention_mixed(const pa_decode_desc *prefill_desc, cons
   if (env && !strcmp(env, "decode-first")) m.order = kDecodeFirst;
   if (env && !strcmp(env, "prefill-first")) m.order = kPrefillFirst;
   const uint64_t rows = (uint64_t)d->num_blocks * d->num_kv_heads * d->block_size;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tk3, tv3;
   if (!encode_2d_bf16(&tk, k_pool, rows, 128, d->block_size, 64, true) ||
-      !encode_2d_bf16(&tv, v_pool, rows, 128, d->block_size, 64, true))
+      !encode_2d_bf16(&tv, v_pool, rows, 128, d->block_size, 64, true) ||
+      !encode_kv_halves_3d(&tk3, k_pool, rows, d->block_size) || !encode_kv_halves_3d(&tv3, v_pool, rows, d->block_size))
     return PA_ERR_CUDA;
   const int G = d->num_q_heads / d->num_kv_heads;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return d->block_size == 16 ? dispatch_mixed<16>(G, tk, tv, pf, dc, m, s) : dispatch_mixed<32>(G, tk, tv, pf, dc, m, s);
+  return d->block_size == 16 ? dispatch_mixed<16>(G, tk, tv, tk3, tv3, pf, dc, m, s)
+                             : dispatch_mixed<32>(G, tk, tv, tk3, tv3, pf, dc, m, s);
 }
